@@ -1,0 +1,461 @@
+"""Pins for the CPU oracle against facts that do not come from the oracle:
+the pages' printed example, closed forms, library routines, invariants and
+brute force. A plausible slip in the oracle (a dropped term, a wrong sign or
+index, a transposed operand) fails at least one test here."""
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from sparse_mixture_experts_69_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, val = line.split(None, 1)
+        vals[key] = float(val)
+    return vals
+
+
+# ------------------------------------------------------------ rounding
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(0)
+    v = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * 10.0,
+        np.array([128.5, 129.5, -128.5, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 3e38, -3.39e38,
+                  1e-39, -2e-40, 0.0, 2 ** -126, 2 ** -133, 1.5 * 2 ** -133], np.float32),
+    ])
+    ref = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    got = np.array([oracle.round_to(float(a), oracle.ROUND_BF16) for a in v])
+    np.testing.assert_array_equal(got, ref.astype(np.float64))
+
+
+def test_f32_rounding_matches_numpy():
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal(1000) * 1e3
+    got = np.array([oracle.round_to(float(a), oracle.ROUND_F32) for a in v])
+    np.testing.assert_array_equal(got, v.astype(np.float32).astype(np.float64))
+    assert oracle.round_to(0.1, oracle.ROUND_NONE) == 0.1
+
+
+# ------------------------------------------------------------ scalars
+
+def test_softplus_closed_forms():
+    assert oracle.softplus(0.0) == pytest.approx(math.log(2.0), abs=1e-15)
+    for u in [-50.0, -3.0, -0.5, 0.25, 2.0, 40.0, 700.0]:
+        assert oracle.softplus(u) == pytest.approx(float(np.logaddexp(0.0, u)), rel=1e-14)
+
+
+@pytest.mark.parametrize("u", [-6.0, -1.3, -0.2, 0.0, 0.7, 2.5, 9.0])
+def test_activations_closed_forms(u):
+    assert oracle.activation(oracle.RELU, u) == max(u, 0.0)
+    assert oracle.activation(oracle.GELU, u) == pytest.approx(u * scipy.special.ndtr(u),
+                                                              rel=1e-13, abs=1e-300)
+    assert oracle.activation(oracle.SWIGLU, u) == pytest.approx(u * scipy.special.expit(u),
+                                                                rel=1e-13, abs=1e-300)
+
+
+# ------------------------------------------------------------ softmax example
+
+def test_softmax_example_from_the_pages():
+    g = _golden("softmax_example.txt")
+    n = int(g["n_logits"])
+    logits = np.full(n, g["max_logit"] + g["gap"])
+    logits[0] = g["max_logit"]
+    exact = 1.0 / (1.0 + (n - 1) * math.exp(g["gap"]))  # closed form of the top score
+    p = oracle.softmax(logits)
+    assert p[0] == pytest.approx(exact, rel=1e-14)
+    assert p.sum() == pytest.approx(1.0, abs=1e-15)
+    # fp32 logits keep the gap: the error vanishes
+    p32 = oracle.softmax(logits.astype(np.float32).astype(np.float64))
+    assert abs(p32[0] - exact) / exact < 1e-6
+    # bf16 logits lose it: 128.5 rounds to 128, every score is 1/10
+    lb = np.array([oracle.round_to(v, oracle.ROUND_BF16) for v in logits])
+    pb = oracle.softmax(lb)
+    err = abs(pb[0] - exact) / exact
+    assert pb[0] == pytest.approx(1.0 / n, rel=1e-15)
+    assert 0.33 <= err <= 0.39, err
+    assert abs(err - g["printed_relative_error"]) < 0.01
+
+
+def test_softmax_subtracts_the_max():
+    # without the max subtraction exp(1000) overflows double
+    p = oracle.softmax([1000.0, 999.0])
+    assert p[0] == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+    p = oracle.softmax([-1000.0, -1001.0, -1002.0])
+    z = 1 + math.exp(-1) + math.exp(-2)
+    np.testing.assert_allclose(p, [1 / z, math.exp(-1) / z, math.exp(-2) / z], rtol=1e-14)
+
+
+# ------------------------------------------------------------ top-k, gates
+
+def _brute_topk(s, k):
+    """Lexicographically-first index set (sorted by descending score, then
+    index) among all k-subsets with the largest exact score sum."""
+    best, best_key = None, None
+    for sub in itertools.combinations(range(len(s)), k):
+        tot = sum(Fraction(float(s[i])) for i in sub)
+        if best_key is None or tot > best_key:
+            best, best_key = sub, tot
+    # order the chosen set: score descending, lower index first on ties
+    return sorted(best, key=lambda i: (-Fraction(float(s[i])), i))
+
+
+@pytest.mark.parametrize("E,k", [(2, 1), (4, 2), (5, 3), (6, 1), (6, 2), (6, 4), (6, 6)])
+def test_topk_brute_force(E, k):
+    rng = np.random.default_rng(E * 10 + k)
+    # small integer scores make ties frequent, so the tie rule is exercised
+    s = rng.integers(0, 3, size=(4, E)).astype(np.float32)
+    p = rng.random((4, E)).astype(np.float32)
+    ids, w = oracle.select(s, p, k)
+    for t in range(4):
+        assert list(ids[t]) == _brute_topk(s[t], k)
+        assert abs(w[t].sum() - 1.0) <= 1e-12
+        np.testing.assert_allclose(w[t], p[t, ids[t]] / p[t, ids[t]].astype(np.float64).sum(),
+                                   rtol=1e-15)
+    ids0, w0 = oracle.select(s, p, k, renorm=False)
+    np.testing.assert_array_equal(ids0, ids)
+    np.testing.assert_array_equal(w0, p[np.arange(4)[:, None], ids].astype(np.float64))
+
+
+def test_top1_renormalised_gate_is_one():
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal((50, 7)).astype(np.float32)
+    p = rng.random((50, 7)).astype(np.float32)
+    ids, w = oracle.select(s, p, 1)
+    assert np.all(w == 1.0)
+    np.testing.assert_array_equal(ids[:, 0], np.argmax(s, axis=1))
+
+
+# ------------------------------------------------------------ router
+
+def test_router_logit_orientation_and_offset():
+    # one-hot tokens read out rows of Wg[d,E]: z[t,:] = Wg[i_t,:] + offset
+    d, E = 5, 4
+    Wg = np.arange(d * E, dtype=np.float32).reshape(d, E) / 7.0
+    off = np.array([0.5, -1.0, 0.0, 2.0], np.float32)
+    x = np.eye(d, dtype=np.float32)[[3, 0, 4]] * 2.0
+    r = oracle.router(x, Wg, 2, offset=off)
+    np.testing.assert_allclose(r["z"], 2.0 * Wg[[3, 0, 4]].astype(np.float64) + off, rtol=1e-15)
+    np.testing.assert_allclose(r["H"], r["z"], rtol=0)
+
+
+def test_router_noise_terms():
+    rng = np.random.default_rng(4)
+    T, d, E = 6, 8, 5
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = rng.standard_normal((d, E)).astype(np.float32)
+    # noise = 0 gives the plain router exactly
+    r0 = oracle.router(x, Wg, 2)
+    rz = oracle.router(x, Wg, 2, Wnoise=rng.standard_normal((d, E)).astype(np.float32),
+                       noise=np.zeros((T, E), np.float32))
+    for key in ("z", "H", "p", "ids", "w"):
+        np.testing.assert_array_equal(r0[key], rz[key])
+    # Wnoise = 0: softplus(0) = ln 2, so H = z + noise * ln 2
+    noise = rng.standard_normal((T, E)).astype(np.float32)
+    rn = oracle.router(x, Wg, 2, Wnoise=np.zeros((d, E), np.float32), noise=noise)
+    np.testing.assert_allclose(rn["H"], r0["z"] + noise.astype(np.float64) * math.log(2.0),
+                               rtol=1e-14, atol=1e-14)
+    # one-hot x with Wnoise column values u: H = z + n * log(1 + e^u)
+    u = np.array([-2.0, 0.0, 1.5, 30.0, -30.0], np.float32)
+    Wn = np.zeros((d, E), np.float32)
+    Wn[0] = u
+    x1 = np.zeros((1, d), np.float32)
+    x1[0, 0] = 1.0
+    n1 = np.full((1, E), 0.5, np.float32)
+    r1 = oracle.router(x1, np.zeros((d, E), np.float32), 1, Wnoise=Wn, noise=n1)
+    np.testing.assert_allclose(r1["H"][0], 0.5 * np.logaddexp(0.0, u.astype(np.float64)),
+                               rtol=1e-14)
+
+
+def test_router_probs_are_softmax_of_H_and_selection_bias():
+    rng = np.random.default_rng(5)
+    T, d, E, k = 9, 16, 12, 3
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = (0.1 * rng.standard_normal((d, E))).astype(np.float32)
+    r = oracle.router(x, Wg, k)
+    np.testing.assert_allclose(r["p"], scipy.special.softmax(r["H"], axis=1), rtol=1e-13)
+    np.testing.assert_array_equal(r["s"], r["H"])
+    # a large bias decides the selection, but the gates stay the unbiased p
+    bias = np.linspace(1.0, 0.0, E).astype(np.float32)[::-1].copy()  # expert E-1 largest
+    rb = oracle.router(x, Wg, k, bias=bias)
+    np.testing.assert_array_equal(rb["ids"], np.tile(np.arange(E - 1, E - 1 - k, -1), (T, 1)))
+    np.testing.assert_allclose(rb["s"], rb["p"] + bias.astype(np.float64), rtol=1e-15)
+    pk = np.take_along_axis(rb["p"], rb["ids"].astype(np.int64), axis=1)
+    np.testing.assert_allclose(rb["w"], pk / pk.sum(axis=1, keepdims=True), rtol=1e-14)
+
+
+# ------------------------------------------------------------ capacity
+
+def test_capacity_formula_values():
+    # capacity = tokens / experts * capacity factor (rounded up)
+    assert oracle.capacity_of(256, 8, 1.25) == 40
+    assert oracle.capacity_of(8192, 64, 1.0) == 128
+    assert oracle.capacity_of(64 * 7, 64, 1.0) == 7  # uniform load: capacity = mean load
+    assert oracle.capacity_of(10, 4, 1.0) == 3  # 2.5 rounds up
+    assert oracle.capacity_of(100, 8, 0.0) == 100  # no limit
+    assert oracle.capacity_of(100, 8, -1.0) == 100
+
+
+@pytest.mark.parametrize("T,E,k,C", [(37, 5, 2, 6), (64, 8, 1, 3), (50, 4, 4, 50), (1, 3, 2, 0),
+                                     (20, 1, 1, 7)])
+def test_capacity_invariants(T, E, k, C):
+    ids = np.stack([np.random.default_rng(T + t).permutation(E)[:k] for t in range(T)]).astype(np.int32)
+    ids[: T // 3] = ids[0]  # a burst of identical choices forces overflow
+    cap = oracle.capacity(ids, E, C)
+    counts, kept, offsets, slot = cap["counts"], cap["kept"], cap["offsets"], cap["slot"]
+    np.testing.assert_array_equal(counts, np.bincount(ids.ravel(), minlength=E))
+    np.testing.assert_array_equal(kept, np.minimum(counts, C))
+    assert offsets[0] == 0 and np.all(np.diff(offsets) == kept)
+    assert (slot >= 0).sum() + (slot < 0).sum() == T * k
+    assert (slot >= 0).sum() == kept.sum()
+    for e in range(E):
+        toks = [t for t in range(T) for j in range(k) if ids[t, j] == e]
+        rows = [slot[t, list(ids[t]).index(e)] for t in toks]
+        # the first C tokens (in token order) get rows offsets[e] .. offsets[e]+kept-1
+        assert rows[: kept[e]] == list(range(offsets[e], offsets[e] + kept[e]))
+        # exactly the last counts-C tokens are dropped
+        assert all(r == -1 for r in rows[kept[e]:])
+    for r, t in enumerate(cap["row_token"]):
+        assert r in slot[t]
+
+
+def test_dispatch_copies_rows():
+    rng = np.random.default_rng(6)
+    T, d, E, k = 11, 6, 4, 2
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    cap = oracle.capacity(ids, E, 4)
+    R = int(cap["offsets"][-1])
+    xp = oracle.dispatch(x, cap["slot"], R)
+    np.testing.assert_array_equal(xp, x[cap["row_token"]])
+
+
+# ------------------------------------------------------------ expert FFN
+
+@pytest.mark.parametrize("act", [oracle.RELU, oracle.GELU, oracle.SWIGLU])
+def test_expert_ffn_one_hot_structure(act):
+    # one nonzero per weight matrix pins which index is summed over
+    d, F = 6, 5
+    i, f, j = 4, 2, 1
+    a, b, c, xv = 0.75, -1.5, 0.625, 2.0  # exactly representable in fp32
+    F1 = 2 * F if act == oracle.SWIGLU else F
+    W1 = np.zeros((F1, d), np.float32)
+    W1[f, i] = a
+    if act == oracle.SWIGLU:
+        W1[F + f, i] = c
+    W2 = np.zeros((d, F), np.float32)
+    W2[j, f] = b
+    x = np.zeros((1, d), np.float32)
+    x[0, i] = xv
+    O = oracle.expert_ffn(x, W1, W2, act)
+    u = a * xv
+    if act == oracle.RELU:
+        h = max(u, 0.0)
+    elif act == oracle.GELU:
+        h = u * scipy.special.ndtr(u)
+    else:
+        h = u * scipy.special.expit(u) * (c * xv)
+    expect = np.zeros(d)
+    expect[j] = b * h
+    np.testing.assert_allclose(O[0], expect, rtol=1e-14, atol=0)
+    # the transposed reading (W1[i,f]) would read zero here
+    assert O[0, j] != 0.0
+
+
+def test_expert_ffn_storage_rounding():
+    d, F = 4, 3
+    W1 = np.zeros((F, d), np.float32)
+    W1[0, 0] = 1.0
+    W2 = np.zeros((d, F), np.float32)
+    W2[2, 0] = 1.0
+    x = np.zeros((1, d), np.float32)
+    x[0, 0] = 1.0 + 2 ** -9 + 2 ** -12  # not a bf16 value
+    O = oracle.expert_ffn(x, W1, W2, oracle.RELU, oracle.ROUND_BF16)
+    assert O[0, 2] == float(torch.tensor(float(x[0, 0])).to(torch.bfloat16))
+    O32 = oracle.expert_ffn(x, W1, W2, oracle.RELU, oracle.ROUND_NONE)
+    assert O32[0, 2] == float(x[0, 0])
+
+
+def test_expert_ffn_linear_in_second_layer():
+    rng = np.random.default_rng(7)
+    n, d, F = 3, 8, 6
+    X = rng.standard_normal((n, d)).astype(np.float32)
+    W1 = rng.standard_normal((F, d)).astype(np.float32)
+    W2 = rng.standard_normal((d, F)).astype(np.float32)
+    O1 = oracle.expert_ffn(X, W1, W2, oracle.GELU)
+    O2 = oracle.expert_ffn(X, W1, 2 * W2, oracle.GELU)
+    np.testing.assert_allclose(O2, 2 * O1, rtol=1e-14)
+    # ReLU with all pre-activations positive is linear: o = W2 W1 x
+    Xp = np.abs(X)
+    W1p = np.abs(W1)
+    O3 = oracle.expert_ffn(Xp, W1p, W2, oracle.RELU)
+    np.testing.assert_allclose(O3, (Xp.astype(np.float64) @ W1p.T.astype(np.float64)) @ W2.T.astype(np.float64),
+                               rtol=1e-12)
+
+
+# ------------------------------------------------------------ combine
+
+def test_combine_drops_and_shared():
+    n, k, d, S = 3, 2, 4, 2
+    O = np.arange(n * k * d, dtype=np.float64).reshape(n, k, d)
+    Os = np.ones((S, n, d))
+    w = np.array([[0.25, 0.75], [1.0, 0.0], [0.5, 0.5]])
+    slot = np.array([[0, 1], [-1, 2], [-1, -1]], np.int32)
+    y = oracle.combine(w, slot, O, Os)
+    np.testing.assert_array_equal(y[0], 0.25 * O[0, 0] + 0.75 * O[0, 1] + 2.0)
+    np.testing.assert_array_equal(y[1], 0.0 * O[1, 1] + 2.0)  # dropped rank 0: gate not renormalised
+    np.testing.assert_array_equal(y[2], np.full(d, 2.0))  # all dropped: shared only
+
+
+# ------------------------------------------------------------ whole layer
+
+def _layer(x, Wg, W1, W2, k, C, act, renorm=True):
+    r = oracle.router(x, Wg, k, renorm=renorm)
+    E = Wg.shape[1]
+    cap = oracle.capacity(r["ids"], E, C)
+    O, _ = oracle.ffn_for_tokens(x, list(range(x.shape[0])), r["ids"], cap["slot"],
+                                 lambda e: W1[e], lambda e: W2[e], act, oracle.ROUND_NONE)
+    return r, cap, oracle.combine(r["w"], cap["slot"], O)
+
+
+@pytest.mark.parametrize("act", [oracle.GELU, oracle.SWIGLU])
+def test_dense_mixture_at_k_equals_E(act):
+    """Dropless, k = E, renormalised: the sparse layer is the dense mixture
+    y = sum_i G(x)_i E_i(x) over all experts ("MoE notes", expert selection)."""
+    rng = np.random.default_rng(8)
+    T, d, E, F = 7, 12, 5, 9
+    F1 = 2 * F if act == oracle.SWIGLU else F
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = (0.3 * rng.standard_normal((d, E))).astype(np.float32)
+    W1 = (0.3 * rng.standard_normal((E, F1, d))).astype(np.float32)
+    W2 = (0.3 * rng.standard_normal((E, d, F))).astype(np.float32)
+    r, cap, y = _layer(x, Wg, W1, W2, E, T, act)
+    dense = np.zeros((T, d))
+    p = scipy.special.softmax(x.astype(np.float64) @ Wg.astype(np.float64), axis=1)
+    for e in range(E):
+        dense += p[:, e:e + 1] * oracle.expert_ffn(x, W1[e], W2[e], act)
+    np.testing.assert_allclose(y, dense, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_brute_force_tiny():
+    """Every piece of the sparse layer against an exhaustive evaluation: for
+    each token, the subset of k experts with the largest total score, its
+    renormalised softmax gates, and capacity by token order."""
+    rng = np.random.default_rng(9)
+    T, d, E, F, k, C = 4, 6, 5, 7, 2, 2
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = rng.standard_normal((d, E)).astype(np.float32)
+    W1 = (0.5 * rng.standard_normal((E, F, d))).astype(np.float32)
+    W2 = (0.5 * rng.standard_normal((E, d, F))).astype(np.float32)
+    r, cap, y = _layer(x, Wg, W1, W2, k, C, oracle.RELU)
+    used = np.zeros(E, int)
+    for t in range(T):
+        logits = [float(sum(Fraction(float(x[t, i])) * Fraction(float(Wg[i, e])) for i in range(d)))
+                  for e in range(E)]
+        chosen = _brute_topk(np.array(logits), k)
+        assert list(r["ids"][t]) == chosen
+        p = np.exp(np.array(logits) - max(logits))
+        p /= p.sum()
+        g = p[chosen] / p[chosen].sum()
+        expect = np.zeros(d)
+        for j, e in enumerate(chosen):
+            if used[e] < C:
+                h = np.maximum(W1[e].astype(np.float64) @ x[t].astype(np.float64), 0.0)
+                expect += g[j] * (W2[e].astype(np.float64) @ h)
+            used[e] += 1
+        np.testing.assert_allclose(y[t], expect, rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------------ statistics
+
+def test_aux_is_one_under_uniform_routing():
+    """Uniform f and P give the minimum E * sum f P = 1 (Switch aux loss)."""
+    T, E, k = 48, 6, 2
+    base = np.array([3.0, 1.0, 0.5, 0.2, -1.0, -2.0], np.float32)
+    H = np.stack([np.roll(base, t % E) for t in range(T)])
+    p = scipy.special.softmax(H.astype(np.float64), axis=1).astype(np.float32)
+    ids, w = oracle.select(H, p, k)
+    st = oracle.aux_stats(p, ids, w.astype(np.float32), E, w_imp=0.01)
+    np.testing.assert_allclose(st["f"], 1.0 / E, rtol=1e-15)
+    assert st["aux"] == pytest.approx(1.0, abs=1e-6)
+    assert st["cv2"] == pytest.approx(0.0, abs=1e-12)
+    assert st["L_imp"] == pytest.approx(0.0, abs=1e-14)
+
+
+def test_aux_uniform_f_gives_sum_P():
+    rng = np.random.default_rng(10)
+    T, E = 40, 4
+    p = scipy.special.softmax(rng.standard_normal((T, E)), axis=1).astype(np.float32)
+    ids = (np.arange(T) % E).reshape(T, 1).astype(np.int32)
+    st = oracle.aux_stats(p, ids, np.ones((T, 1), np.float32), E)
+    assert st["aux"] == pytest.approx(p.astype(np.float64).sum(axis=1).mean(), rel=1e-12)
+    assert st["aux"] == pytest.approx(1.0, abs=1e-6)
+
+
+def test_aux_collapsed_routing_closed_forms():
+    # every token on expert 0 with p one-hot: aux = E; importance [T,0..0]:
+    # CV^2 = E - 1 (population variance)
+    T, E = 30, 5
+    p = np.zeros((T, E), np.float32)
+    p[:, 0] = 1.0
+    ids = np.zeros((T, 1), np.int32)
+    st = oracle.aux_stats(p, ids, np.ones((T, 1), np.float32), E, w_imp=0.5)
+    assert st["aux"] == pytest.approx(E, rel=1e-15)
+    assert st["cv2"] == pytest.approx(E - 1, rel=1e-14)
+    assert st["L_imp"] == pytest.approx(0.5 * (E - 1), rel=1e-14)
+    np.testing.assert_array_equal(st["I"], [T, 0, 0, 0, 0])
+
+
+def test_bias_update_signs():
+    T, k, E = 12, 2, 4  # mean load 6
+    counts = np.array([9, 6, 3, 6], np.int32)
+    b = np.array([0.25, -0.5, 0.125, 1e-8], np.float32)
+    out = oracle.bias_update(counts, b, T, k, 1e-3)
+    g = np.float32(1e-3)
+    np.testing.assert_array_equal(out, [b[0] - g, b[1], b[2] + g, b[3]])
+    # non-integral mean load: 7 * 2 / 4 = 3.5
+    out2 = oracle.bias_update(np.array([4, 3, 4, 3], np.int32), np.zeros(4, np.float32), 7, 2, 0.5)
+    np.testing.assert_array_equal(out2, [-0.5, 0.5, -0.5, 0.5])
+
+
+# ------------------------------------------------------------ generator
+
+def test_synth_deterministic_and_sliceable():
+    a = synth.normal((64, 33), seed=0, tid=100)
+    b = synth.normal((64, 33), seed=0, tid=100)
+    torch.testing.assert_close(a, b, rtol=0, atol=0)
+    tail = synth.normal((10, 33), seed=0, tid=100, offset=54 * 33)
+    torch.testing.assert_close(a[54:], tail, rtol=0, atol=0)
+    assert not torch.equal(a, synth.normal((64, 33), seed=1, tid=100))
+    v = synth.normal((200000,), seed=3, tid=101, std=0.02).double()
+    assert abs(v.mean().item()) < 3e-4 and abs(v.std().item() / 0.02 - 1) < 0.01
+    u = synth.uniform((100000,), seed=3, tid=102, lo=-0.1, hi=0.1).double()
+    assert u.min() >= -0.1 and u.max() < 0.1 and abs(u.mean().item()) < 2e-3
+
+
+def test_importance_sums_the_gates():
+    # Importance(X) = sum over the batch of the sparse gates G(x): hand-computed
+    ids = np.array([[0, 2], [2, 1], [0, 1]], np.int32)
+    w = np.array([[0.75, 0.25], [0.5, 0.5], [0.125, 0.875]], np.float32)
+    p = np.full((3, 3), 1.0 / 3.0, np.float32)
+    st = oracle.aux_stats(p, ids, w, 3, w_imp=2.0)
+    np.testing.assert_array_equal(st["I"], [0.875, 1.375, 0.75])
+    mean = 3.0 / 3.0
+    var = ((0.875 - mean) ** 2 + (1.375 - mean) ** 2 + (0.75 - mean) ** 2) / 3.0
+    assert st["cv2"] == pytest.approx(var / mean ** 2, rel=1e-14)
+    assert st["L_imp"] == pytest.approx(2.0 * var / mean ** 2, rel=1e-14)
+    np.testing.assert_allclose(st["f"], [2 / 6, 2 / 6, 2 / 6], rtol=1e-15)
