@@ -1,0 +1,480 @@
+"""Benchmark of the sparse-MoE layer forward pass on one B300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload switch]
+    python bench.py --impl reference ...     # the CPU oracle, timed on host cores
+
+One step = one moe_layer_fwd (router -> capacity/dispatch -> grouped expert
+GEMMs -> combine -> statistics; plus the loss-free bias update where the
+workload has one) over one batch of T synthetic tokens. Prints one JSON line.
+
+value      tokens/s over all ranks, inputs already resident in HBM
+e2e        the same call with the step's inputs copied from pinned host memory
+           and the result (y, aux) copied back inside the timed region
+roofline   the grouped expert GEMM (the dominant kernel): algorithmic bytes
+           (weights of touched experts + activations in/out) per launch over its
+           CUDA-event duration, against the measured HBM copy bandwidth
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "MoE-layer fwd tokens/s on 1 B300; grouped-GEMM TFLOP/s & HBM GB/s vs peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="switch")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+    a.steps = max(a.steps, 1)
+    return a
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def workload_desc(wl):
+    c = wl.cfg
+    act = {0: "ReLU", 1: "GELU", 2: "SwiGLU"}[c.act]
+    s = (f"{wl.name}: T={c.T} d={c.d_model} E={c.n_experts} k={c.top_k} F={c.d_ff} {act}"
+         f" shared={c.n_shared} cf={c.capacity_factor:g}")
+    if wl.noisy:
+        s += " noisy-KeepTopK"
+    if wl.zipf_s:
+        s += f" zipf-offset={wl.zipf_s}"
+    if wl.sel_bias:
+        s += f" sel-bias+update(rate={wl.bias_rate:g})"
+    return s
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "group_table.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_mixture_experts_69_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """dram bytes per grouped-GEMM launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    rec = d.get(workload)
+    if not rec or rec.get("source_hash") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- CPU oracle leg
+
+class OracleInputs:
+    """Host-side inputs for the oracle: the small tensors whole, expert weights
+    fetched per expert on first use (copied from the device, or generated on
+    the host with the same seeded generator) and cached as float32."""
+
+    def __init__(self, wl, inp=None):
+        import numpy as np
+
+        from sparse_mixture_experts_69_b300 import synth
+        from sparse_mixture_experts_69_b300.workloads import W_STD, make_inputs
+
+        self.wl, self._np, self._synth, self._std = wl, np, synth, W_STD
+        c = wl.cfg
+        if inp is None:  # host only: generate all but the expert weights
+            small = make_inputs(wl.with_(n_experts=c.n_experts), "cpu", experts=False)
+            self.inp, self.dev = small, None
+        else:
+            self.inp, self.dev = inp, inp["x"].device
+        self.small = {k: (None if v is None or k in ("W1", "W2", "W1s", "W2s") else v.cpu())
+                      for k, v in self.inp.items()}
+        self.cache = {}
+
+    def _get(self, key, tid, e, shape):
+        if (key, e) in self.cache:
+            return self.cache[(key, e)]
+        if self.dev is not None:
+            t = self.inp[key][e].float().cpu()
+        else:
+            import math
+            t = self._synth.normal(shape, self.wl.seed, tid, self._std, self.wl.cfg.torch_dtype,
+                                   "cpu", offset=e * math.prod(shape)).float()
+        a = self._np.ascontiguousarray(t.numpy(), dtype=self._np.float32)
+        self.cache[(key, e)] = a
+        return a
+
+    def W1(self, e):
+        c = self.wl.cfg
+        return self._get("W1", 10, e, (c.F1, c.d_model))
+
+    def W2(self, e):
+        c = self.wl.cfg
+        return self._get("W2", 11, e, (c.d_model, c.d_ff))
+
+    def W1s(self, s):
+        c = self.wl.cfg
+        return self._get("W1s", 12, s, (c.F1, c.d_model))
+
+    def W2s(self, s):
+        c = self.wl.cfg
+        return self._get("W2s", 13, s, (c.d_model, c.d_ff))
+
+
+def oracle_tokens_per_s(oi, n_tok, seed=5):
+    """Time the oracle (as it stands) on n_tok sampled tokens of the workload:
+    router, then every expert FFN those tokens chose, then combine. Expert
+    weights are fetched before the clock starts."""
+    import numpy as np
+
+    import oracle
+    from sparse_mixture_experts_69_b300 import synth
+
+    wl = oi.wl
+    c = wl.cfg
+    tok = sorted(set(synth.randint((n_tok,), seed, 400, c.T).tolist()))
+    tt = torch.as_tensor(tok)
+    g = lambda n: oi.small[n]
+    rows = lambda n: None if oi.small[n] is None else oi.small[n][tt]
+    rd = oracle.ROUND_BF16 if c.dtype == 1 else oracle.ROUND_F32
+    slot = np.zeros((len(tok), c.top_k), np.int32)
+    # routing decides which experts are needed: fetch them untimed, then time it all
+    r0 = oracle.router(rows("x"), g("Wg"), c.top_k, Wnoise=g("Wnoise"), noise=rows("noise"),
+                       offset=g("logit_offset"), bias=g("sel_bias"), renorm=bool(c.renorm_topk))
+    for e in sorted(set(r0["ids"].ravel().tolist())):
+        oi.W1(e), oi.W2(e)
+    for s in range(c.n_shared):
+        oi.W1s(s), oi.W2s(s)
+    x_rows = rows("x")
+    t0 = time.perf_counter()
+    r = oracle.router(x_rows, g("Wg"), c.top_k, Wnoise=g("Wnoise"), noise=rows("noise"),
+                      offset=g("logit_offset"), bias=g("sel_bias"), renorm=bool(c.renorm_topk))
+    O, Os = oracle.ffn_for_tokens(x_rows, list(range(len(tok))), r["ids"], slot, oi.W1, oi.W2,
+                                  c.act, rd, c.n_shared, oi.W1s, oi.W2s)
+    oracle.combine(r["w"], slot, O, Os, rd)
+    dt = time.perf_counter() - t0
+    return len(tok), dt
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    import oracle
+    oracle.build()
+    oi = OracleInputs(wl, inp)
+    n, dt = oracle_tokens_per_s(oi, 16)
+    per_tok = dt / max(n, 1)
+    n2 = int(max(16, min(wl.cfg.T, budget_s / max(per_tok, 1e-6))))
+    n2, dt2 = oracle_tokens_per_s(oi, n2, seed=6)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": n2 / dt2, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n2} sampled tokens of the {wl.name} workload (router + chosen expert "
+                      f"FFNs + combine, plain double loops, OpenMP over rows); {dt2:.1f} s"}
+
+
+def run_reference(a):
+    """--impl reference: the CPU oracle, timed on the host cores, same workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from sparse_mixture_experts_69_b300.workloads import WORKLOADS
+    import oracle
+    oracle.build()
+    wl = WORKLOADS[a.workload]
+    oi = OracleInputs(wl, None)
+    # per-step sample sized so warm-up + steps take about two minutes of compute
+    n, dt = oracle_tokens_per_s(oi, 4)
+    per_tok = dt / max(n, 1)
+    n_step = int(max(1, min(256, 120.0 / (a.steps + a.warmup) / max(per_tok, 1e-6))))
+    for i in range(a.warmup):
+        oracle_tokens_per_s(oi, n_step, seed=10 + i)
+    done, total = 0, 0.0
+    for i in range(a.steps):
+        m, dt = oracle_tokens_per_s(oi, n_step, seed=1000 + i)
+        done += m
+        total += dt
+    value = done / total
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": 1e3 * total / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(wl), "global_batch": wl.cfg.T,
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"{n_step} sampled tokens per step of the {wl.name} "
+                                       "workload (router + chosen expert FFNs + combine)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        return run_reference(a)
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from sparse_mixture_experts_69_b300 import moe
+    from sparse_mixture_experts_69_b300.workloads import WORKLOADS, make_inputs
+
+    wl = WORKLOADS[a.workload].with_(seed=rank)
+    c = wl.cfg
+    T, E, k, d = c.T, c.n_experts, c.top_k, c.d_model
+    inp = make_inputs(wl, dev)
+    ws = moe.workspace(c, dev)
+    y = torch.empty((T, d), dtype=c.torch_dtype, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    aux_vecs = torch.empty((3, E), dtype=torch.float32, device=dev)
+    out3 = torch.empty(3, dtype=torch.float32, device=dev)
+    bias = inp["sel_bias"].clone() if inp["sel_bias"] is not None else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x, noise):
+        moe.moe_layer_fwd(c, x, inp["Wg"], inp["Wnoise"], noise, inp["logit_offset"], bias,
+                          inp["W1"], inp["W2"], inp["W1s"], inp["W2s"], y, ids, w, counts,
+                          aux_vecs, out3, ws, stream)
+        if wl.bias_rate:
+            moe.moe_bias_update(c, counts, bias, wl.bias_rate, stream)
+
+    def barrier():
+        if pg:
+            pg.barrier()
+
+    # ------------------------------------------------ device-resident timing
+    for _ in range(a.warmup):
+        step(inp["x"], inp["noise"])
+    st = moe.moe_read_device_error(c, ws)
+    if st != 0:
+        raise RuntimeError("device status after warm-up: " + moe.moe_status_string(st))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(a.steps):
+            step(inp["x"], inp["noise"])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = ms
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_max = float(t.item())
+    st = moe.moe_read_device_error(c, ws)
+    if st != 0:
+        raise RuntimeError("device status after timing: " + moe.moe_status_string(st))
+    value = world * T * a.steps / (ms_max / 1e3)
+
+    # ------------------------------------------------ per-stage split (same calls, stage APIs)
+    C, R_max = moe.moe_capacity(c)
+    logits = torch.empty((T, E), device=dev)
+    probs = torch.empty((T, E), device=dev)
+    kept = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, k), dtype=torch.int32, device=dev)
+    row_token = torch.empty(R_max, dtype=torch.int32, device=dev)
+    xp = torch.empty((R_max, d), dtype=c.torch_dtype, device=dev)
+    yp = torch.empty((R_max, d), dtype=c.torch_dtype, device=dev)
+    ys = torch.empty((c.n_shared, T, d), dtype=c.torch_dtype, device=dev) if c.n_shared else None
+    fP = torch.empty((3, E), device=dev)
+    n_split = max(10, min(200, a.steps // 10))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_split)]
+    for i in range(n_split + 3):
+        e = evs[i - 3] if i >= 3 else None
+        if e: e[0].record(stream)
+        moe.moe_route(c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"],
+                      bias, logits, probs, None, ids, w, 0, ws, stream)
+        if e: e[1].record(stream)
+        moe.moe_dispatch(c, inp["x"], ids, counts, kept, offsets, slot, xp, row_token, ws, stream)
+        if e: e[2].record(stream)
+        moe.moe_expert_ffn(c, xp, offsets, inp["W1"], inp["W2"], inp["x"], inp["W1s"], inp["W2s"],
+                           yp, ys, ws, stream)
+        if e: e[3].record(stream)
+        moe.moe_combine(c, yp, slot, w, ys, y, ws, stream)
+        if e: e[4].record(stream)
+        moe.moe_aux_stats(c, probs, ids, w, fP[0], fP[1], fP[2], out3, ws, stream)
+        if e: e[5].record(stream)
+    torch.cuda.synchronize()
+    names = ["route", "dispatch", "expert_ffn", "combine", "aux"]
+    stage_ms = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
+                for j, n in enumerate(names)}
+
+    # algorithmic work of the expert FFN (two grouped-GEMM launches)
+    kept_h = kept.cpu()
+    R = int(kept_h.sum())
+    touched = int((kept_h > 0).sum())
+    es = 2 if c.dtype == 1 else 4
+    F, F1, S = c.d_ff, c.F1, c.n_shared
+    w_bytes = (touched + S) * (F1 * d + d * F) * es
+    act_bytes = (R + S * T) * (d + F + F + d) * es  # up: read x rows, write h; down: read h, write y
+    ffn_bytes = w_bytes + act_bytes
+    flops = 2 * (R + S * T) * d * (F1 + F)
+    ffn_ms = stage_ms["expert_ffn"]
+    pk, pk_kind = peaks()
+    hbm = pk["hbm_gbs"]
+    achieved_gbs = ffn_bytes / (ffn_ms / 1e3) / 1e9
+    tflops = flops / (ffn_ms / 1e3) / 1e12
+    traffic = ncu_traffic(a.workload)
+
+    # ------------------------------------------------ end to end (host buffers)
+    x_host = inp["x"].cpu().pin_memory()
+    noise_host = inp["noise"].cpu().pin_memory() if inp["noise"] is not None else None
+    y_host = torch.empty_like(y, device="cpu").pin_memory()
+    o3_host = torch.empty(3, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    noise_dev = torch.empty_like(inp["noise"]) if noise_host is not None else None
+    K2 = max(10, a.steps // 4)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        if noise_host is not None:
+            noise_dev.copy_(noise_host, non_blocking=True)
+        step(x_dev, noise_dev)
+        y_host.copy_(y, non_blocking=True)
+        o3_host.copy_(out3, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(K2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    barrier()
+    if pg:
+        t = torch.tensor([e2e_s], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = x_host.numel() * x_host.element_size() + (
+        noise_host.numel() * 4 if noise_host is not None else 0)
+    d2h = y_host.numel() * y_host.element_size() + 12
+    e2e_value = world * T * K2 / e2e_s
+
+    launches_per_step = (3 if c.dtype == 1 else 2) + 4 + 2 + 1 + 2 + (1 if wl.bias_rate else 0)
+
+    if rank != 0:
+        return 0
+    cb = None
+    if not a.no_cpu_baseline and world == 1:
+        cb = cpu_baseline(wl, inp)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_max / a.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if c.dtype == 1 else "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "global_batch": world * T,
+                   "seq_len": None, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: each step streams "
+                         f"{w_bytes / 1e9:.2f} GB of expert weights through the 126 MB L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm, "traffic": traffic,
+                     "kernel": "grouped_gemm_tc_kernel (expert FFN: up + down launches)",
+                     "algorithmic_bytes_per_launch": ffn_bytes / 2, "peak_kind": pk_kind,
+                     "tflops": tflops,
+                     "tflops_frac_of_bf16_peak": tflops / pk["bf16_tflops"]},
+        "cpu_baseline": cb,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": K2},
+        "gpu_launches": launches_per_step * a.steps,
+        "clocks": clocks,
+        "stage_ms": stage_ms,
+        "rows_kept": R, "experts_touched": touched,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

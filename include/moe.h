@@ -1,0 +1,216 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the forward pass of a sparse
+ * Mixture-of-Experts FFN layer on one NVIDIA B300 (sm_103a).
+ *
+ * The method (sources are the study-note pages this library follows):
+ *   router     "MoE notes" (chiang97912.github.io), sections Expert selection
+ *              and KeepTopK: logits x.Wg, optional trainable noise
+ *              H = x.Wg + StandardNormal() * Softplus(x.Wnoise), KeepTopK,
+ *              G(x) = Softmax(KeepTopK(H, k)).
+ *              heavensheep.xyz MoE notes, section Training: softmax with the
+ *              maximum subtracted, exponentials in fp32.
+ *              ld246.com MoE Q3: loss-free balance, a per-expert bias added to
+ *              the softmax scores for the Top-K choice only.
+ *   capacity   "MoE notes", section Expert capacity: capacity =
+ *              (tokens per batch / number of experts) * capacity factor;
+ *              mkbk-pku.cn MoE notes, load-balance section: a token beyond
+ *              capacity is dropped (its output is zero; the caller's residual
+ *              connection carries it).
+ *   dispatch   mkbk-pku.cn MoE notes, communication section: tokens bucketed
+ *              by expert and packed contiguously (here an in-HBM permutation).
+ *   experts    mkbk-pku.cn MoE notes, section on experts and the grouped-GEMM
+ *              optimisation: each expert is a two-layer FFN; all experts run as
+ *              one grouped GEMM.
+ *   combine    "MoE notes": y = sum_i G(x)_i E_i(x); shared experts
+ *              (ld246.com Q4, heavensheep.xyz) are always on, weight 1.
+ *   statistics heavensheep.xyz MoE notes, section Training (Switch aux loss
+ *              from f_i and P_i); "MoE notes", section Auxiliary loss
+ *              (Importance, CV, L_importance).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless stated; the caller allocates and
+ *     owns all memory, including the workspace `ws`. The library never
+ *     allocates, frees or synchronises, except moe_read_device_error.
+ *   - All work is enqueued on `stream` in order; functions return after
+ *     enqueueing. They hold no state between calls and are re-entrant as long
+ *     as concurrent calls use different workspaces.
+ *   - Layouts are row-major. "dtype" below is cfg->dtype: float32 or bf16
+ *     (raw 16-bit storage). Pointers passed to the library must be 16-byte
+ *     aligned; d_model and d_ff must be multiples of 8.
+ *   - Host-side argument errors return before anything is enqueued.
+ *     A failed launch returns MOE_ERR_CUDA. Conditions found on the device
+ *     (non-finite values, out-of-range ids, a barrier wait that ran out) are
+ *     recorded in the workspace status word and reported by
+ *     moe_read_device_error. Kernels never trap.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Same handle as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* bad size, NULL required pointer, k > E ...  */
+    MOE_ERR_UNSUPPORTED = 2, /* valid but not implemented (alignment, sizes) */
+    MOE_ERR_WORKSPACE = 3,   /* ws_bytes below moe_workspace_size          */
+    MOE_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed        */
+    MOE_ERR_NONFINITE = 5,   /* device: NaN/Inf in router scores or output  */
+    MOE_ERR_TIMEOUT = 6,     /* device: a pipeline wait exceeded its limit  */
+    MOE_ERR_DEVICE_ARG = 7   /* device: expert id / offsets out of range    */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_RELU = 0, MOE_GELU = 1, MOE_SWIGLU = 2 } moe_act;
+
+/* Problem statement of one MoE layer call. */
+typedef struct {
+    int32_t T;               /* tokens in the batch, >= 1                      */
+    int32_t d_model;         /* d, multiple of 8                               */
+    int32_t n_experts;       /* E routed experts, 1..1024                      */
+    int32_t top_k;           /* k, 1..min(E, 32)                               */
+    int32_t d_ff;            /* F, expert hidden size, multiple of 8           */
+    int32_t n_shared;        /* S always-on shared experts, 0..64              */
+    float capacity_factor;   /* C = ceil(T * cf / E); cf <= 0 means C = T      */
+    int32_t renorm_topk;     /* 1: gates p_j / sum_chosen p; 0: gates p_j      */
+    int32_t dtype;           /* moe_dtype of x, weights, h, expert outputs, y  */
+    int32_t act;             /* moe_act; SwiGLU = silu(gate) * up              */
+    float importance_weight; /* w in L_importance = w * CV^2                   */
+} moe_config;
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(moe_status status);
+
+/* Capacity C and the row bound R_max = min(T*k, E*C) of the expert-sorted
+ * buffers (xp, yp, row_token). Host only. */
+MOE_API moe_status moe_capacity(const moe_config* cfg, int32_t* capacity, int32_t* rows_max);
+
+/* Bytes of workspace any entry point below needs for this configuration.
+ * One workspace sized this way serves every entry point. Host only. */
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Zero the workspace status word (enqueued on stream). Call once on a new
+ * workspace before its first use. */
+MOE_API moe_status moe_workspace_reset(const moe_config* cfg, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream);
+
+/* Router ("MoE notes", Expert selection + KeepTopK; heavensheep.xyz softmax
+ * numerics; ld246.com Q3 selection bias).
+ *   x            [T,d] dtype
+ *   Wg           [d,E] dtype
+ *   Wnoise       [d,E] dtype or NULL   noisy router: H = z + noise*softplus(x.Wnoise)
+ *   noise        [T,E] float32 or NULL  standard-normal draws, supplied by the caller
+ *   logit_offset [E] float32 or NULL    added to the logits
+ *   sel_bias     [E] float32 or NULL    added to softmax p for the top-k choice only
+ *   logits  out  [T,E] float32          z = x.Wg (+ offset), fp32 accumulation
+ *   probs   out  [T,E] float32          p = softmax(H), max subtracted, fp32
+ *   sel_scores   [T,E] float32 or NULL  out: the scores top-k ranked (H, or p + bias)
+ *   topk_ids out [T,k] int32            descending score, lower index wins ties
+ *   topk_w   out [T,k] float32          gates from the unbiased p
+ * from_scores = 1 skips the logits: top-k is taken on the caller's sel_scores
+ * (input) and gates on the caller's probs (input); x, Wg, logits are unused. */
+MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* Wg,
+                             const void* Wnoise, const float* noise, const float* logit_offset,
+                             const float* sel_bias, float* logits, float* probs,
+                             float* sel_scores, int32_t* topk_ids, float* topk_w,
+                             int32_t from_scores, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Capacity and dispatch ("MoE notes", Expert capacity; mkbk-pku.cn MoE notes,
+ * bucketize + contiguous packing). Assignments are served in token order
+ * (within a token, in rank order); the first C of each expert are kept.
+ *   x         [T,d] dtype, topk_ids [T,k] int32 (distinct per token, in [0,E))
+ *   counts    out [E] int32    assignments per expert before the cap
+ *   kept      out [E] int32    min(counts, C)
+ *   offsets   out [E+1] int32  exclusive prefix sum of kept; R = offsets[E]
+ *   slot      out [T,k] int32  row of the assignment in xp, -1 if dropped
+ *   xp        out [R_max,d] dtype  xp[slot[t,j]] = x[t]; rows >= R untouched
+ *   row_token out [R_max] int32    token of each row < R */
+MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                                int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot,
+                                void* xp, int32_t* row_token, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+
+/* Expert FFNs as one grouped GEMM pair (mkbk-pku.cn MoE notes: experts, grouped
+ * GEMM). Rows offsets[e]..offsets[e+1]-1 of xp go through expert e:
+ *   ReLU/GELU: yp = act(xp W1[e]^T) W2[e]^T,   W1 [E,F,d]
+ *   SwiGLU   : yp = (silu(xp W1[e][0:F]^T) * (xp W1[e][F:2F]^T)) W2[e]^T,  W1 [E,2F,d]
+ *   W2 [E,d,F]. The hidden activations are stored in the workspace in dtype.
+ * Shared experts (S > 0) run the same way on all T rows of x:
+ *   W1s [S,F1,d], W2s [S,d,F], ys out [S,T,d]; x, W1s, W2s, ys may be NULL if S = 0.
+ *   yp out [R_max,d] dtype (rows >= offsets[E] untouched). */
+MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                                  const void* W1, const void* W2, const void* x,
+                                  const void* W1s, const void* W2s, void* yp, void* ys,
+                                  void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Combine back to token order ("MoE notes": y = sum_i G(x)_i E_i(x)):
+ *   y[t] = sum over j with slot[t,j] >= 0 of topk_w[t,j] * yp[slot[t,j]]
+ *        + sum_s ys[s,t]
+ * accumulated in fp32 in a fixed order (deterministic), stored in dtype.
+ * Dropped assignments add nothing and the gates are not renormalised.
+ *   yp [R_max,d], slot [T,k], topk_w [T,k], ys [S,T,d] or NULL, y out [T,d]. */
+MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot,
+                               const float* topk_w, const void* ys, void* y, void* ws,
+                               size_t ws_bytes, moe_stream_t stream);
+
+/* Load-balance statistics (heavensheep.xyz MoE notes, Switch aux loss;
+ * "MoE notes", Auxiliary loss):
+ *   f[e] = #{(t,j): topk_ids[t,j] = e} / (T k)     (before capacity)
+ *   P[e] = mean_t probs[t,e]
+ *   importance[e] = sum of topk_w over assignments to e
+ *   out3 = { aux = E * sum_e f[e] P[e],
+ *            cv2 = (population std of importance / its mean)^2,
+ *            L_imp = importance_weight * cv2 }
+ * f, P, importance: out [E] float32 or NULL; out3: out [3] float32.
+ * Reduction order is fixed (deterministic). */
+MOE_API moe_status moe_aux_stats(const moe_config* cfg, const float* probs,
+                                 const int32_t* topk_ids, const float* topk_w, float* f,
+                                 float* P, float* importance, float* out3, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+
+/* Loss-free bias update (heavensheep.xyz notes on DeepSeek-V3; ld246.com Q3):
+ *   bias[e] -= rate if counts[e] > T k / E;  += rate if below;  unchanged if equal.
+ * counts [E] int32 (from moe_dispatch), bias [E] float32 in/out. fp32 arithmetic. */
+MOE_API moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float* bias,
+                                   float rate, moe_stream_t stream);
+
+/* The whole layer: route -> dispatch -> expert FFN -> combine -> statistics.
+ * Inputs as in moe_route and moe_expert_ffn. Outputs:
+ *   y         [T,d] dtype
+ *   topk_ids  [T,k] int32 or NULL, topk_w [T,k] float32 or NULL
+ *   counts    [E] int32 or NULL (before capacity)
+ *   aux_vecs  [3,E] float32 or NULL: rows f, P, importance
+ *   out3      [3] float32 or NULL: aux, cv2, L_imp
+ * Intermediates (logits, probs, slots, xp, h, yp, ys) live in ws. */
+MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const void* Wg,
+                                 const void* Wnoise, const float* noise,
+                                 const float* logit_offset, const float* sel_bias,
+                                 const void* W1, const void* W2, const void* W1s,
+                                 const void* W2s, void* y, int32_t* topk_ids, float* topk_w,
+                                 int32_t* counts, float* aux_vecs, float* out3, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream`, read and clear the workspace status word, and map it
+ * to MOE_OK, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_ARG (the
+ * first set, in that order of precedence: TIMEOUT, DEVICE_ARG, NONFINITE). */
+MOE_API moe_status moe_read_device_error(const moe_config* cfg, void* ws, size_t ws_bytes,
+                                         moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -157,30 +157,43 @@ void oracle_router(int T, int d, int E, int k, const float* x, const float* Wg,
                    const float* Wnoise, const float* noise, const float* offset,
                    const float* bias, int renorm, double* z, double* H, double* p, double* s,
                    int32_t* ids, double* w) {
-#pragma omp parallel for schedule(static)
-    for (int t = 0; t < T; ++t) {
-        const float* xt = x + (size_t)t * d;
-        double* zt = z + (size_t)t * E;
-        double* Ht = H + (size_t)t * E;
-        double* pt = p + (size_t)t * E;
-        double* st = s + (size_t)t * E;
-        for (int e = 0; e < E; ++e) {
-            double acc = 0.0;
-            for (int i = 0; i < d; ++i) acc += (double)xt[i] * (double)Wg[(size_t)i * E + e];
-            if (offset) acc += (double)offset[e];
-            zt[e] = acc;
-            double h = acc;
-            if (Wnoise && noise) {
-                double an = 0.0;
-                for (int i = 0; i < d; ++i) an += (double)xt[i] * (double)Wnoise[(size_t)i * E + e];
-                h += (double)noise[(size_t)t * E + e] * oracle_softplus(an);
+#pragma omp parallel
+    {
+        double* zn = (double*)malloc(sizeof(double) * E);
+#pragma omp for schedule(static)
+        for (int t = 0; t < T; ++t) {
+            const float* xt = x + (size_t)t * d;
+            double* zt = z + (size_t)t * E;
+            double* Ht = H + (size_t)t * E;
+            double* pt = p + (size_t)t * E;
+            double* st = s + (size_t)t * E;
+            /* each z[t,e] (and zn[t,e]) is summed over i = 0..d-1 in order; the
+             * loop over e sits inside only so that Wg is read row by row */
+            for (int e = 0; e < E; ++e) {
+                zt[e] = 0.0;
+                zn[e] = 0.0;
             }
-            Ht[e] = h;
+            for (int i = 0; i < d; ++i) {
+                const double xi = (double)xt[i];
+                const float* wrow = Wg + (size_t)i * E;
+                for (int e = 0; e < E; ++e) zt[e] += xi * (double)wrow[e];
+                if (Wnoise && noise) {
+                    const float* nrow = Wnoise + (size_t)i * E;
+                    for (int e = 0; e < E; ++e) zn[e] += xi * (double)nrow[e];
+                }
+            }
+            for (int e = 0; e < E; ++e) {
+                if (offset) zt[e] += (double)offset[e];
+                double h = zt[e];
+                if (Wnoise && noise) h += (double)noise[(size_t)t * E + e] * oracle_softplus(zn[e]);
+                Ht[e] = h;
+            }
+            oracle_softmax(E, Ht, pt);
+            for (int e = 0; e < E; ++e) st[e] = bias ? pt[e] + (double)bias[e] : Ht[e];
+            topk_row(E, k, st, ids + (size_t)t * k);
+            gates_row(k, ids + (size_t)t * k, pt, renorm, w + (size_t)t * k);
         }
-        oracle_softmax(E, Ht, pt);
-        for (int e = 0; e < E; ++e) st[e] = bias ? pt[e] + (double)bias[e] : Ht[e];
-        topk_row(E, k, st, ids + (size_t)t * k);
-        gates_row(k, ids + (size_t)t * k, pt, renorm, w + (size_t)t * k);
+        free(zn);
     }
 }
 

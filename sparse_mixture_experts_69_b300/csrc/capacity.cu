@@ -1,0 +1,193 @@
+// Capacity assignment and dispatch.
+//
+// Method: "MoE notes" (chiang97912.github.io), section Expert capacity
+// (capacity = tokens per batch / experts * capacity factor); mkbk-pku.cn MoE
+// notes, load-balance section (a token beyond capacity is dropped) and the
+// grouped-GEMM section (tokens bucketed by expert, packed contiguously).
+//
+// Token-order priority without any inter-block waiting, in three launches:
+//   1. hist : per block of 256 tokens, assignments per expert
+//   2. scan : per expert, exclusive prefix over blocks (block base); totals
+//             give counts, kept = min(counts, C), offsets = scan of kept
+//   3. slot : within a block, the rank of (t, e) among earlier tokens of the
+//             block that chose e, from per-warp lane bitmasks; slot = base + rank
+// then a permute copies each token's row to its kept rows.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// blk_hist is expert-major: [E][nblk]
+__global__ void __launch_bounds__(kCapBlockTokens) cap_hist_kernel(
+    int T, int k, int E, int nblk, const int32_t* __restrict__ ids, int32_t* __restrict__ blk_hist,
+    int* status) {
+    extern __shared__ int hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * kCapBlockTokens + threadIdx.x;
+    bool bad = false;
+    if (t < T) {
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            if (e >= 0 && e < E) {
+                atomicAdd(&hist[e], 1);
+                for (int q = 0; q < j; ++q)
+                    if (ids[(size_t)t * k + q] == e) bad = true;  // ids must be distinct
+            } else {
+                bad = true;
+            }
+        }
+    }
+    if (bad) flag_status(status, DEV_BAD_ARG);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        blk_hist[(size_t)e * nblk + blockIdx.x] = hist[e];
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// One block of 1024 threads. Warp w scans experts w, w+32, ...
+__global__ void __launch_bounds__(1024) cap_scan_kernel(
+    int nblk, int E, int C, const int32_t* __restrict__ blk_hist, int32_t* __restrict__ blk_base,
+    int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets) {
+    __shared__ int kp[1024];
+    __shared__ int wsum[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = warp; e < E; e += 32) {
+        int running = 0;
+        for (int b0 = 0; b0 < nblk; b0 += 32) {
+            int b = b0 + lane;
+            int v = b < nblk ? blk_hist[(size_t)e * nblk + b] : 0;
+            int incl = warp_incl_scan(v);
+            if (b < nblk) blk_base[(size_t)e * nblk + b] = running + incl - v;
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            counts[e] = running;
+            int kv = running < C ? running : C;
+            kept[e] = kv;
+            kp[e] = kv;
+        }
+    }
+    __syncthreads();
+    // exclusive scan of kept over experts (E <= 1024)
+    const int e = threadIdx.x;
+    int v = e < E ? kp[e] : 0;
+    int incl = warp_incl_scan(v);
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int s = wsum[lane];
+        int si = warp_incl_scan(s);
+        wsum[lane] = si - s;
+    }
+    __syncthreads();
+    if (e < E) offsets[e] = wsum[warp] + incl - v;
+    if (e == E - 1) offsets[E] = wsum[warp] + incl;
+}
+
+// Dynamic smem: mask[8][E] lane bitmasks (bit l of mask[w][e]: lane l of warp w chose e)
+__global__ void __launch_bounds__(kCapBlockTokens) cap_slot_kernel(
+    int T, int k, int E, int C, int nblk, const int32_t* __restrict__ ids,
+    const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
+    int32_t* __restrict__ slot, int32_t* __restrict__ row_token) {
+    extern __shared__ unsigned mask[];
+    constexpr int W = kCapBlockTokens / 32;
+    for (int i = threadIdx.x; i < W * E; i += blockDim.x) mask[i] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * kCapBlockTokens + threadIdx.x;
+    if (t < T)
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            if (e >= 0 && e < E) atomicOr(&mask[warp * E + e], 1u << lane);
+        }
+    __syncthreads();
+    if (t >= T) return;
+    const unsigned lt = lanemask_lt();
+    for (int j = 0; j < k; ++j) {
+        const size_t a = (size_t)t * k + j;
+        int e = ids[a];
+        int out = -1;
+        if (e >= 0 && e < E) {
+            int r = __popc(mask[warp * E + e] & lt);
+            for (int w = 0; w < warp; ++w) r += __popc(mask[w * E + e]);
+            int sl = blk_base[(size_t)e * nblk + blockIdx.x] + r;
+            if (sl < C) {
+                out = offsets[e] + sl;
+                row_token[out] = t;
+            }
+        }
+        slot[a] = out;
+    }
+}
+
+cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_hist,
+                            int32_t* blk_base, int32_t* counts, int32_t* kept, int32_t* offsets,
+                            int32_t* slot, int32_t* row_token, int* status, cudaStream_t st) {
+    const int nblk = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
+    cap_hist_kernel<<<nblk, kCapBlockTokens, s.E * sizeof(int), st>>>(s.T, s.k, s.E, nblk, ids,
+                                                                      blk_hist, status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    cap_scan_kernel<<<1, 1024, 0, st>>>(nblk, s.E, s.C, blk_hist, blk_base, counts, kept,
+                                        offsets);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const size_t smem = (size_t)(kCapBlockTokens / 32) * s.E * sizeof(unsigned);
+    cap_slot_kernel<<<nblk, kCapBlockTokens, smem, st>>>(s.T, s.k, s.E, s.C, nblk, ids, blk_base,
+                                                         offsets, slot, row_token);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- permute
+// One warp per token: read the row once (16-byte vectors), write it to each of
+// the token's kept rows. Algorithmic bytes: T d b read + R d b written.
+__global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec,
+                                                      const uint4* __restrict__ x,
+                                                      const int32_t* __restrict__ slot,
+                                                      uint4* __restrict__ xp) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
+    unsigned live = __ballot_sync(0xffffffffu, my_slot >= 0);
+    const uint4* src = x + (size_t)t * nvec;
+    // the loop bound is warp-uniform so every shuffle has all lanes present
+    for (int v0 = 0; v0 < nvec; v0 += 32) {
+        const int v = v0 + lane;
+        const bool ok = v < nvec;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (ok) val = __ldcs(src + v);
+        unsigned m = live;
+        while (m) {
+            const int j = __ffs(m) - 1;
+            m &= m - 1;
+            const int r = __shfl_sync(0xffffffffu, my_slot, j);
+            if (ok) xp[(size_t)r * nvec + v] = val;
+        }
+    }
+}
+
+cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
+                           cudaStream_t st) {
+    const int nvec = s.d * s.esize / 16;
+    permute_kernel<<<(s.T + 7) / 8, 256, 0, st>>>(s.T, s.k, nvec, (const uint4*)x, slot,
+                                                 (uint4*)xp);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

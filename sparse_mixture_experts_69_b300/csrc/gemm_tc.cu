@@ -1,0 +1,586 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05, sm_103a), bf16 in,
+// fp32 accumulation in tensor memory, used for
+//   - the expert FFN up projection with a fused ReLU / GELU / SwiGLU epilogue,
+//   - the expert FFN down projection,
+//   - the router logits (one group, fp32 output split into logits and noise logits).
+//
+// Method: mkbk-pku.cn MoE notes, section on MoE optimisation (all experts' GEMMs
+// merged into one grouped schedule over expert-contiguous rows).
+//
+// Structure (one persistent CTA per SM, 6 warps):
+//   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per stage,
+//               128-byte swizzle, completion on a per-stage mbarrier
+//   warp 1      owns the tensor-memory allocation; lane 0 issues tcgen05.mma
+//               (M=128, N=BN, K=16 per instruction) and commits stage releases
+//               and finished accumulators to mbarriers
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//               32*(w%4) .. +31 = tile rows), activation, bf16 pack, global store
+// Two accumulator buffers in TMEM let the epilogue of one tile overlap the
+// main loop of the next. Every mbarrier wait is bounded in time; on expiry the
+// CTA records DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+#include <algorithm>
+#include <mutex>
+
+#include "group_table.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle atom row
+constexpr int kThreads = 192;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+enum Epi : int { EPI_ACT = 0, EPI_GLU = 1, EPI_ROUTER = 2 };
+
+struct TcArgs {
+    GroupedGemm p;
+    const float* offset;  // router: [E] or NULL
+    float* logits;        // router: [T,E]
+    float* zn;            // router: [T,E] or NULL
+    int E_router;         // router: columns < E_router are logits
+};
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN >= 256 ? 4 : BN >= 128 ? 6 : 8;
+    static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // power of two for BN in {32..256}
+    static constexpr int B_BOX_ROWS = BN < 128 ? BN : 128;
+    static constexpr int B_LOADS = BN / B_BOX_ROWS;
+    // M=128, N=BN, D=f32, A=B=bf16, both K-major
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                                      ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    static constexpr size_t smem_bytes(int G) {
+        return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (size_t)(G + 1);
+    }
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity to complete. Returns false if the
+// CTA is aborting or the wait exceeded kTimeoutNs (which starts the abort).
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                       int* status, unsigned long long limit_ns) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            flag_status(status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate)
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` once all tcgen05 operations issued so far by this thread are done.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core groups 1024 bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                    // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+    d |= (uint64_t)1 << 46;                    // descriptor version
+    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+    return d;
+}
+
+// 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 16 columns at taddr_a and 16 at taddr_b, one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va, float* vb) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,"
+        "%27,%28,%29,%30,%31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[16 + i]);
+    }
+}
+
+// ------------------------------------------------------------ epilogue math
+__device__ __forceinline__ float act_apply(int act, float u) {
+    if (act == MOE_RELU) return fmaxf(u, 0.f);
+    if (act == MOE_GELU) return 0.5f * u * erfcf(-u * 0.70710678118654752f);
+    return u;
+}
+__device__ __forceinline__ float silu(float u) { return u / (1.f + expf(-u)); }
+
+// Store n (<= 32, multiple of 8 when vec) bf16 values of one row.
+__device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* v, int n) {
+    if (n >= 32) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 pk;
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+            d4[q] = pk;
+        }
+    } else {
+        for (int i = 0; i < n; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0,
+                           const __grid_constant__ CUtensorMap tmA1,
+                           const __grid_constant__ CUtensorMap tmB0,
+                           const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+    using C = Cfg<BN>;
+    const GroupedGemm& p = args.p;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* tfull = empty + C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* mt_start = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.E + p.S;
+    const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
+    const int nt = (p.N + ncol_tile - 1) / ncol_tile;
+    const int nkb = (p.K + BK - 1) / BK;
+
+    build_tile_table(p, BM, mt_start);
+    __syncthreads();
+    const int total = mt_start[G] * nt;
+    if ((int)blockIdx.x >= total) return;  // no work: leave before any allocation
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tmap(&tmA0);
+        prefetch_tmap(&tmA1);
+        prefetch_tmap(&tmB0);
+        prefetch_tmap(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
+                const bool routed = gt.g < p.E;
+                const CUtensorMap* ma = routed ? &tmA0 : &tmA1;
+                const CUtensorMap* mb = routed ? &tmB0 : &tmB1;
+                int brow[C::B_LOADS];
+#pragma unroll
+                for (int h = 0; h < C::B_LOADS; ++h) {
+                    if (EPI == EPI_GLU)
+                        brow[h] = gt.b_row + h * p.N + gt.n_tile * 128;  // gate half, up half
+                    else
+                        brow[h] = gt.b_row + gt.n_tile * BN + h * C::B_BOX_ROWS;
+                }
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, kTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    tma_load_2d(sA + stage * C::A_BYTES, ma, &full[stage], kb * BK, gt.a_row);
+#pragma unroll
+                    for (int h = 0; h < C::B_LOADS; ++h)
+                        tma_load_2d(sB + stage * C::B_BYTES + h * C::B_BOX_ROWS * 128, mb,
+                                    &full[stage], kb * BK, brow[h]);
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // aborting: let the copies already issued land before smem is released
+                for (int s = 0; s < C::STAGES; ++s)
+                    if ((filled >> s) & 1u) {
+                        volatile int never = 0;
+                        mbar_wait(&full[s], (fill_parity >> s) & 1u, &never, p.status,
+                                  kTimeoutNs / 8);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
+                const int b = local & 1;
+                const uint32_t tph = (local >> 1) & 1;
+                if (!mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.status, kTimeoutNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_sw128(smem_u32(sA + stage * C::A_BYTES));
+                    const uint64_t bd = sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, C::IDESC,
+                                  (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit(&empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) umma_commit(&tfull[b]);
+            }
+            if (!ok) {
+                umma_commit(drain);
+                volatile int never = 0;
+                mbar_wait(drain, 0, &never, p.status, kTimeoutNs / 8);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+            const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
+            const int b = local & 1;
+            const uint32_t tph = (local >> 1) & 1;
+            if (!mbar_wait(&tfull[b], tph, abort_flag, p.status, kTimeoutNs)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t)(b * BN) + ((uint32_t)(32 * q) << 16);
+            const bool rv = row < gt.rows;
+            const bool routed = gt.g < p.E;
+            if (EPI == EPI_ROUTER) {
+                const int t = gt.out_row + row;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+                    const int n0 = gt.n_tile * BN + c;
+                    if (rv) {
+                        for (int i = 0; i < 32; ++i) {
+                            const int n = n0 + i;
+                            if (n >= p.N) break;
+                            if (n < args.E_router)
+                                args.logits[(size_t)t * args.E_router + n] =
+                                    v[i] + (args.offset ? args.offset[n] : 0.f);
+                            else
+                                args.zn[(size_t)t * args.E_router + (n - args.E_router)] = v[i];
+                        }
+                    }
+                }
+            } else {
+                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(routed ? p.out0 : p.out1);
+                __nv_bfloat16* orow = out + (size_t)(gt.out_row + row) * p.N;
+                if (EPI == EPI_GLU) {
+#pragma unroll 1
+                    for (int c = 0; c < 128; c += 16) {
+                        float g[16], u[16], v[32];
+                        tmem_ld16x2(taddr + c, taddr + 128 + c, g, u);
+                        const int n0 = gt.n_tile * 128 + c;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = silu(g[i]) * u[i];
+                        if (rv && n0 < p.N) {
+                            const int n = min(16, p.N - n0);
+                            if (n == 16) {
+                                uint4* d4 = reinterpret_cast<uint4*>(orow + n0);
+#pragma unroll
+                                for (int qq = 0; qq < 2; ++qq) {
+                                    uint4 pk;
+                                    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i)
+                                        h[i] = __floats2bfloat162_rn(v[8 * qq + 2 * i],
+                                                                     v[8 * qq + 2 * i + 1]);
+                                    d4[qq] = pk;
+                                }
+                            } else {
+                                for (int i = 0; i < n; ++i) orow[n0 + i] = __float2bfloat16_rn(v[i]);
+                            }
+                        }
+                    }
+                } else {
+                    const int act = p.glu ? -1 : p.act;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        float v[32];
+                        tmem_ld32(taddr + c, v);
+                        const int n0 = gt.n_tile * BN + c;
+                        if (rv && n0 < p.N) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = act_apply(act, v[i]);
+                            store_bf16_row(orow + n0, v, min(32, p.N - n0));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[b]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix; box [box_rows, 64].
+static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
+                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
+    using C = Cfg<BN>;
+    const GroupedGemm& p = a.p;
+    CUtensorMap mA0, mA1, mB0, mB1;
+    const int G = p.E + p.S;
+    if (!make_map(&mA0, p.A0 ? p.A0 : p.A1, p.A0 ? p.rows_a0 : p.rows_a1, p.K, BM) ||
+        !make_map(&mA1, p.A1 ? p.A1 : p.A0, p.A1 ? p.rows_a1 : p.rows_a0, p.K, BM))
+        return cudaErrorInvalidValue;
+    const int brows0 = p.E * p.b_rows_group, brows1 = p.S * p.b_rows_group;
+    if (!make_map(&mB0, p.B0 ? p.B0 : p.B1, p.B0 ? brows0 : brows1, p.K, C::B_BOX_ROWS) ||
+        !make_map(&mB1, p.B1 ? p.B1 : p.B0, p.B1 ? brows1 : brows0, p.K, C::B_BOX_ROWS))
+        return cudaErrorInvalidValue;
+    const size_t smem = C::smem_bytes(G);
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<BN, EPI>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    // upper bound of the tile count, from host-known sizes
+    const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
+    const long long nt = (p.N + ncol_tile - 1) / ncol_tile;
+    long long mt = (long long)p.rows_a0 / BM + p.E + (long long)p.S * ((p.T + BM - 1) / BM);
+    if (p.E == 0) mt = (long long)p.S * ((p.T + BM - 1) / BM);
+    const long long bound = std::max<long long>(1, mt * nt);
+    const int grid = (int)std::min<long long>(bound, num_sms());
+    grouped_gemm_tc_kernel<BN, EPI><<<grid, kThreads, smem, st>>>(mA0, mA1, mB0, mB1, a);
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+
+size_t tc_smem_bytes_max(int G) { return tc::Cfg<256>::smem_bytes(G); }
+
+cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStream_t st) {
+    tc::TcArgs a{};
+    a.p = g;
+    if (g.glu) return tc::launch<256, tc::EPI_GLU>(a, st);
+    return tc::launch<256, tc::EPI_ACT>(a, st);
+}
+
+cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
+                                    const float* offset, float* logits, float* zn, int* status,
+                                    cudaStream_t st) {
+    tc::TcArgs a{};
+    GroupedGemm& p = a.p;
+    p.offsets = nullptr;
+    p.E = 0;
+    p.S = 1;
+    p.T = s.T;
+    p.a1_row0 = 0;
+    p.a1_stride = 0;
+    p.rows_a0 = 0;
+    p.rows_a1 = s.T;
+    p.N = Nr;
+    p.K = s.d;
+    p.b_rows_group = Nr;
+    p.glu = 0;
+    p.act = -1;
+    p.A0 = nullptr;
+    p.A1 = x;
+    p.B0 = nullptr;
+    p.B1 = wgT;
+    p.out0 = nullptr;
+    p.out1 = nullptr;
+    p.status = status;
+    a.offset = offset;
+    a.logits = logits;
+    a.zn = zn;
+    a.E_router = s.E;
+    if (Nr <= 32) return tc::launch<32, tc::EPI_ROUTER>(a, st);
+    if (Nr <= 64) return tc::launch<64, tc::EPI_ROUTER>(a, st);
+    if (Nr <= 128) return tc::launch<128, tc::EPI_ROUTER>(a, st);
+    return tc::launch<256, tc::EPI_ROUTER>(a, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,98 @@
+// Tile table of a grouped GEMM, built on the device from the expert offsets.
+//
+// Group g < E is routed expert g (rows offsets[g] .. offsets[g+1]-1 of A0);
+// group E + s is shared expert s (T rows of A1). Each group is cut into
+// ceil(M_g / BM) row tiles and nt column tiles. Tiles are numbered group by
+// group; inside a group column-tile-major, row tiles consecutive, so CTAs that
+// run at the same time share the same weight tile through L2.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+struct GroupTile {
+    int g;        // group
+    int m0;       // first row of the tile inside the group
+    int n_tile;   // column tile
+    int rows;     // valid rows of the group from m0 (may exceed BM)
+    int a_row;    // first A row of the tile
+    int out_row;  // first output row of the tile (in out0 for routed, out1 for shared)
+    int b_row;    // first B row of the group (in B0 or B1)
+};
+
+__device__ __forceinline__ int group_rows(const GroupedGemm& p, int g, int* a_row, int* out_row,
+                                          bool* bad) {
+    if (g < p.E) {
+        int lo = p.offsets[g], hi = p.offsets[g + 1];
+        if (lo < 0 || hi < lo || hi > p.rows_a0) {
+            *bad = true;
+            *a_row = 0;
+            *out_row = 0;
+            return 0;
+        }
+        *a_row = lo;
+        *out_row = lo;
+        return hi - lo;
+    }
+    const int s = g - p.E;
+    *a_row = p.a1_row0 + s * p.a1_stride;
+    *out_row = s * p.T;
+    return p.T;
+}
+
+// Warp 0 of the block fills mt_start[0..G] (row-tile prefix). Caller syncs.
+__device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, int* mt_start) {
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    const int G = p.E + p.S;
+    int running = 0;
+    bool bad = false;
+    for (int base = 0; base < G; base += 32) {
+        const int g = base + lane;
+        int mt = 0;
+        if (g < G) {
+            int ar, orow;
+            int M = group_rows(p, g, &ar, &orow, &bad);
+            mt = (M + BM - 1) / BM;
+        }
+        int incl = mt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (g < G) mt_start[g] = running + incl - mt;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) mt_start[G] = running;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DEV_BAD_ARG);
+}
+
+__device__ __forceinline__ GroupTile decode_tile(const GroupedGemm& p, const int* mt_start,
+                                                 int nt, int BM, int tile) {
+    const int G = p.E + p.S;
+    // largest g with mt_start[g] * nt <= tile
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (mt_start[mid] * nt <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    GroupTile t;
+    t.g = lo;
+    const int mt = mt_start[lo + 1] - mt_start[lo];
+    const int local = tile - mt_start[lo] * nt;
+    t.n_tile = local / mt;
+    t.m0 = (local % mt) * BM;
+    bool bad = false;
+    int a_row, out_row;
+    const int M = group_rows(p, lo, &a_row, &out_row, &bad);
+    t.rows = M - t.m0;
+    t.a_row = a_row + t.m0;
+    t.out_row = out_row + t.m0;
+    t.b_row = (lo < p.E ? lo : lo - p.E) * p.b_rows_group;
+    return t;
+}
+
+}  // namespace moe

@@ -1,0 +1,429 @@
+// Host side of the C ABI declared in include/moe.h: argument validation,
+// workspace carving and the order of launches on the caller's stream.
+#include <math.h>
+
+#include <algorithm>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStream_t st);
+cudaError_t launch_grouped_gemm_simt(const Shape& s, const GroupedGemm& g, cudaStream_t st);
+
+cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream_t st) {
+    return s.dtype == MOE_BF16 ? launch_grouped_gemm_tc(s, g, st)
+                               : launch_grouped_gemm_simt(s, g, st);
+}
+
+int num_sms() {
+    static int cache[128] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(const Shape& s) {
+    WsLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align256(off + std::max<size_t>(bytes, 1));
+        return o;
+    };
+    const size_t T = s.T, E = s.E, k = s.k, d = s.d, F = s.F, S = s.S, R = s.R_max;
+    const size_t es = s.esize;
+    L.status = take(256);
+    L.zn = take(T * E * 4);
+    L.wgT = take(2 * E * d * es);
+    L.logits = take(T * E * 4);
+    L.probs = take(T * E * 4);
+    L.ids = take(T * k * 4);
+    L.w = take(T * k * 4);
+    L.slot = take(T * k * 4);
+    L.counts = take(E * 4);
+    L.kept = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.row_token = take(R * 4);
+    const size_t nblk = (T + kCapBlockTokens - 1) / kCapBlockTokens;
+    L.blk_hist = take(nblk * E * 4);
+    L.blk_base = take(nblk * E * 4);
+    L.xp = take(R * d * es);
+    L.h = take((R + S * T) * F * es);
+    L.yp = take(R * d * es);
+    L.ys = take(S * T * d * es);
+    const size_t nblk_aux = (T + kAuxBlockTokens - 1) / kAuxBlockTokens;
+    L.aux_part = take(nblk_aux * 3 * E * 4);
+    L.aux_vecs = take(3 * E * 4);
+    L.out3 = take(16);
+    L.total = off;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+moe_status make_shape(const moe_config* c, Shape* s) {
+    if (!c || !s) return MOE_ERR_INVALID_ARG;
+    if (c->T < 1 || c->d_model < 1 || c->n_experts < 1 || c->top_k < 1 || c->d_ff < 1 ||
+        c->n_shared < 0 || c->top_k > c->n_experts)
+        return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->act < MOE_RELU || c->act > MOE_SWIGLU) return MOE_ERR_INVALID_ARG;
+    if (c->renorm_topk != 0 && c->renorm_topk != 1) return MOE_ERR_INVALID_ARG;
+    if (!isfinite(c->capacity_factor) || !isfinite(c->importance_weight))
+        return MOE_ERR_INVALID_ARG;
+    if (c->n_experts > 1024 || c->top_k > 32 || c->n_shared > 64) return MOE_ERR_UNSUPPORTED;
+    if (c->d_model % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    const long long T = c->T, E = c->n_experts, k = c->top_k, S = c->n_shared;
+    long long C = T;
+    if (c->capacity_factor > 0.f) {
+        C = (long long)ceil((double)T * (double)c->capacity_factor / (double)E);
+        if (C > T) C = T;  // no expert can receive more than T tokens
+    }
+    const long long R = std::min(T * k, E * C);
+    const long long F1 = c->act == MOE_SWIGLU ? 2LL * c->d_ff : c->d_ff;
+    // row indices and TMA coordinates are 32-bit
+    if (T * k >= (1LL << 31) || R + S * T >= (1LL << 31) || E * F1 >= (1LL << 31) ||
+        E * (long long)c->d_model >= (1LL << 31))
+        return MOE_ERR_UNSUPPORTED;
+    s->T = c->T;
+    s->d = c->d_model;
+    s->E = c->n_experts;
+    s->k = c->top_k;
+    s->F = c->d_ff;
+    s->S = c->n_shared;
+    s->F1 = (int)F1;
+    s->C = (int)C;
+    s->R_max = (int)R;
+    s->dtype = c->dtype;
+    s->act = c->act;
+    s->renorm = c->renorm_topk;
+    s->w_imp = c->importance_weight;
+    s->esize = c->dtype == MOE_BF16 ? 2 : 4;
+    return MOE_OK;
+}
+
+moe_status check_ws(const Shape& s, void* ws, size_t ws_bytes, WsLayout* L) {
+    *L = ws_layout(s);
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return MOE_ERR_UNSUPPORTED;
+    if (ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+#define MOE_TRY(expr)                          \
+    do {                                       \
+        moe_status _st = (expr);               \
+        if (_st != MOE_OK) return _st;         \
+    } while (0)
+#define MOE_CUDA(expr)                               \
+    do {                                             \
+        if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)
+
+// -------------------------------------------------------------- stage bodies
+moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x, const void* Wg,
+                      const void* Wnoise, const float* noise, const float* offset,
+                      const float* bias, float* logits, float* probs, float* sel, int32_t* ids,
+                      float* w, cudaStream_t st) {
+    int* status = at<int>(ws, L.status);
+    const bool noisy = Wnoise != nullptr;
+    const int Nr = noisy ? 2 * s.E : s.E;
+    float* zn = noisy ? at<float>(ws, L.zn) : nullptr;
+    if (s.dtype == MOE_BF16) {
+        void* wgT = at<void>(ws, L.wgT);
+        MOE_CUDA(launch_transpose_router_w(s, Wg, Wnoise, wgT, st));
+        MOE_CUDA(launch_router_gemm_bf16(s, Nr, x, wgT, offset, logits, zn, status, st));
+    } else {
+        MOE_CUDA(launch_router_gemm_f32(s, Nr, static_cast<const float*>(x),
+                                        static_cast<const float*>(Wg),
+                                        static_cast<const float*>(Wnoise), offset, logits, zn,
+                                        st));
+    }
+    MOE_CUDA(launch_router_select(s, logits, zn, noisy ? noise : nullptr, bias, probs, sel, ids,
+                                  w, 0, nullptr, nullptr, status, st));
+    return MOE_OK;
+}
+
+moe_status dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const void* x,
+                         const int32_t* ids, int32_t* counts, int32_t* kept, int32_t* offsets,
+                         int32_t* slot, void* xp, int32_t* row_token, cudaStream_t st) {
+    int* status = at<int>(ws, L.status);
+    MOE_CUDA(launch_capacity(s, ids, at<int32_t>(ws, L.blk_hist), at<int32_t>(ws, L.blk_base),
+                             counts, kept, offsets, slot, row_token, status, st));
+    MOE_CUDA(launch_permute(s, x, slot, xp, st));
+    return MOE_OK;
+}
+
+moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
+                    const int32_t* offsets, const void* W1, const void* W2, const void* x,
+                    const void* W1s, const void* W2s, void* yp, void* ys, cudaStream_t st) {
+    int* status = at<int>(ws, L.status);
+    void* h = at<void>(ws, L.h);
+    void* h_shared = static_cast<char*>(h) + (size_t)s.R_max * s.F * s.esize;
+    GroupedGemm up{};
+    up.offsets = offsets;
+    up.E = s.E;
+    up.S = s.S;
+    up.T = s.T;
+    up.a1_row0 = 0;
+    up.a1_stride = 0;
+    up.rows_a0 = s.R_max;
+    up.rows_a1 = s.T;
+    up.N = s.F;
+    up.K = s.d;
+    up.b_rows_group = s.F1;
+    up.glu = s.act == MOE_SWIGLU;
+    up.act = s.act;
+    up.A0 = xp;
+    up.A1 = s.S ? x : nullptr;
+    up.B0 = W1;
+    up.B1 = s.S ? W1s : nullptr;
+    up.out0 = h;
+    up.out1 = h_shared;
+    up.status = status;
+    MOE_CUDA(launch_grouped_gemm(s, up, st));
+    GroupedGemm dn{};
+    dn.offsets = offsets;
+    dn.E = s.E;
+    dn.S = s.S;
+    dn.T = s.T;
+    dn.a1_row0 = s.R_max;
+    dn.a1_stride = s.T;
+    dn.rows_a0 = s.R_max;
+    dn.rows_a1 = s.R_max + s.S * s.T;
+    dn.N = s.d;
+    dn.K = s.F;
+    dn.b_rows_group = s.d;
+    dn.glu = 0;
+    dn.act = -1;
+    dn.A0 = h;
+    dn.A1 = s.S ? h : nullptr;
+    dn.B0 = W2;
+    dn.B1 = s.S ? W2s : nullptr;
+    dn.out0 = yp;
+    dn.out1 = s.S ? ys : nullptr;
+    dn.status = status;
+    MOE_CUDA(launch_grouped_gemm(s, dn, st));
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+MOE_API const char* moe_status_string(moe_status status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: unsupported size or alignment";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA call or launch failed";
+        case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE: NaN or Inf found on the device";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a device pipeline wait ran out";
+        case MOE_ERR_DEVICE_ARG: return "MOE_ERR_DEVICE_ARG: expert id or offsets out of range";
+    }
+    return "unknown moe_status";
+}
+
+MOE_API moe_status moe_capacity(const moe_config* cfg, int32_t* capacity, int32_t* rows_max) {
+    Shape s;
+    MOE_TRY(make_shape(cfg, &s));
+    if (capacity) *capacity = s.C;
+    if (rows_max) *rows_max = s.R_max;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+    Shape s;
+    MOE_TRY(make_shape(cfg, &s));
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(s).total;
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_workspace_reset(const moe_config* cfg, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    MOE_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, 256, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* Wg,
+                             const void* Wnoise, const float* noise, const float* logit_offset,
+                             const float* sel_bias, float* logits, float* probs,
+                             float* sel_scores, int32_t* topk_ids, float* topk_w,
+                             int32_t from_scores, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!topk_ids || !topk_w || !probs) return MOE_ERR_INVALID_ARG;
+    if (from_scores) {
+        if (!sel_scores) return MOE_ERR_INVALID_ARG;
+        MOE_CUDA(launch_router_select(s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                      topk_ids, topk_w, 1, sel_scores, probs,
+                                      at<int>(ws, L.status), st));
+        return MOE_OK;
+    }
+    if (!x || !Wg || !logits) return MOE_ERR_INVALID_ARG;
+    if ((Wnoise == nullptr) != (noise == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg) || (Wnoise && !aligned16(Wnoise)))
+        return MOE_ERR_UNSUPPORTED;
+    return route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
+                      sel_scores, topk_ids, topk_w, st);
+}
+
+MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                                int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot,
+                                void* xp, int32_t* row_token, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    if (!x || !topk_ids || !counts || !kept || !offsets || !slot || !xp || !row_token)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_UNSUPPORTED;
+    return dispatch_impl(s, L, ws, x, topk_ids, counts, kept, offsets, slot, xp, row_token,
+                         (cudaStream_t)stream);
+}
+
+MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
+                                  const void* W1, const void* W2, const void* x,
+                                  const void* W1s, const void* W2s, void* yp, void* ys,
+                                  void* ws, size_t ws_bytes, moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    if (!xp || !offsets || !W1 || !W2 || !yp) return MOE_ERR_INVALID_ARG;
+    if (s.S > 0 && (!x || !W1s || !W2s || !ys)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(xp) || !aligned16(W1) || !aligned16(W2) || !aligned16(yp)) return MOE_ERR_UNSUPPORTED;
+    if (s.S > 0 && (!aligned16(x) || !aligned16(W1s) || !aligned16(W2s) || !aligned16(ys)))
+        return MOE_ERR_UNSUPPORTED;
+    return ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, (cudaStream_t)stream);
+}
+
+MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot,
+                               const float* topk_w, const void* ys, void* y, void* ws,
+                               size_t ws_bytes, moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    if (!yp || !slot || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+    if (s.S > 0 && !ys) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(yp) || !aligned16(y) || (ys && !aligned16(ys))) return MOE_ERR_UNSUPPORTED;
+    MOE_CUDA(launch_combine(s, yp, slot, topk_w, s.S ? ys : nullptr, y, at<int>(ws, L.status),
+                            (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_aux_stats(const moe_config* cfg, const float* probs,
+                                 const int32_t* topk_ids, const float* topk_w, float* f,
+                                 float* P, float* importance, float* out3, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    if (!probs || !topk_ids || !topk_w || !out3) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_aux(s, probs, topk_ids, topk_w, at<float>(ws, L.aux_part), f, P, importance,
+                        out3, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts, float* bias,
+                                   float rate, moe_stream_t stream) {
+    Shape s;
+    MOE_TRY(make_shape(cfg, &s));
+    if (!counts || !bias || !isfinite(rate)) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_bias_update(s, counts, bias, rate, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const void* Wg,
+                                 const void* Wnoise, const float* noise,
+                                 const float* logit_offset, const float* sel_bias,
+                                 const void* W1, const void* W2, const void* W1s,
+                                 const void* W2s, void* y, int32_t* topk_ids, float* topk_w,
+                                 int32_t* counts, float* aux_vecs, float* out3, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!x || !Wg || !W1 || !W2 || !y) return MOE_ERR_INVALID_ARG;
+    if ((Wnoise == nullptr) != (noise == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (s.S > 0 && (!W1s || !W2s)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg) || (Wnoise && !aligned16(Wnoise)) || !aligned16(W1) ||
+        !aligned16(W2) || !aligned16(y) || (s.S > 0 && (!aligned16(W1s) || !aligned16(W2s))))
+        return MOE_ERR_UNSUPPORTED;
+    float* logits = at<float>(ws, L.logits);
+    float* probs = at<float>(ws, L.probs);
+    int32_t* ids = topk_ids ? topk_ids : at<int32_t>(ws, L.ids);
+    float* w = topk_w ? topk_w : at<float>(ws, L.w);
+    int32_t* cnt = counts ? counts : at<int32_t>(ws, L.counts);
+    int32_t* kept = at<int32_t>(ws, L.kept);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* slot = at<int32_t>(ws, L.slot);
+    int32_t* row_token = at<int32_t>(ws, L.row_token);
+    void* xp = at<void>(ws, L.xp);
+    void* yp = at<void>(ws, L.yp);
+    void* ys = at<void>(ws, L.ys);
+    MOE_TRY(route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
+                       nullptr, ids, w, st));
+    MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token, st));
+    MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, st));
+    MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
+    float* av = aux_vecs ? aux_vecs : at<float>(ws, L.aux_vecs);
+    float* o3 = out3 ? out3 : at<float>(ws, L.out3);
+    MOE_CUDA(launch_aux(s, probs, ids, w, at<float>(ws, L.aux_part), av, av + s.E, av + 2 * s.E,
+                        o3, st));
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_read_device_error(const moe_config* cfg, void* ws, size_t ws_bytes,
+                                         moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    cudaStream_t st = (cudaStream_t)stream;
+    int word = 0;
+    MOE_CUDA(cudaMemcpyAsync(&word, at<int>(ws, L.status), sizeof(int), cudaMemcpyDeviceToHost, st));
+    MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), st));
+    MOE_CUDA(cudaStreamSynchronize(st));
+    if (word & DEV_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (word & DEV_BAD_ARG) return MOE_ERR_DEVICE_ARG;
+    if (word & DEV_NONFINITE) return MOE_ERR_NONFINITE;
+    return MOE_OK;
+}
+
+}  // extern "C"

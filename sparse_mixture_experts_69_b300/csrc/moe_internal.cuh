@@ -1,0 +1,139 @@
+// Internal declarations shared by the CUDA sources of libmoe.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- status word
+// Bits OR-ed by kernels into the first int of the workspace.
+enum : int { DEV_TIMEOUT = 1, DEV_NONFINITE = 2, DEV_BAD_ARG = 4 };
+
+// ------------------------------------------------------------- shape helpers
+struct Shape {
+    int T, d, E, k, F, S;
+    int F1;       // rows of one expert's W1: 2F for SwiGLU, else F
+    int C;        // capacity
+    int R_max;    // min(T k, E C): rows of xp / yp / row_token
+    int dtype;    // MOE_F32 / MOE_BF16
+    int act;
+    int renorm;
+    float w_imp;
+    int esize;    // bytes per element of dtype
+};
+
+// Workspace layout (byte offsets, each 256-aligned). One layout serves every
+// entry point so the stages can be called separately on the same buffer.
+struct WsLayout {
+    size_t status;     // int32 status word (+ padding)
+    size_t zn;         // [T,E] f32 noise logits x.Wnoise
+    size_t wgT;        // [Nr,d] dtype: Wg^T (rows 0..E-1) and Wnoise^T (E..2E-1)
+    size_t logits;     // [T,E] f32 (layer only)
+    size_t probs;      // [T,E] f32 (layer only)
+    size_t ids;        // [T,k] i32 (layer only)
+    size_t w;          // [T,k] f32 (layer only)
+    size_t slot;       // [T,k] i32 (layer only)
+    size_t counts;     // [E] i32 (layer only)
+    size_t kept;       // [E] i32 (layer only)
+    size_t offsets;    // [E+1] i32 (layer only)
+    size_t row_token;  // [R_max] i32 (layer only)
+    size_t blk_hist;   // [nblk,E] i32
+    size_t blk_base;   // [nblk,E] i32
+    size_t xp;         // [R_max,d] dtype (layer only)
+    size_t h;          // [R_max + S T, F] dtype
+    size_t yp;         // [R_max,d] dtype (layer only)
+    size_t ys;         // [S T, d] dtype (layer only)
+    size_t aux_part;   // [nblk_aux, 3E] f32
+    size_t aux_vecs;   // [3E] f32 (layer only)
+    size_t out3;       // [4] f32 (layer only)
+    size_t total;
+};
+
+constexpr int kCapBlockTokens = 256;  // tokens per block of the capacity kernels
+constexpr int kAuxBlockTokens = 128;  // tokens per block of the statistics kernel
+
+WsLayout ws_layout(const Shape& s);
+
+// --------------------------------------------------------------- launchers
+// Each returns a cudaError_t from the launch (cudaGetLastError).
+
+// Router: Wg [d,E] (+ Wnoise) -> WgT [Nr,d]
+cudaError_t launch_transpose_router_w(const Shape& s, const void* Wg, const void* Wnoise,
+                                      void* wgT, cudaStream_t st);
+// Router GEMM for float32 inputs (SIMT), reading Wg / Wnoise [d,E] in place:
+// cols < E -> logits (+offset), cols >= E -> zn
+cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const float* Wg,
+                                   const float* Wnoise, const float* offset, float* logits,
+                                   float* zn, cudaStream_t st);
+// Router GEMM for bf16 inputs (tcgen05)
+cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
+                                    const float* offset, float* logits, float* zn, int* status,
+                                    cudaStream_t st);
+// Noise, softmax, selection bias, top-k, gates
+cudaError_t launch_router_select(const Shape& s, const float* logits, const float* zn,
+                                 const float* noise, const float* bias, float* probs,
+                                 float* sel, int32_t* ids, float* w, int from_scores,
+                                 const float* sel_in, const float* probs_in, int* status,
+                                 cudaStream_t st);
+
+// Capacity: histogram -> scan -> slots; then the permute of x rows into xp
+cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_hist,
+                            int32_t* blk_base, int32_t* counts, int32_t* kept, int32_t* offsets,
+                            int32_t* slot, int32_t* row_token, int* status, cudaStream_t st);
+cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
+                           cudaStream_t st);
+
+// Grouped expert GEMMs. Up: h = act(A W1^T); down: out = h W2^T.
+struct GroupedGemm {
+    // routed groups e < E: rows offsets[e] .. offsets[e+1]-1 of A0, out0
+    const int32_t* offsets;
+    int E;
+    // shared groups s < S: rows a1_row0 + s*a1_stride .. + T of A1; out1 rows s*T ..
+    int S, T;
+    int a1_row0, a1_stride;
+    int rows_a0;        // rows of A0 (bounds: R_max)
+    int rows_a1;        // rows of A1
+    int N;              // output columns
+    int K;              // reduction length
+    int b_rows_group;   // rows of one expert's B matrix (F1 or d)
+    int glu;            // SwiGLU: B rows [0,N) gate, [N,2N) up
+    int act;            // -1 none, MOE_RELU, MOE_GELU (ignored when glu)
+    const void* A0; const void* A1;  // A matrices [rows, K] dtype
+    const void* B0; const void* B1;  // B matrices [groups * b_rows_group, K] dtype
+    void* out0; void* out1;          // [rows, N] dtype
+    int* status;
+};
+cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream_t st);
+
+// Combine, statistics, bias
+cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, const float* w,
+                           const void* ys, void* y, int* status, cudaStream_t st);
+cudaError_t launch_aux(const Shape& s, const float* probs, const int32_t* ids, const float* w,
+                       float* part, float* f, float* P, float* I, float* out3,
+                       cudaStream_t st);
+cudaError_t launch_bias_update(const Shape& s, const int32_t* counts, float* bias, float rate,
+                               cudaStream_t st);
+
+int num_sms();
+
+// ------------------------------------------------------------ device helpers
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ void flag_status(int* status, int bit) {
+    if (status) atomicOr(status, bit);
+}
+
+}  // namespace moe

@@ -1,0 +1,251 @@
+// Router kernels: the transposed copy of the router weights for the tensor-core
+// GEMM, the float32 (SIMT) router GEMM, and the per-token selection kernel
+// (noise, max-subtracted softmax, selection bias, top-k, gates).
+//
+// Method: "MoE notes" (chiang97912.github.io), sections Expert selection and
+// KeepTopK; heavensheep.xyz MoE notes, section Training (softmax numerics);
+// ld246.com MoE Q3 (bias on the softmax scores, for the top-k choice only).
+#include <float.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ transpose
+// WgT[n, i] = Wg[i, n] for n < E; WgT[E + n, i] = Wnoise[i, n]. 32x32 tiles.
+template <typename Tv>
+__global__ void transpose_router_w_kernel(int d, int E, const Tv* __restrict__ Wg,
+                                          const Tv* __restrict__ Wn, Tv* __restrict__ wgT) {
+    __shared__ Tv tile[32][33];
+    const Tv* src = blockIdx.z == 0 ? Wg : Wn;
+    const int i0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+        int i = i0 + r, n = n0 + threadIdx.x;
+        if (i < d && n < E) tile[r][threadIdx.x] = src[(size_t)i * E + n];
+    }
+    __syncthreads();
+    Tv* dst = wgT + (size_t)blockIdx.z * E * d;
+    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+        int n = n0 + r, i = i0 + threadIdx.x;
+        if (i < d && n < E) dst[(size_t)n * d + i] = tile[threadIdx.x][r];
+    }
+}
+
+cudaError_t launch_transpose_router_w(const Shape& s, const void* Wg, const void* Wnoise,
+                                      void* wgT, cudaStream_t st) {
+    dim3 grid((s.E + 31) / 32, (s.d + 31) / 32, Wnoise ? 2 : 1), block(32, 8);
+    if (s.dtype == MOE_BF16)
+        transpose_router_w_kernel<uint16_t><<<grid, block, 0, st>>>(
+            s.d, s.E, (const uint16_t*)Wg, (const uint16_t*)Wnoise, (uint16_t*)wgT);
+    else
+        transpose_router_w_kernel<float><<<grid, block, 0, st>>>(
+            s.d, s.E, (const float*)Wg, (const float*)Wnoise, (float*)wgT);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------- float32 router GEMM
+// z[t, n] = sum_i x[t, i] W[i, n], W = [Wg | Wnoise] read in place ([d,E] each).
+// 64x64 output tile per block, 16-deep k slices, 4x4 per thread, fp32 FMA.
+__global__ void __launch_bounds__(256) router_gemm_f32_kernel(
+    int T, int d, int E, int Nr, const float* __restrict__ x, const float* __restrict__ Wg,
+    const float* __restrict__ Wn, const float* __restrict__ offset, float* __restrict__ logits,
+    float* __restrict__ zn) {
+    __shared__ float As[16][64 + 1];
+    __shared__ float Bs[16][64 + 1];
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < d; k0 += 16) {
+        for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+            int r = i / 16, kk = i % 16, t = m0 + r, kx = k0 + kk;
+            As[kk][r] = (t < T && kx < d) ? x[(size_t)t * d + kx] : 0.f;
+        }
+        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+            int kk = i / 64, c = i % 64, n = n0 + c, kx = k0 + kk;
+            float v = 0.f;
+            if (kx < d && n < Nr) v = n < E ? Wg[(size_t)kx * E + n] : Wn[(size_t)kx * E + (n - E)];
+            Bs[kk][c] = v;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int t = m0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int n = n0 + tx * 4 + j;
+            if (n >= Nr) continue;
+            if (n < E)
+                logits[(size_t)t * E + n] = acc[i][j] + (offset ? offset[n] : 0.f);
+            else
+                zn[(size_t)t * E + (n - E)] = acc[i][j];
+        }
+    }
+}
+
+cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const float* Wg,
+                                   const float* Wnoise, const float* offset, float* logits,
+                                   float* zn, cudaStream_t st) {
+    dim3 grid((Nr + 63) / 64, (s.T + 63) / 64);
+    router_gemm_f32_kernel<<<grid, 256, 0, st>>>(s.T, s.d, s.E, Nr, x, Wg, Wnoise, offset,
+                                                 logits, zn);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ selection
+struct SelectArgs {
+    int T, E, k, renorm, from_scores;
+    const float* logits;   // [T,E] z
+    const float* zn;       // [T,E] x.Wnoise or NULL
+    const float* noise;    // [T,E] or NULL
+    const float* bias;     // [E] or NULL
+    const float* sel_in;   // from_scores: [T,E]
+    const float* probs_in; // from_scores: [T,E]
+    float* probs;          // out [T,E]
+    float* sel;            // out [T,E] or NULL
+    int32_t* ids;          // out [T,k]
+    float* w;              // out [T,k]
+    int* status;
+};
+
+__device__ __forceinline__ float softplus_f(float u) {
+    return fmaxf(u, 0.f) + log1pf(expf(-fabsf(u)));
+}
+
+// One warp per token; lane l holds experts l, l+32, ... (EPL per lane).
+template <int EPL>
+__global__ void __launch_bounds__(256) router_select_kernel(SelectArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    const int E = a.E;
+    const size_t row = (size_t)t * E;
+    float sc[EPL], pr[EPL];
+    bool nonfinite = false;
+    if (a.from_scores) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            int e = lane + 32 * i;
+            sc[i] = e < E ? a.sel_in[row + e] : -FLT_MAX;
+            pr[i] = e < E ? a.probs_in[row + e] : 0.f;
+            if (e < E && !isfinite(sc[i])) nonfinite = true;
+        }
+    } else {
+        float H[EPL];
+        float m = -FLT_MAX;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            int e = lane + 32 * i;
+            float h = -FLT_MAX;
+            if (e < E) {
+                h = a.logits[row + e];
+                if (a.zn && a.noise) h = h + a.noise[row + e] * softplus_f(a.zn[row + e]);
+                if (!isfinite(h)) nonfinite = true;
+                m = fmaxf(m, h);
+            }
+            H[i] = h;
+        }
+        m = warp_max(m);
+        float part = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            int e = lane + 32 * i;
+            pr[i] = e < E ? expf(H[i] - m) : 0.f;
+            part += pr[i];
+        }
+        const float sum = warp_sum(part);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            int e = lane + 32 * i;
+            if (e < E) {
+                pr[i] = pr[i] / sum;
+                a.probs[row + e] = pr[i];
+                sc[i] = a.bias ? pr[i] + a.bias[e] : H[i];
+                if (a.sel) a.sel[row + e] = sc[i];
+            } else {
+                sc[i] = -FLT_MAX;
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, nonfinite) && lane == 0) flag_status(a.status, DEV_NONFINITE);
+
+    // top-k: k rounds of a warp arg-max ordered by (score desc, index asc)
+    unsigned taken = 0;
+    int my_id = 0;
+    float my_p = 0.f, psum = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+        float bv = 0.f;
+        int be = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (be == INT_MAX || sc[i] > bv)) {
+                bv = sc[i];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        be = __shfl_sync(0xffffffffu, be, 0);
+        const int owner = be & 31, slot_i = be >> 5;
+        float mine = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            if (i == slot_i) mine = pr[i];
+        if (lane == owner) taken |= 1u << slot_i;
+        const float pj = __shfl_sync(0xffffffffu, mine, owner);
+        psum += pj;
+        if (lane == j) {
+            my_id = be;
+            my_p = pj;
+        }
+    }
+    if (lane < a.k) {
+        a.ids[(size_t)t * a.k + lane] = my_id;
+        a.w[(size_t)t * a.k + lane] = a.renorm ? my_p / psum : my_p;
+    }
+}
+
+cudaError_t launch_router_select(const Shape& s, const float* logits, const float* zn,
+                                 const float* noise, const float* bias, float* probs,
+                                 float* sel, int32_t* ids, float* w, int from_scores,
+                                 const float* sel_in, const float* probs_in, int* status,
+                                 cudaStream_t st) {
+    SelectArgs a;
+    a.T = s.T; a.E = s.E; a.k = s.k; a.renorm = s.renorm; a.from_scores = from_scores;
+    a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
+    a.sel_in = sel_in; a.probs_in = probs_in;
+    a.probs = probs; a.sel = sel; a.ids = ids; a.w = w; a.status = status;
+    const int warps = 8;
+    dim3 grid((s.T + warps - 1) / warps), block(32 * warps);
+    if (s.E <= 32) router_select_kernel<1><<<grid, block, 0, st>>>(a);
+    else if (s.E <= 64) router_select_kernel<2><<<grid, block, 0, st>>>(a);
+    else if (s.E <= 128) router_select_kernel<4><<<grid, block, 0, st>>>(a);
+    else if (s.E <= 256) router_select_kernel<8><<<grid, block, 0, st>>>(a);
+    else if (s.E <= 512) router_select_kernel<16><<<grid, block, 0, st>>>(a);
+    else router_select_kernel<32><<<grid, block, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

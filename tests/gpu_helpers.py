@@ -1,0 +1,100 @@
+"""Shared pieces of the GPU parity tests: running the C ABI through the
+binding, and the comparison rules.
+
+Tolerances (floating point) follow the stated targets:
+  router logits / probs  max |gpu - ref| <= 1e-4 * max |ref| per token row
+  gates                  the probs' rule when the probs come from each side's own
+                         logits (a gate is a renormalised prob, so a logit error d
+                         moves it by a relative ~d); relative 1e-5 when both sides
+                         get identical probs (fp32 division vs double)
+  expert / layer output  max |gpu - ref| <= 2e-2 * max |ref| (bf16),
+                         1e-4 * max |ref| (fp32)
+  aux, cv2               relative 1e-5
+Integer outputs (ids, slots, counts, offsets, rows) are compared bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from sparse_mixture_experts_69_b300 import moe
+
+TOL_Y = {moe.MOE_BF16: 2e-2, moe.MOE_F32: 1e-4}
+TOL_LOGITS = 1e-4
+TOL_GATE = 1e-5
+TOL_AUX = 1e-5
+
+
+def np32(t):
+    return t.detach().float().cpu().numpy()
+
+
+def assert_rowwise(gpu, ref, rel, what):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(gpu - ref).max(axis=1)
+    scale = np.abs(ref).max(axis=1)
+    bad = err > rel * np.maximum(scale, 1e-30)
+    assert not bad.any(), f"{what}: {bad.sum()} rows off, worst {np.max(err / np.maximum(scale, 1e-30)):.3e}"
+
+
+def assert_maxabs(gpu, ref, rel, what):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(gpu - ref).max() if ref.size else 0.0
+    scale = np.abs(ref).max() if ref.size else 0.0
+    assert err <= rel * scale, f"{what}: max|d| {err:.3e} > {rel} * max|ref| {scale:.3e}"
+    return err / scale if scale else 0.0
+
+
+def check_topk_valid(ids_gpu, s_ref, k, tol_rel=1e-5):
+    """GPU ids against reference scores: equal except where the scores tie
+    within tol_rel; returns the indices of tokens whose ids differ."""
+    ids_gpu = np.asarray(ids_gpu)
+    T = ids_gpu.shape[0]
+    diff = []
+    for t in range(T):
+        s = s_ref[t]
+        order = sorted(range(len(s)), key=lambda e: (-s[e], e))[:k]
+        if list(ids_gpu[t]) == order:
+            continue
+        tol = tol_rel * max(np.abs(s).max(), 1e-30)
+        chosen = list(ids_gpu[t])
+        assert len(set(chosen)) == k, f"token {t}: repeated ids {chosen}"
+        # the GPU order must be non-increasing in the reference scores up to tol,
+        # and nothing left out may beat the last chosen score by more than tol
+        for a, b in zip(chosen, chosen[1:]):
+            assert s[a] >= s[b] - tol, f"token {t}: order {chosen} vs scores"
+        rest = [e for e in range(len(s)) if e not in chosen]
+        if rest:
+            assert max(s[e] for e in rest) <= min(s[e] for e in chosen) + tol, \
+                f"token {t}: ids {chosen} are not a top-{k} (ref {order})"
+        diff.append(t)
+    return diff
+
+
+def layer_outputs(wl, inp, device):
+    c = wl.cfg
+    T, E, k, d = c.T, c.n_experts, c.top_k, c.d_model
+    out = {
+        "y": torch.empty((T, d), dtype=c.torch_dtype, device=device),
+        "ids": torch.empty((T, k), dtype=torch.int32, device=device),
+        "w": torch.empty((T, k), dtype=torch.float32, device=device),
+        "counts": torch.empty(E, dtype=torch.int32, device=device),
+        "aux_vecs": torch.empty((3, E), dtype=torch.float32, device=device),
+        "out3": torch.empty(3, dtype=torch.float32, device=device),
+    }
+    return out
+
+
+def run_layer(wl, inp, device, ws=None):
+    c = wl.cfg
+    if ws is None:
+        ws = moe.workspace(c, device)
+    o = layer_outputs(wl, inp, device)
+    moe.moe_layer_fwd(c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"],
+                      inp["sel_bias"], inp["W1"], inp["W2"], inp["W1s"], inp["W2s"], o["y"],
+                      o["ids"], o["w"], o["counts"], o["aux_vecs"], o["out3"], ws)
+    st = moe.moe_read_device_error(c, ws)
+    assert st == 0, moe.moe_status_string(st)
+    return o, ws

@@ -1,0 +1,77 @@
+"""GPU parity of the tensor-core (tcgen05) kernels: the bf16 router GEMM and
+the grouped expert GEMMs, on shapes that span several tiles, ragged expert
+row counts (0, 1, 127, 128, 129, ...), ragged N and K tails and shared experts."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mixture_experts_69_b300 import moe, synth
+
+from gpu_helpers import TOL_LOGITS, assert_rowwise, check_topk_valid, np32
+from test_gpu_stages import run_ffn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,d,E,k,noisy,offset,bias", [
+    (300, 256, 8, 2, False, True, False),
+    (1000, 200, 40, 3, False, False, False),
+    (8192, 1024, 64, 1, True, False, False),
+    (129, 7168, 256, 8, False, False, True),
+    (64, 4096, 64, 6, False, False, False),
+    (77, 512, 300, 4, False, False, False),
+])
+def test_router_bf16(cuda_device, T, d, E, k, noisy, offset, bias):
+    cfg = moe.Config(T=T, d_model=d, n_experts=E, top_k=k, d_ff=64, dtype=moe.MOE_BF16)
+    dev = cuda_device
+    bf = torch.bfloat16
+    x = synth.normal((T, d), 11, 101, 1.0, bf)
+    Wg = synth.normal((d, E), 11, 102, 0.02, bf)
+    Wn = synth.normal((d, E), 11, 103, 0.02, bf) if noisy else None
+    noise = synth.normal((T, E), 11, 104) if noisy else None
+    off = synth.zipf_logit_offset(E, 1.2) if offset else None
+    b = synth.uniform((E,), 11, 105, -0.1, 0.1) if bias else None
+    g = lambda t: None if t is None else t.to(dev)
+    logits = torch.empty((T, E), device=dev)
+    probs = torch.empty((T, E), device=dev)
+    sel = torch.empty((T, E), device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), device=dev)
+    ws = moe.workspace(cfg, dev)
+    moe.moe_route(cfg, g(x), g(Wg), g(Wn), g(noise), g(off), g(b), logits, probs, sel, ids, w, 0, ws)
+    assert moe.moe_read_device_error(cfg, ws) == 0
+    r = oracle.router(x, Wg, k, Wnoise=Wn, noise=noise, offset=off, bias=b)
+    assert_rowwise(np32(logits), r["z"], TOL_LOGITS, "logits")
+    assert_rowwise(np32(probs), r["p"], TOL_LOGITS, "probs")
+    assert_rowwise(np32(sel), r["s"], TOL_LOGITS, "sel_scores")
+    diff = check_topk_valid(ids.cpu().numpy(), r["s"], k)
+    assert len(diff) <= max(1, T // 1000), diff
+    same = [t for t in range(T) if t not in diff]
+    assert_rowwise(np32(w)[same], r["w"][same], TOL_LOGITS, "gates")
+
+
+@pytest.mark.parametrize("act", [moe.MOE_RELU, moe.MOE_GELU, moe.MOE_SWIGLU])
+def test_expert_ffn_bf16_ragged(cuda_device, act):
+    """Per-expert rows 0, 1, 127, 128, 129, 300; d=200 (K tail), F=136 (N tail)."""
+    cfg = moe.Config(T=200, d_model=200, n_experts=6, top_k=4, d_ff=136, n_shared=2,
+                     dtype=moe.MOE_BF16, act=act)
+    run_ffn(cfg, [0, 1, 127, 128, 129, 300], 21, cuda_device)
+
+
+@pytest.mark.parametrize("act", [moe.MOE_RELU, moe.MOE_SWIGLU])
+def test_expert_ffn_bf16_many_tiles(cuda_device, act):
+    """More tiles than SMs, so the persistent CTAs loop and both TMEM
+    accumulator buffers are reused several times."""
+    cfg = moe.Config(T=1024, d_model=1024, n_experts=8, top_k=2, d_ff=2048, n_shared=0,
+                     dtype=moe.MOE_BF16, act=act)
+    counts = [512, 100, 300, 0, 260, 380, 200, 296]
+    run_ffn(cfg, counts, 22, cuda_device)
+
+
+def test_expert_ffn_bf16_single_row_experts(cuda_device):
+    """Decode-like: one or two rows per expert, 64 experts."""
+    cfg = moe.Config(T=64, d_model=512, n_experts=64, top_k=2, d_ff=256, n_shared=1,
+                     dtype=moe.MOE_BF16, act=moe.MOE_SWIGLU)
+    counts = [2 if e % 3 == 0 else (1 if e % 3 == 1 else 0) for e in range(64)]
+    run_ffn(cfg, counts, 23, cuda_device)
