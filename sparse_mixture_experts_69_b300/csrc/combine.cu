@@ -112,93 +112,143 @@ cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, 
 }
 
 // --------------------------------------------------------------- statistics
-// Pass 1: per block of kAuxBlockTokens tokens, per expert e (thread e):
-//   part[b][e]      = sum_t probs[t,e]
-//   part[b][E+e]    = sum of gates of assignments to e
-//   part[b][2E+e]   = number of assignments to e
-// sums run over tokens in order, so the result does not depend on scheduling.
-__global__ void __launch_bounds__(256) aux_partial_kernel(int T, int E, int k,
-                                                          const float* __restrict__ probs,
-                                                          const int32_t* __restrict__ ids,
-                                                          const float* __restrict__ w,
-                                                          float* __restrict__ part) {
-    extern __shared__ unsigned char sm[];
-    int32_t* sid = reinterpret_cast<int32_t*>(sm);
-    float* sw = reinterpret_cast<float*>(sm + sizeof(int32_t) * kAuxBlockTokens * k);
-    const int t0 = blockIdx.x * kAuxBlockTokens;
-    const int nt = min(kAuxBlockTokens, T - t0);
-    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
-        sid[i] = ids[(size_t)t0 * k + i];
-        sw[i] = w[(size_t)t0 * k + i];
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float P = 0.f, I = 0.f;
-        int c = 0;
-        for (int t = 0; t < nt; ++t) P += probs[(size_t)(t0 + t) * E + e];
-        for (int i = 0; i < nt * k; ++i)
-            if (sid[i] == e) {
-                I += sw[i];
-                ++c;
-            }
-        float* pb = part + (size_t)blockIdx.x * 3 * E;
-        pb[e] = P;
-        pb[E + e] = I;
-        pb[2 * E + e] = (float)c;
-    }
+// One launch. Each block takes kAuxBlockTokens tokens and adds, per expert e,
+//   sum_t probs[t,e]           as 32.32 fixed point (uint64)
+//   sum of gates assigned to e as 32.32 fixed point (uint64)
+//   number of assignments to e (uint32)
+// into the workspace accumulators with integer atomics. Integer addition is
+// associative, so the totals do not depend on the order blocks run in. The
+// last block to finish (ticket counter) turns the totals into f, P,
+// importance, aux and CV^2 with a fixed-order tree, then zeroes the
+// accumulators for the next call. Quantisation: 2^-32 per term.
+struct AuxAcc {
+    unsigned long long* P;  // [E]
+    unsigned long long* I;  // [E]
+    unsigned int* cnt;      // [E]
+    unsigned int* ticket;   // [1]
+};
+
+constexpr float kFix = 4294967296.0f;  // 2^32
+
+__device__ __forceinline__ unsigned long long to_fix(float v) {
+    // v in [0, 1]; v * 2^32 is exact in fp32, then rounded to an integer
+    return v > 0.f ? __float2ull_rn(v * kFix) : 0ull;
 }
 
-// Pass 2 (one block): totals over blocks in block order (double), then
-// f = count / (T k), P = sum p / T, aux = E sum f P, CV^2 of importance.
-__global__ void __launch_bounds__(1024) aux_final_kernel(int T, int E, int k, int nblk,
-                                                         float w_imp,
-                                                         const float* __restrict__ part,
-                                                         float* f, float* P, float* I,
-                                                         float* out3) {
-    __shared__ double sfp[1024], simp[1024];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        double sp = 0.0, si = 0.0, sc = 0.0;
-        for (int b = 0; b < nblk; ++b) {
-            const float* pb = part + (size_t)b * 3 * E;
-            sp += pb[e];
-            si += pb[E + e];
-            sc += pb[2 * E + e];
-        }
-        const double fe = sc / ((double)T * (double)k);
-        const double Pe = sp / (double)T;
-        if (f) f[e] = (float)fe;
-        if (P) P[e] = (float)Pe;
-        if (I) I[e] = (float)si;
-        sfp[e] = fe * Pe;
-        simp[e] = si;
+// fixed-order sum over a block of doubles (one value per thread)
+__device__ double block_sum_fixed(double v, double* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    double tot = 0.0;
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += scratch[w];
+        scratch[32] = tot;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        double aux = 0.0, mean = 0.0;
-        for (int e = 0; e < E; ++e) {
-            aux += sfp[e];
-            mean += simp[e];
+    tot = scratch[32];
+    __syncthreads();
+    return tot;
+}
+
+__global__ void __launch_bounds__(256) aux_kernel(int T, int E, int k, int nblk, float w_imp,
+                                                  const float* __restrict__ probs,
+                                                  const int32_t* __restrict__ ids,
+                                                  const float* __restrict__ w, AuxAcc acc,
+                                                  float* f, float* P, float* I, float* out3) {
+    extern __shared__ unsigned long long sm64[];
+    unsigned long long* sP = sm64;
+    unsigned long long* sI = sm64 + E;
+    unsigned int* sC = reinterpret_cast<unsigned int*>(sm64 + 2 * E);
+    __shared__ double red[33];
+    __shared__ int is_last;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        sP[e] = 0;
+        sI[e] = 0;
+        sC[e] = 0;
+    }
+    __syncthreads();
+    const int t0 = blockIdx.x * kAuxBlockTokens;
+    const int nt = min(kAuxBlockTokens, T - t0);
+    // column sums of probs: thread -> (column e, every rstep-th row)
+    const int rstep = E <= (int)blockDim.x ? (int)blockDim.x / E : 1;
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+        const int e = e0 + (int)threadIdx.x % min(E, (int)blockDim.x);
+        const int r0 = E <= (int)blockDim.x ? (int)threadIdx.x / E : 0;
+        if (e < E && r0 < rstep) {
+            unsigned long long acc_p = 0;
+            for (int r = r0; r < nt; r += rstep) acc_p += to_fix(probs[(size_t)(t0 + r) * E + e]);
+            atomicAdd(&sP[e], acc_p);
         }
-        mean /= (double)E;
-        double var = 0.0;
-        for (int e = 0; e < E; ++e) var += (simp[e] - mean) * (simp[e] - mean);
-        var /= (double)E;
+        if (E <= (int)blockDim.x) break;
+    }
+    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+        const int e = ids[(size_t)t0 * k + i];
+        if (e < 0 || e >= E) continue;
+        atomicAdd(&sI[e], to_fix(w[(size_t)t0 * k + i]));
+        atomicAdd(&sC[e], 1u);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (sP[e]) atomicAdd(&acc.P[e], sP[e]);
+        if (sI[e]) atomicAdd(&acc.I[e], sI[e]);
+        if (sC[e]) atomicAdd(&acc.cnt[e], sC[e]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(acc.ticket, 1u) == (unsigned)(nblk - 1);
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // last block: totals -> statistics (fixed-order reductions), then reset
+    const double inv_fix = 1.0 / 4294967296.0;
+    double s_fp = 0.0, s_i = 0.0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const double pe = (double)__ldcg(&acc.P[e]) * inv_fix / (double)T;
+        const double ie = (double)__ldcg(&acc.I[e]) * inv_fix;
+        const double fe = (double)__ldcg(&acc.cnt[e]) / ((double)T * (double)k);
+        if (f) f[e] = (float)fe;
+        if (P) P[e] = (float)pe;
+        if (I) I[e] = (float)ie;
+        s_fp += fe * pe;
+        s_i += ie;
+    }
+    const double sum_fp = block_sum_fixed(s_fp, red);
+    const double mean = block_sum_fixed(s_i, red) / (double)E;
+    double s_v = 0.0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const double d = (double)__ldcg(&acc.I[e]) * inv_fix - mean;
+        s_v += d * d;
+    }
+    const double var = block_sum_fixed(s_v, red) / (double)E;
+    if (threadIdx.x == 0) {
         const double cv2 = var / (mean * mean);
-        out3[0] = (float)(aux * (double)E);
+        out3[0] = (float)(sum_fp * (double)E);
         out3[1] = (float)cv2;
         out3[2] = (float)((double)w_imp * cv2);
     }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        acc.P[e] = 0;
+        acc.I[e] = 0;
+        acc.cnt[e] = 0;
+    }
+    if (threadIdx.x == 0) *acc.ticket = 0;
 }
 
 cudaError_t launch_aux(const Shape& s, const float* probs, const int32_t* ids, const float* w,
-                       float* part, float* f, float* P, float* I, float* out3,
+                       void* acc_mem, float* f, float* P, float* I, float* out3,
                        cudaStream_t st) {
     const int nblk = (s.T + kAuxBlockTokens - 1) / kAuxBlockTokens;
-    const size_t smem = (size_t)kAuxBlockTokens * s.k * (sizeof(int32_t) + sizeof(float));
-    aux_partial_kernel<<<nblk, 256, smem, st>>>(s.T, s.E, s.k, probs, ids, w, part);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    aux_final_kernel<<<1, 1024, 0, st>>>(s.T, s.E, s.k, nblk, s.w_imp, part, f, P, I, out3);
+    AuxAcc acc;
+    acc.P = static_cast<unsigned long long*>(acc_mem);
+    acc.I = acc.P + s.E;
+    acc.cnt = reinterpret_cast<unsigned int*>(acc.I + s.E);
+    acc.ticket = acc.cnt + s.E;
+    const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int)) + 8;
+    aux_kernel<<<nblk, 256, smem, st>>>(s.T, s.E, s.k, nblk, s.w_imp, probs, ids, w, acc, f, P,
+                                        I, out3);
     return cudaGetLastError();
 }
 

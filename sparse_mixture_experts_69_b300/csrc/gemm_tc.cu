@@ -23,11 +23,33 @@
 
 #include "group_table.cuh"
 
+// Compile-time tuning knobs (defaults are the measured best on B300).
+#ifndef MOE_TC_KH
+#define MOE_TC_KH 1  // 64-wide K halves per pipeline stage (1 or 2)
+#endif
+#ifndef MOE_TC_PROMO
+#define MOE_TC_PROMO 2  // L2 promotion of TMA loads: 0 none, 1 128 B, 2 256 B
+#endif
+#ifndef MOE_TC_HINT
+#define MOE_TC_HINT 0  // 1: weight tiles evict-first, activation tiles evict-last
+#endif
+#ifndef MOE_TC_ROT
+#define MOE_TC_ROT 0  // 1: each tile starts its k loop at a tile-dependent block
+#endif
+#ifndef MOE_TC_BN_ACT
+#define MOE_TC_BN_ACT 256  // output tile width of the ReLU/GELU/plain expert GEMMs
+#endif
+#ifndef MOE_TC_SMEM
+#define MOE_TC_SMEM (192 * 1024)  // shared memory for the pipeline stages
+#endif
+
 namespace moe {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle atom row
+constexpr int KH = MOE_TC_KH;
+constexpr int BKH = 64;      // 64 bf16 = 128 bytes = one swizzle atom row
+constexpr int BK = BKH * KH; // K per pipeline stage
 constexpr int kThreads = 192;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
@@ -43,10 +65,13 @@ struct TcArgs {
 
 template <int BN>
 struct Cfg {
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int A_HALF = BM * BKH * 2;  // one 64-wide K half of the A tile
+    static constexpr int B_HALF = BN * BKH * 2;
+    static constexpr int A_BYTES = A_HALF * KH;
+    static constexpr int B_BYTES = B_HALF * KH;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN >= 256 ? 4 : BN >= 128 ? 6 : 8;
+    static constexpr int STAGES_FIT = MOE_TC_SMEM / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // power of two for BN in {32..256}
     static constexpr int B_BOX_ROWS = BN < 128 ? BN : 128;
     static constexpr int B_LOADS = BN / B_BOX_ROWS;
@@ -115,6 +140,24 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                 int x, int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -217,20 +260,26 @@ __device__ __forceinline__ float act_apply(int act, float u) {
 }
 __device__ __forceinline__ float silu(float u) { return u / (1.f + expf(-u)); }
 
-// Store n (<= 32, multiple of 8 when vec) bf16 values of one row.
-__device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* v, int n) {
-    if (n >= 32) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// Store NV (multiple of 8) bf16 values of one row; n = how many are in range.
+template <int NV>
+__device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float (&v)[NV], int n) {
+    if (n >= NV) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 pk;
-            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
-            d4[q] = pk;
+        for (int q = 0; q < NV / 8; ++q) {
+            uint4 pk = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
+                                  pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                  pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                                  pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            reinterpret_cast<uint4*>(dst)[q] = pk;
         }
     } else {
-        for (int i = 0; i < n; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if (i < n) dst[i] = __float2bfloat16_rn(v[i]);
     }
 }
 
@@ -298,6 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            const uint64_t pol_a = MOE_TC_HINT ? policy_evict_last() : 0;
+            const uint64_t pol_b = MOE_TC_HINT ? policy_evict_first() : 0;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;
@@ -315,17 +366,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else
                         brow[h] = gt.b_row + gt.n_tile * BN + h * C::B_BOX_ROWS;
                 }
-                for (int kb = 0; kb < nkb; ++kb) {
+                const int rot = MOE_TC_ROT ? tile % nkb : 0;
+                for (int kb0 = 0; kb0 < nkb; ++kb0) {
+                    const int kb = kb0 + rot < nkb ? kb0 + rot : kb0 + rot - nkb;
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, kTimeoutNs)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    tma_load_2d(sA + stage * C::A_BYTES, ma, &full[stage], kb * BK, gt.a_row);
 #pragma unroll
-                    for (int h = 0; h < C::B_LOADS; ++h)
-                        tma_load_2d(sB + stage * C::B_BYTES + h * C::B_BOX_ROWS * 128, mb,
-                                    &full[stage], kb * BK, brow[h]);
+                    for (int hk = 0; hk < KH; ++hk) {
+                        const int kx = kb * BK + hk * BKH;
+                        uint8_t* a_dst = sA + stage * C::A_BYTES + hk * C::A_HALF;
+                        uint8_t* b_dst = sB + stage * C::B_BYTES + hk * C::B_HALF;
+                        if (MOE_TC_HINT) {
+                            tma_load_2d_hint(a_dst, ma, &full[stage], kx, gt.a_row, pol_a);
+#pragma unroll
+                            for (int h = 0; h < C::B_LOADS; ++h)
+                                tma_load_2d_hint(b_dst + h * C::B_BOX_ROWS * 128, mb, &full[stage],
+                                                 kx, brow[h], pol_b);
+                        } else {
+                            tma_load_2d(a_dst, ma, &full[stage], kx, gt.a_row);
+#pragma unroll
+                            for (int h = 0; h < C::B_LOADS; ++h)
+                                tma_load_2d(b_dst + h * C::B_BOX_ROWS * 128, mb, &full[stage], kx,
+                                            brow[h]);
+                        }
+                    }
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -366,12 +433,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_sw128(smem_u32(sA + stage * C::A_BYTES));
-                    const uint64_t bd = sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, C::IDESC,
-                                  (kb | kk) != 0 ? 1u : 0u);
+                    for (int hk = 0; hk < KH; ++hk) {
+                        const uint64_t ad =
+                            sdesc_sw128(smem_u32(sA + stage * C::A_BYTES + hk * C::A_HALF));
+                        const uint64_t bd =
+                            sdesc_sw128(smem_u32(sB + stage * C::B_BYTES + hk * C::B_HALF));
+#pragma unroll
+                        for (int kk = 0; kk < BKH / 16; ++kk)
+                            umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, C::IDESC,
+                                      (kb | hk | kk) != 0 ? 1u : 0u);
+                    }
                     umma_commit(&empty[stage]);
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -425,29 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (EPI == EPI_GLU) {
 #pragma unroll 1
                     for (int c = 0; c < 128; c += 16) {
-                        float g[16], u[16], v[32];
+                        float g[16], u[16], v16[16];
                         tmem_ld16x2(taddr + c, taddr + 128 + c, g, u);
                         const int n0 = gt.n_tile * 128 + c;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = silu(g[i]) * u[i];
-                        if (rv && n0 < p.N) {
-                            const int n = min(16, p.N - n0);
-                            if (n == 16) {
-                                uint4* d4 = reinterpret_cast<uint4*>(orow + n0);
-#pragma unroll
-                                for (int qq = 0; qq < 2; ++qq) {
-                                    uint4 pk;
-                                    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i)
-                                        h[i] = __floats2bfloat162_rn(v[8 * qq + 2 * i],
-                                                                     v[8 * qq + 2 * i + 1]);
-                                    d4[qq] = pk;
-                                }
-                            } else {
-                                for (int i = 0; i < n; ++i) orow[n0 + i] = __float2bfloat16_rn(v[i]);
-                            }
-                        }
+                        for (int i = 0; i < 16; ++i) v16[i] = silu(g[i]) * u[i];
+                        if (rv && n0 < p.N) store_bf16_row<16>(orow + n0, v16, p.N - n0);
                     }
                 } else {
                     const int act = p.glu ? -1 : p.act;
@@ -459,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (rv && n0 < p.N) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = act_apply(act, v[i]);
-                            store_bf16_row(orow + n0, v, min(32, p.N - n0));
+                            store_bf16_row<32>(orow + n0, v, p.N - n0);
                         }
                     }
                 }
@@ -501,11 +556,14 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int b
     if (!fn) return false;
     cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)BKH, (cuuint32_t)box_rows};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
                     box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    MOE_TC_PROMO == 0   ? CU_TENSOR_MAP_L2_PROMOTION_NONE
+                    : MOE_TC_PROMO == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                        : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -539,13 +597,11 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
 
 }  // namespace tc
 
-size_t tc_smem_bytes_max(int G) { return tc::Cfg<256>::smem_bytes(G); }
-
 cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStream_t st) {
     tc::TcArgs a{};
     a.p = g;
     if (g.glu) return tc::launch<256, tc::EPI_GLU>(a, st);
-    return tc::launch<256, tc::EPI_ACT>(a, st);
+    return tc::launch<MOE_TC_BN_ACT, tc::EPI_ACT>(a, st);
 }
 
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,

@@ -60,8 +60,7 @@ WsLayout ws_layout(const Shape& s) {
     L.h = take((R + S * T) * F * es);
     L.yp = take(R * d * es);
     L.ys = take(S * T * d * es);
-    const size_t nblk_aux = (T + kAuxBlockTokens - 1) / kAuxBlockTokens;
-    L.aux_part = take(nblk_aux * 3 * E * 4);
+    L.aux_acc = take(E * (8 + 8 + 4) + 16);
     L.aux_vecs = take(3 * E * 4);
     L.out3 = take(16);
     L.total = off;
@@ -268,6 +267,8 @@ MOE_API moe_status moe_workspace_reset(const moe_config* cfg, void* ws, size_t w
     MOE_TRY(make_shape(cfg, &s));
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
     MOE_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, 256, (cudaStream_t)stream));
+    MOE_CUDA(cudaMemsetAsync(at<char>(ws, L.aux_acc), 0, (size_t)s.E * 20 + 16,
+                             (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -353,7 +354,7 @@ MOE_API moe_status moe_aux_stats(const moe_config* cfg, const float* probs,
     MOE_TRY(make_shape(cfg, &s));
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
     if (!probs || !topk_ids || !topk_w || !out3) return MOE_ERR_INVALID_ARG;
-    MOE_CUDA(launch_aux(s, probs, topk_ids, topk_w, at<float>(ws, L.aux_part), f, P, importance,
+    MOE_CUDA(launch_aux(s, probs, topk_ids, topk_w, at<void>(ws, L.aux_acc), f, P, importance,
                         out3, (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -404,7 +405,7 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
     MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
     float* av = aux_vecs ? aux_vecs : at<float>(ws, L.aux_vecs);
     float* o3 = out3 ? out3 : at<float>(ws, L.out3);
-    MOE_CUDA(launch_aux(s, probs, ids, w, at<float>(ws, L.aux_part), av, av + s.E, av + 2 * s.E,
+    MOE_CUDA(launch_aux(s, probs, ids, w, at<void>(ws, L.aux_acc), av, av + s.E, av + 2 * s.E,
                         o3, st));
     return MOE_OK;
 }

@@ -48,14 +48,14 @@ struct WsLayout {
     size_t h;          // [R_max + S T, F] dtype
     size_t yp;         // [R_max,d] dtype (layer only)
     size_t ys;         // [S T, d] dtype (layer only)
-    size_t aux_part;   // [nblk_aux, 3E] f32
+    size_t aux_acc;    // statistics accumulators: [2E] u64, [E] u32, ticket (zero between calls)
     size_t aux_vecs;   // [3E] f32 (layer only)
     size_t out3;       // [4] f32 (layer only)
     size_t total;
 };
 
 constexpr int kCapBlockTokens = 256;  // tokens per block of the capacity kernels
-constexpr int kAuxBlockTokens = 128;  // tokens per block of the statistics kernel
+constexpr int kAuxBlockTokens = 256;  // tokens per block of the statistics kernel
 
 WsLayout ws_layout(const Shape& s);
 
@@ -114,7 +114,7 @@ cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream
 cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, const float* w,
                            const void* ys, void* y, int* status, cudaStream_t st);
 cudaError_t launch_aux(const Shape& s, const float* probs, const int32_t* ids, const float* w,
-                       float* part, float* f, float* P, float* I, float* out3,
+                       void* acc_mem, float* f, float* P, float* I, float* out3,
                        cudaStream_t st);
 cudaError_t launch_bias_update(const Shape& s, const int32_t* counts, float* bias, float rate,
                                cudaStream_t st);
