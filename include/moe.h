@@ -203,6 +203,30 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
                                  int32_t* counts, float* aux_vecs, float* out3, void* ws,
                                  size_t ws_bytes, moe_stream_t stream);
 
+/* Statistics without a workspace. The pages have no counterpart to this call.
+ *
+ * Same inputs, outputs and results as moe_aux_stats, for callers that cannot
+ * hand the library any device memory of their own: for instance a plugin
+ * running inside a host framework that owns every allocation and gives its
+ * plugins no workspace, or code on a path where allocating (and the implicit
+ * synchronisation that can come with it) is not allowed. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Its scratch (the fixed-point accumulators) is a file-scope device array
+ * inside libmoe.so sized for at most 512 experts (10,256 bytes); every GPU
+ * that loads the library holds one copy until the process exits. n_experts
+ * above 512 returns MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up that array's device address (with
+ *     the device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     each call clears it on its stream before use. Calls whose work overlaps
+ *     on the GPU (other streams, other threads) race on it: serialise them. */
+MOE_API moe_status moe_aux_stats_noalloc(const moe_config* cfg, const float* probs,
+                                         const int32_t* topk_ids, const float* topk_w,
+                                         float* f, float* P, float* importance, float* out3,
+                                         moe_stream_t stream);
+
 /* Synchronise `stream`, read and clear the workspace status word, and map it
  * to MOE_OK, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_ARG (the
  * first set, in that order of precedence: TIMEOUT, DEVICE_ARG, NONFINITE). */

@@ -3,6 +3,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -428,3 +429,56 @@ MOE_API moe_status moe_read_device_error(const moe_config* cfg, void* ws, size_t
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ statistics without a workspace
+// moe_aux_stats_noalloc keeps its accumulators in this file-scope device array
+// instead of a caller-provided workspace. Every GPU that loads the library
+// holds one copy until the process exits. It fits up to
+// MOE_AUX_NOALLOC_MAX_EXPERTS experts: two u64 sums and one u32 count per
+// expert, plus the ticket counter of the statistics kernel.
+#define MOE_AUX_NOALLOC_MAX_EXPERTS 512
+static __device__ __align__(256) unsigned char g_aux_noalloc_scratch[MOE_AUX_NOALLOC_MAX_EXPERTS * 20 + 16];
+
+namespace {
+
+// Host code may not hand g_aux_noalloc_scratch itself to a kernel: on the host
+// that name is a stand-in, not a device address. Its device address is
+// looked up once per device, with that device current, and cached.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+moe_status noalloc_scratch_current_device(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_aux_noalloc_scratch) != cudaSuccess || !ptr)
+            return MOE_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" MOE_API moe_status moe_aux_stats_noalloc(const moe_config* cfg, const float* probs,
+                                                    const int32_t* topk_ids,
+                                                    const float* topk_w, float* f, float* P,
+                                                    float* importance, float* out3,
+                                                    moe_stream_t stream) {
+    Shape s;
+    MOE_TRY(make_shape(cfg, &s));
+    if (!probs || !topk_ids || !topk_w || !out3) return MOE_ERR_INVALID_ARG;
+    if (s.E > MOE_AUX_NOALLOC_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    MOE_TRY(noalloc_scratch_current_device(&scratch));
+    cudaStream_t st = (cudaStream_t)stream;
+    // the array keeps whatever the previous call left: start this call from zero
+    MOE_CUDA(cudaMemsetAsync(scratch, 0, (size_t)s.E * 20 + 16, st));
+    MOE_CUDA(launch_aux(s, probs, topk_ids, topk_w, scratch, f, P, importance, out3, st));
+    return MOE_OK;
+}

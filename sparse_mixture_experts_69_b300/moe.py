@@ -85,6 +85,7 @@ _SIGS = {
     "moe_bias_update": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, _P]),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_P] * 16 + [_P, ctypes.c_size_t, _P]),
     "moe_read_device_error": (ctypes.c_int, [_CFG, _P, ctypes.c_size_t, _P]),
+    "moe_aux_stats_noalloc": (ctypes.c_int, [_CFG] + [_P] * 7 + [_P]),
 }
 
 
@@ -183,6 +184,15 @@ def moe_aux_stats(cfg: Config, probs, topk_ids, topk_w, f, P, importance, out3, 
     _check(lib().moe_aux_stats(ctypes.byref(cfg.c()), _p(probs), _p(topk_ids), _p(topk_w), _p(f),
                                _p(P), _p(importance), _p(out3), _p(ws), ws.numel(), _s(stream)),
            "moe_aux_stats")
+
+
+def moe_aux_stats_noalloc(cfg: Config, probs, topk_ids, topk_w, f, P, importance, out3,
+                          stream=None):
+    """moe_aux_stats without a workspace: the library's own device scratch is used
+    (at most 512 experts; calls must not overlap on the GPU)."""
+    _check(lib().moe_aux_stats_noalloc(ctypes.byref(cfg.c()), _p(probs), _p(topk_ids),
+                                       _p(topk_w), _p(f), _p(P), _p(importance), _p(out3),
+                                       _s(stream)), "moe_aux_stats_noalloc")
 
 
 def moe_bias_update(cfg: Config, counts, bias, rate: float, stream=None):
