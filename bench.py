@@ -364,27 +364,37 @@ def main():
     yp = torch.empty((R_max, d), dtype=c.torch_dtype, device=dev)
     ys = torch.empty((c.n_shared, T, d), dtype=c.torch_dtype, device=dev) if c.n_shared else None
     fP = torch.empty((3, E), device=dev)
-    n_split = max(10, min(200, a.steps // 10))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_split)]
-    for i in range(n_split + 3):
-        e = evs[i - 3] if i >= 3 else None
-        if e: e[0].record(stream)
-        moe.moe_route(c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"],
-                      bias, logits, probs, None, ids, w, 0, ws, stream)
-        if e: e[1].record(stream)
-        moe.moe_dispatch(c, inp["x"], ids, counts, kept, offsets, slot, xp, row_token, ws, stream)
-        if e: e[2].record(stream)
-        moe.moe_expert_ffn(c, xp, offsets, inp["W1"], inp["W2"], inp["x"], inp["W1s"], inp["W2s"],
-                           yp, ys, ws, stream)
-        if e: e[3].record(stream)
-        moe.moe_combine(c, yp, slot, w, ys, y, ws, stream)
-        if e: e[4].record(stream)
-        moe.moe_aux_stats(c, probs, ids, w, fP[0], fP[1], fP[2], out3, ws, stream)
-        if e: e[5].record(stream)
-    torch.cuda.synchronize()
-    names = ["route", "dispatch", "expert_ffn", "combine", "aux"]
-    stage_ms = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
-                for j, n in enumerate(names)}
+    # each stage alone, called back to back so the device queue never runs dry
+    def time_calls(fn, n):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    n_split = max(20, min(200, a.steps // 10))
+    stage_ms = {
+        "route": time_calls(lambda: moe.moe_route(
+            c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"], bias,
+            logits, probs, None, ids, w, 0, ws, stream), n_split),
+        "dispatch": time_calls(lambda: moe.moe_dispatch(
+            c, inp["x"], ids, counts, kept, offsets, slot, xp, row_token, ws, stream), n_split),
+        "expert_ffn": time_calls(lambda: moe.moe_expert_ffn(
+            c, xp, offsets, inp["W1"], inp["W2"], inp["x"], inp["W1s"], inp["W2s"], yp, ys, ws,
+            stream), n_split),
+        "combine": time_calls(lambda: moe.moe_combine(c, yp, slot, w, ys, y, ws, stream),
+                              n_split),
+        "aux": time_calls(lambda: moe.moe_aux_stats(c, probs, ids, w, fP[0], fP[1], fP[2], out3,
+                                                    ws, stream), n_split),
+    }
+    st = moe.moe_read_device_error(c, ws)
+    if st != 0:
+        raise RuntimeError("device status after the stage timing: " + moe.moe_status_string(st))
 
     # algorithmic work of the expert FFN (two grouped-GEMM launches)
     kept_h = kept.cpu()
@@ -439,7 +449,9 @@ def main():
     d2h = y_host.numel() * y_host.element_size() + 12
     e2e_value = world * T * K2 / e2e_s
 
-    launches_per_step = (3 if c.dtype == 1 else 2) + 4 + 2 + 1 + 2 + (1 if wl.bias_rate else 0)
+    # layer path: [Wg transpose (bf16)], router GEMM, fused selection + histogram +
+    # statistics, capacity scan, slots, permute, up GEMM, down GEMM, combine
+    launches_per_step = (9 if c.dtype == 1 else 8) + (1 if wl.bias_rate else 0)
 
     if rank != 0:
         return 0

@@ -22,7 +22,7 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-// blk_hist is expert-major: [E][nblk]
+// blk_hist is expert-major: [E][nblk]; written whole here (no atomics into it)
 __global__ void __launch_bounds__(kCapBlockTokens) cap_hist_kernel(
     int T, int k, int E, int nblk, const int32_t* __restrict__ ids, int32_t* __restrict__ blk_hist,
     int* status) {
@@ -61,7 +61,7 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 
 // One block of 1024 threads. Warp w scans experts w, w+32, ...
 __global__ void __launch_bounds__(1024) cap_scan_kernel(
-    int nblk, int E, int C, const int32_t* __restrict__ blk_hist, int32_t* __restrict__ blk_base,
+    int nblk, int E, int C, int32_t* __restrict__ blk_hist, int32_t* __restrict__ blk_base,
     int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets) {
     __shared__ int kp[1024];
     __shared__ int wsum[32];
@@ -70,7 +70,11 @@ __global__ void __launch_bounds__(1024) cap_scan_kernel(
         int running = 0;
         for (int b0 = 0; b0 < nblk; b0 += 32) {
             int b = b0 + lane;
-            int v = b < nblk ? blk_hist[(size_t)e * nblk + b] : 0;
+            int v = 0;
+            if (b < nblk) {
+                v = blk_hist[(size_t)e * nblk + b];
+                blk_hist[(size_t)e * nblk + b] = 0;  // counters start at zero for the next call
+            }
             int incl = warp_incl_scan(v);
             if (b < nblk) blk_base[(size_t)e * nblk + b] = running + incl - v;
             running += __shfl_sync(0xffffffffu, incl, 31);
@@ -137,12 +141,16 @@ __global__ void __launch_bounds__(kCapBlockTokens) cap_slot_kernel(
 
 cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_hist,
                             int32_t* blk_base, int32_t* counts, int32_t* kept, int32_t* offsets,
-                            int32_t* slot, int32_t* row_token, int* status, cudaStream_t st) {
+                            int32_t* slot, int32_t* row_token, int* status, bool hist_ready,
+                            cudaStream_t st) {
     const int nblk = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
-    cap_hist_kernel<<<nblk, kCapBlockTokens, s.E * sizeof(int), st>>>(s.T, s.k, s.E, nblk, ids,
-                                                                      blk_hist, status);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    cudaError_t err;
+    if (!hist_ready) {
+        cap_hist_kernel<<<nblk, kCapBlockTokens, s.E * sizeof(int), st>>>(s.T, s.k, s.E, nblk,
+                                                                          ids, blk_hist, status);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
     cap_scan_kernel<<<1, 1024, 0, st>>>(nblk, s.E, s.C, blk_hist, blk_base, counts, kept,
                                         offsets);
     err = cudaGetLastError();

@@ -633,9 +633,14 @@ cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const
     a.logits = logits;
     a.zn = zn;
     a.E_router = s.E;
-    if (Nr <= 32) return tc::launch<32, tc::EPI_ROUTER>(a, st);
-    if (Nr <= 64) return tc::launch<64, tc::EPI_ROUTER>(a, st);
-    if (Nr <= 128) return tc::launch<128, tc::EPI_ROUTER>(a, st);
+    // Narrowest tile that covers Nr, halved while that leaves too few tiles to
+    // keep most SMs streaming x (the router reads T d b bytes of x and little else).
+    const int mt = (s.T + tc::BM - 1) / tc::BM;
+    int bn = Nr <= 32 ? 32 : Nr <= 64 ? 64 : Nr <= 128 ? 128 : 256;
+    while (bn > 32 && mt * ((Nr + bn - 1) / bn) < (3 * num_sms()) / 4) bn >>= 1;
+    if (bn == 32) return tc::launch<32, tc::EPI_ROUTER>(a, st);
+    if (bn == 64) return tc::launch<64, tc::EPI_ROUTER>(a, st);
+    if (bn == 128) return tc::launch<128, tc::EPI_ROUTER>(a, st);
     return tc::launch<256, tc::EPI_ROUTER>(a, st);
 }
 

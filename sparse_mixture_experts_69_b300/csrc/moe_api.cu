@@ -42,7 +42,11 @@ WsLayout ws_layout(const Shape& s) {
     };
     const size_t T = s.T, E = s.E, k = s.k, d = s.d, F = s.F, S = s.S, R = s.R_max;
     const size_t es = s.esize;
+    const size_t nblk = (T + kCapBlockTokens - 1) / kCapBlockTokens;
     L.status = take(256);
+    L.aux_acc = take(E * (8 + 8 + 4) + 16);
+    L.blk_hist = take(nblk * E * 4);
+    L.zero_end = off;
     L.zn = take(T * E * 4);
     L.wgT = take(2 * E * d * es);
     L.logits = take(T * E * 4);
@@ -54,14 +58,11 @@ WsLayout ws_layout(const Shape& s) {
     L.kept = take(E * 4);
     L.offsets = take((E + 1) * 4);
     L.row_token = take(R * 4);
-    const size_t nblk = (T + kCapBlockTokens - 1) / kCapBlockTokens;
-    L.blk_hist = take(nblk * E * 4);
     L.blk_base = take(nblk * E * 4);
     L.xp = take(R * d * es);
     L.h = take((R + S * T) * F * es);
     L.yp = take(R * d * es);
     L.ys = take(S * T * d * es);
-    L.aux_acc = take(E * (8 + 8 + 4) + 16);
     L.aux_vecs = take(3 * E * 4);
     L.out3 = take(16);
     L.total = off;
@@ -141,10 +142,12 @@ T* at(void* ws, size_t off) {
     } while (0)
 
 // -------------------------------------------------------------- stage bodies
+// aux: if non-NULL ([3E] f, P, importance followed by out3 at aux_out3), the
+// selection kernel also counts the capacity histogram and the statistics.
 moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x, const void* Wg,
                       const void* Wnoise, const float* noise, const float* offset,
                       const float* bias, float* logits, float* probs, float* sel, int32_t* ids,
-                      float* w, cudaStream_t st) {
+                      float* w, float* aux_vecs, float* aux_out3, cudaStream_t st) {
     int* status = at<int>(ws, L.status);
     const bool noisy = Wnoise != nullptr;
     const int Nr = noisy ? 2 * s.E : s.E;
@@ -159,17 +162,25 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x
                                         static_cast<const float*>(Wnoise), offset, logits, zn,
                                         st));
     }
-    MOE_CUDA(launch_router_select(s, logits, zn, noisy ? noise : nullptr, bias, probs, sel, ids,
-                                  w, 0, nullptr, nullptr, status, st));
+    if (aux_out3) {
+        MOE_CUDA(launch_router_select_fused(s, logits, zn, noisy ? noise : nullptr, bias, probs,
+                                            ids, w, status, at<int32_t>(ws, L.blk_hist),
+                                            at<void>(ws, L.aux_acc), aux_vecs, aux_vecs + s.E,
+                                            aux_vecs + 2 * s.E, aux_out3, st));
+    } else {
+        MOE_CUDA(launch_router_select(s, logits, zn, noisy ? noise : nullptr, bias, probs, sel,
+                                      ids, w, 0, nullptr, nullptr, status, st));
+    }
     return MOE_OK;
 }
 
 moe_status dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const void* x,
                          const int32_t* ids, int32_t* counts, int32_t* kept, int32_t* offsets,
-                         int32_t* slot, void* xp, int32_t* row_token, cudaStream_t st) {
+                         int32_t* slot, void* xp, int32_t* row_token, bool hist_ready,
+                         cudaStream_t st) {
     int* status = at<int>(ws, L.status);
     MOE_CUDA(launch_capacity(s, ids, at<int32_t>(ws, L.blk_hist), at<int32_t>(ws, L.blk_base),
-                             counts, kept, offsets, slot, row_token, status, st));
+                             counts, kept, offsets, slot, row_token, status, hist_ready, st));
     MOE_CUDA(launch_permute(s, x, slot, xp, st));
     return MOE_OK;
 }
@@ -267,9 +278,7 @@ MOE_API moe_status moe_workspace_reset(const moe_config* cfg, void* ws, size_t w
     WsLayout L;
     MOE_TRY(make_shape(cfg, &s));
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
-    MOE_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, 256, (cudaStream_t)stream));
-    MOE_CUDA(cudaMemsetAsync(at<char>(ws, L.aux_acc), 0, (size_t)s.E * 20 + 16,
-                             (cudaStream_t)stream));
+    MOE_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -297,7 +306,7 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* W
     if (!aligned16(x) || !aligned16(Wg) || (Wnoise && !aligned16(Wnoise)))
         return MOE_ERR_UNSUPPORTED;
     return route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
-                      sel_scores, topk_ids, topk_w, st);
+                      sel_scores, topk_ids, topk_w, nullptr, nullptr, st);
 }
 
 MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_ids,
@@ -312,7 +321,7 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int3
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_UNSUPPORTED;
     return dispatch_impl(s, L, ws, x, topk_ids, counts, kept, offsets, slot, xp, row_token,
-                         (cudaStream_t)stream);
+                         false, (cudaStream_t)stream);
 }
 
 MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
@@ -399,15 +408,15 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
     void* xp = at<void>(ws, L.xp);
     void* yp = at<void>(ws, L.yp);
     void* ys = at<void>(ws, L.ys);
-    MOE_TRY(route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
-                       nullptr, ids, w, st));
-    MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token, st));
-    MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, st));
-    MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
     float* av = aux_vecs ? aux_vecs : at<float>(ws, L.aux_vecs);
     float* o3 = out3 ? out3 : at<float>(ws, L.out3);
-    MOE_CUDA(launch_aux(s, probs, ids, w, at<void>(ws, L.aux_acc), av, av + s.E, av + 2 * s.E,
-                        o3, st));
+    // route + capacity histogram + statistics, then scan/slots, permute,
+    // expert GEMMs, combine
+    MOE_TRY(route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
+                       nullptr, ids, w, av, o3, st));
+    MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token, true, st));
+    MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, st));
+    MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
     return MOE_OK;
 }
 

@@ -30,7 +30,11 @@ struct Shape {
 // Workspace layout (byte offsets, each 256-aligned). One layout serves every
 // entry point so the stages can be called separately on the same buffer.
 struct WsLayout {
+    // regions that must read zero between calls come first (moe_workspace_reset)
     size_t status;     // int32 status word (+ padding)
+    size_t aux_acc;    // statistics accumulators: [2E] u64, [E] u32, ticket
+    size_t blk_hist;   // [E][nblk] i32 capacity histogram counters
+    size_t zero_end;   // end of the zero-between-calls prefix
     size_t zn;         // [T,E] f32 noise logits x.Wnoise
     size_t wgT;        // [Nr,d] dtype: Wg^T (rows 0..E-1) and Wnoise^T (E..2E-1)
     size_t logits;     // [T,E] f32 (layer only)
@@ -42,13 +46,11 @@ struct WsLayout {
     size_t kept;       // [E] i32 (layer only)
     size_t offsets;    // [E+1] i32 (layer only)
     size_t row_token;  // [R_max] i32 (layer only)
-    size_t blk_hist;   // [nblk,E] i32
-    size_t blk_base;   // [nblk,E] i32
+    size_t blk_base;   // [E][nblk] i32
     size_t xp;         // [R_max,d] dtype (layer only)
     size_t h;          // [R_max + S T, F] dtype
     size_t yp;         // [R_max,d] dtype (layer only)
     size_t ys;         // [S T, d] dtype (layer only)
-    size_t aux_acc;    // statistics accumulators: [2E] u64, [E] u32, ticket (zero between calls)
     size_t aux_vecs;   // [3E] f32 (layer only)
     size_t out3;       // [4] f32 (layer only)
     size_t total;
@@ -81,10 +83,20 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
                                  const float* sel_in, const float* probs_in, int* status,
                                  cudaStream_t st);
 
+// Layer path: selection + capacity histogram + statistics in one kernel
+cudaError_t launch_router_select_fused(const Shape& s, const float* logits, const float* zn,
+                                       const float* noise, const float* bias, float* probs,
+                                       int32_t* ids, float* w, int* status, int32_t* blk_hist,
+                                       void* acc_mem, float* f, float* P, float* I, float* out3,
+                                       cudaStream_t st);
+
 // Capacity: histogram -> scan -> slots; then the permute of x rows into xp
+// hist_ready: blk_hist already holds the per-block histograms (the fused router
+// kernel counted them), so only the scan and slot kernels run.
 cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_hist,
                             int32_t* blk_base, int32_t* counts, int32_t* kept, int32_t* offsets,
-                            int32_t* slot, int32_t* row_token, int* status, cudaStream_t st);
+                            int32_t* slot, int32_t* row_token, int* status, bool hist_ready,
+                            cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
                            cudaStream_t st);
 

@@ -7,7 +7,9 @@
 // ld246.com MoE Q3 (bias on the softmax scores, for the top-k choice only).
 #include <float.h>
 
-#include "moe_internal.cuh"
+#include <algorithm>
+
+#include "aux_common.cuh"
 
 namespace moe {
 
@@ -126,15 +128,16 @@ __device__ __forceinline__ float softplus_f(float u) {
     return fmaxf(u, 0.f) + log1pf(expf(-fabsf(u)));
 }
 
-// One warp per token; lane l holds experts l, l+32, ... (EPL per lane).
+// One token by one warp; lane l holds experts l, l+32, ... (EPL per lane).
+// On return pr[] holds this lane's probabilities, and lanes j < k hold the
+// j-th chosen expert (my_id) and its gate (my_w).
 template <int EPL>
-__global__ void __launch_bounds__(256) router_select_kernel(SelectArgs a) {
+__device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (&pr)[EPL],
+                                             int& my_id, float& my_w) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= a.T) return;
     const int E = a.E;
     const size_t row = (size_t)t * E;
-    float sc[EPL], pr[EPL];
+    float sc[EPL];
     bool nonfinite = false;
     if (a.from_scores) {
 #pragma unroll
@@ -185,8 +188,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(SelectArgs a) {
 
     // top-k: k rounds of a warp arg-max ordered by (score desc, index asc)
     unsigned taken = 0;
-    int my_id = 0;
     float my_p = 0.f, psum = 0.f;
+    my_id = 0;
     for (int j = 0; j < a.k; ++j) {
         float bv = 0.f;
         int be = INT_MAX;
@@ -221,10 +224,22 @@ __global__ void __launch_bounds__(256) router_select_kernel(SelectArgs a) {
             my_p = pj;
         }
     }
+    my_w = a.renorm ? my_p / psum : my_p;
     if (lane < a.k) {
         a.ids[(size_t)t * a.k + lane] = my_id;
-        a.w[(size_t)t * a.k + lane] = a.renorm ? my_p / psum : my_p;
+        a.w[(size_t)t * a.k + lane] = my_w;
     }
+}
+
+// Standalone selection: one warp per token.
+template <int EPL>
+__global__ void __launch_bounds__(256) router_select_kernel(SelectArgs a) {
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    float pr[EPL];
+    int id;
+    float w;
+    select_token<EPL>(a, t, pr, id, w);
 }
 
 cudaError_t launch_router_select(const Shape& s, const float* logits, const float* zn,
@@ -245,6 +260,83 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
     else if (s.E <= 256) router_select_kernel<8><<<grid, block, 0, st>>>(a);
     else if (s.E <= 512) router_select_kernel<16><<<grid, block, 0, st>>>(a);
     else router_select_kernel<32><<<grid, block, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+// Layer path: selection fused with the capacity histogram and the
+// load-balance statistics. Warps stride over tokens; per expert each lane
+// keeps a running fixed-point sum of its probabilities, and each chosen
+// (token, expert) adds 1 to blk_hist[e][token / kCapBlockTokens] (the scan
+// kernel zeroes those counters after reading them) and its gate to the
+// block's importance sum.
+template <int EPL>
+__global__ void __launch_bounds__(256) router_select_fused_kernel(SelectArgs a, int32_t* blk_hist,
+                                                                  int nblk_cap, AuxAcc acc,
+                                                                  AuxOut out) {
+    extern __shared__ unsigned long long sm64[];
+    const int E = a.E;
+    unsigned long long* sP = sm64;
+    unsigned long long* sI = sm64 + E;
+    unsigned int* sC = reinterpret_cast<unsigned int*>(sm64 + 2 * E);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        sP[e] = 0;
+        sI[e] = 0;
+        sC[e] = 0;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int warps = blockDim.x >> 5;
+    unsigned long long regP[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) regP[i] = 0;
+    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < a.T; t += gridDim.x * warps) {
+        float pr[EPL];
+        int id;
+        float w;
+        select_token<EPL>(a, t, pr, id, w);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) regP[i] += to_fix(pr[i]);
+        if (lane < a.k) {
+            atomicAdd(&sI[id], to_fix(w));
+            atomicAdd(&sC[id], 1u);
+            atomicAdd(&blk_hist[(size_t)id * nblk_cap + t / kCapBlockTokens], 1);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && regP[i]) atomicAdd(&sP[e], regP[i]);
+    }
+    __syncthreads();
+    aux_publish_and_finalize(a.T, E, a.k, acc, out, sP, sI, sC);
+}
+
+cudaError_t launch_router_select_fused(const Shape& s, const float* logits, const float* zn,
+                                       const float* noise, const float* bias, float* probs,
+                                       int32_t* ids, float* w, int* status, int32_t* blk_hist,
+                                       void* acc_mem, float* f, float* P, float* I, float* out3,
+                                       cudaStream_t st) {
+    SelectArgs a;
+    a.T = s.T; a.E = s.E; a.k = s.k; a.renorm = s.renorm; a.from_scores = 0;
+    a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
+    a.sel_in = nullptr; a.probs_in = nullptr;
+    a.probs = probs; a.sel = nullptr; a.ids = ids; a.w = w; a.status = status;
+    const int nblk_cap = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
+    const AuxAcc acc = aux_acc_at(acc_mem, s.E);
+    const AuxOut out{f, P, I, out3, s.w_imp};
+    const int warps = 8;
+    const int grid = std::min((s.T + warps - 1) / warps, 4 * num_sms());
+    const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int)) + 8;
+#define MOE_SEL_FUSED(EPL)                                                                   \
+    router_select_fused_kernel<EPL><<<grid, 32 * warps, smem, st>>>(a, blk_hist, nblk_cap, acc, \
+                                                                    out)
+    if (s.E <= 32) MOE_SEL_FUSED(1);
+    else if (s.E <= 64) MOE_SEL_FUSED(2);
+    else if (s.E <= 128) MOE_SEL_FUSED(4);
+    else if (s.E <= 256) MOE_SEL_FUSED(8);
+    else if (s.E <= 512) MOE_SEL_FUSED(16);
+    else MOE_SEL_FUSED(32);
+#undef MOE_SEL_FUSED
     return cudaGetLastError();
 }
 

@@ -287,7 +287,7 @@ def test_tiny_layer_full_parity(cuda_device):
     wl = WORKLOADS["tiny"]
     c = wl.cfg
     inp = make_inputs(wl, cuda_device)
-    o, _ = run_layer(wl, inp, cuda_device)
+    o, ws = run_layer(wl, inp, cuda_device)
     cpu = {k2: (None if v is None else v.cpu()) for k2, v in inp.items()}
     r = oracle.router(cpu["x"], cpu["Wg"], c.top_k)
     diff = check_topk_valid(o["ids"].cpu().numpy(), r["s"], c.top_k)
@@ -307,6 +307,14 @@ def test_tiny_layer_full_parity(cuda_device):
     o3 = np32(o["out3"])
     assert o3[0] == pytest.approx(st["aux"], rel=TOL_AUX)
     assert o3[1] == pytest.approx(st["cv2"], rel=TOL_AUX)
+    av = np32(o["aux_vecs"])
+    np.testing.assert_allclose(av[0], st["f"], rtol=1e-6)
+    np.testing.assert_allclose(av[1], st["P"], rtol=TOL_AUX)
+    np.testing.assert_allclose(av[2], st["I"], rtol=TOL_AUX)
+    # a second call on the same workspace (counters reset by the kernels) agrees
+    o2, _ = run_layer(wl, inp, cuda_device, ws)
+    for key in o:
+        assert torch.equal(o[key], o2[key]), key
 
 
 def test_nonfinite_input_is_reported(cuda_device):
