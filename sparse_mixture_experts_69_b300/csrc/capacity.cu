@@ -26,6 +26,8 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 __global__ void __launch_bounds__(kCapBlockTokens) cap_hist_kernel(
     int T, int k, int E, int nblk, const int32_t* __restrict__ ids, int32_t* __restrict__ blk_hist,
     int* status) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ int hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
@@ -63,6 +65,8 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 __global__ void __launch_bounds__(1024) cap_scan_kernel(
     int nblk, int E, int C, int32_t* __restrict__ blk_hist, int32_t* __restrict__ blk_base,
     int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int kp[1024];
     __shared__ int wsum[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -108,6 +112,8 @@ __global__ void __launch_bounds__(kCapBlockTokens) cap_slot_kernel(
     int T, int k, int E, int C, int nblk, const int32_t* __restrict__ ids,
     const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
     int32_t* __restrict__ slot, int32_t* __restrict__ row_token) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ unsigned mask[];
     constexpr int W = kCapBlockTokens / 32;
     for (int i = threadIdx.x; i < W * E; i += blockDim.x) mask[i] = 0;
@@ -139,26 +145,135 @@ __global__ void __launch_bounds__(kCapBlockTokens) cap_slot_kernel(
     }
 }
 
+// Scan and slots in one launch, for up to kMaxFusedCapBlocks token blocks.
+// Every block reads the histogram rows itself: counts[e] = sum over blocks,
+// its own base = sum over earlier blocks, offsets = exclusive scan of
+// kept = min(counts, C) over experts (block 0 writes counts, kept, offsets).
+// Then the lane-bitmask ranks of cap_slot_kernel. The last block to finish
+// reading (ticket) zeroes the histogram counters and the ticket.
+constexpr int kMaxFusedCapBlocks = 256;
+
+__global__ void __launch_bounds__(kCapBlockTokens) cap_scan_slot_kernel(
+    int T, int k, int E, int C, int nblk, const int32_t* __restrict__ ids,
+    int32_t* __restrict__ blk_hist, unsigned int* __restrict__ ticket,
+    int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ slot, int32_t* __restrict__ row_token) {
+    pdl_trigger();
+    pdl_wait();
+    extern __shared__ unsigned mask[];                  // [8][E]
+    int* s_base = reinterpret_cast<int*>(mask + (kCapBlockTokens / 32) * E);  // [E]
+    int* s_off = s_base + E;                             // [E+1]
+    __shared__ int wsum[kCapBlockTokens / 32];
+    __shared__ int s_last;
+    constexpr int W = kCapBlockTokens / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int b = blockIdx.x;
+    for (int i = threadIdx.x; i < W * E; i += blockDim.x) mask[i] = 0;
+    // per expert: base (earlier blocks) and total
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t* row = blk_hist + (size_t)e * nblk;
+        int before = 0, total = 0;
+#pragma unroll 8
+        for (int q = 0; q < nblk; ++q) {
+            const int v = __ldcg(row + q);
+            total += v;
+            before += q < b ? v : 0;
+        }
+        s_base[e] = before;
+        s_off[e] = total < C ? total : C;  // kept, scanned below
+        if (b == 0) {
+            counts[e] = total;
+            kept[e] = s_off[e];
+        }
+    }
+    __syncthreads();
+    // this block no longer needs the histogram: the last one to get here clears it
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(ticket, 1u) == (unsigned)(nblk - 1);
+    }
+    // exclusive scan of kept over experts: each thread scans a contiguous run
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int lo = threadIdx.x * per, hi = min(E, lo + per);
+    int run = 0;
+    for (int e = lo; e < hi; ++e) run += s_off[e];
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += wsum[w];
+    int acc = wbase + incl - run;
+    for (int e = lo; e < hi; ++e) {
+        const int kv = s_off[e];
+        s_off[e] = acc;
+        acc += kv;
+    }
+    if (threadIdx.x == blockDim.x - 1) s_off[E] = acc;
+    __syncthreads();
+    if (b == 0)
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+    if (s_last) {
+        __threadfence();
+        for (int i = threadIdx.x; i < E * nblk; i += blockDim.x) blk_hist[i] = 0;
+        if (threadIdx.x == 0) *ticket = 0u;
+    }
+    // slots (as in cap_slot_kernel)
+    const int t = b * kCapBlockTokens + threadIdx.x;
+    if (t < T)
+        for (int j = 0; j < k; ++j) {
+            const int e = ids[(size_t)t * k + j];
+            if (e >= 0 && e < E) atomicOr(&mask[warp * E + e], 1u << lane);
+        }
+    __syncthreads();
+    if (t >= T) return;
+    const unsigned lt = lanemask_lt();
+    for (int j = 0; j < k; ++j) {
+        const size_t a = (size_t)t * k + j;
+        const int e = ids[a];
+        int out = -1;
+        if (e >= 0 && e < E) {
+            int r = __popc(mask[warp * E + e] & lt);
+            for (int w = 0; w < warp; ++w) r += __popc(mask[w * E + e]);
+            const int sl = s_base[e] + r;
+            if (sl < C) {
+                out = s_off[e] + sl;
+                row_token[out] = t;
+            }
+        }
+        slot[a] = out;
+    }
+}
+
 cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_hist,
-                            int32_t* blk_base, int32_t* counts, int32_t* kept, int32_t* offsets,
-                            int32_t* slot, int32_t* row_token, int* status, bool hist_ready,
-                            cudaStream_t st) {
+                            unsigned int* cap_ticket, int32_t* blk_base, int32_t* counts,
+                            int32_t* kept, int32_t* offsets, int32_t* slot, int32_t* row_token,
+                            int* status, bool hist_ready, cudaStream_t st) {
     const int nblk = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
     cudaError_t err;
     if (!hist_ready) {
-        cap_hist_kernel<<<nblk, kCapBlockTokens, s.E * sizeof(int), st>>>(s.T, s.k, s.E, nblk,
-                                                                          ids, blk_hist, status);
-        err = cudaGetLastError();
+        err = launch_k(cap_hist_kernel, dim3(nblk), dim3(kCapBlockTokens), s.E * sizeof(int), st,
+                       s.T, s.k, s.E, nblk, ids, blk_hist, status);
         if (err != cudaSuccess) return err;
     }
-    cap_scan_kernel<<<1, 1024, 0, st>>>(nblk, s.E, s.C, blk_hist, blk_base, counts, kept,
-                                        offsets);
-    err = cudaGetLastError();
+    if (nblk <= kMaxFusedCapBlocks) {
+        const size_t smem = (size_t)(kCapBlockTokens / 32) * s.E * sizeof(unsigned) +
+                            (size_t)(2 * s.E + 1) * sizeof(int);
+        return launch_k(cap_scan_slot_kernel, dim3(nblk), dim3(kCapBlockTokens), smem, st, s.T,
+                        s.k, s.E, s.C, nblk, ids, blk_hist, cap_ticket, counts, kept, offsets,
+                        slot, row_token);
+    }
+    err = launch_k(cap_scan_kernel, dim3(1), dim3(1024), 0, st, nblk, s.E, s.C, blk_hist, blk_base,
+                   counts, kept, offsets);
     if (err != cudaSuccess) return err;
     const size_t smem = (size_t)(kCapBlockTokens / 32) * s.E * sizeof(unsigned);
-    cap_slot_kernel<<<nblk, kCapBlockTokens, smem, st>>>(s.T, s.k, s.E, s.C, nblk, ids, blk_base,
-                                                         offsets, slot, row_token);
-    return cudaGetLastError();
+    return launch_k(cap_slot_kernel, dim3(nblk), dim3(kCapBlockTokens), smem, st, s.T, s.k, s.E,
+                    s.C, nblk, ids, (const int32_t*)blk_base, (const int32_t*)offsets, slot,
+                    row_token);
 }
 
 // ---------------------------------------------------------------- permute
@@ -168,24 +283,33 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec,
                                                       const uint4* __restrict__ x,
                                                       const int32_t* __restrict__ slot,
                                                       uint4* __restrict__ xp) {
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
+    pdl_wait();
     const int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
     unsigned live = __ballot_sync(0xffffffffu, my_slot >= 0);
     const uint4* src = x + (size_t)t * nvec;
-    // the loop bound is warp-uniform so every shuffle has all lanes present
-    for (int v0 = 0; v0 < nvec; v0 += 32) {
-        const int v = v0 + lane;
-        const bool ok = v < nvec;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (ok) val = __ldcs(src + v);
+    // the loop bound is warp-uniform so every shuffle has all lanes present;
+    // each lane loads up to 4 vectors before storing them
+    for (int v0 = 0; v0 < nvec; v0 += 128) {
+        uint4 val[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int v = v0 + 32 * q + lane;
+            if (v < nvec) val[q] = __ldcs(src + v);
+        }
         unsigned m = live;
         while (m) {
             const int j = __ffs(m) - 1;
             m &= m - 1;
             const int r = __shfl_sync(0xffffffffu, my_slot, j);
-            if (ok) xp[(size_t)r * nvec + v] = val;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int v = v0 + 32 * q + lane;
+                if (v < nvec) xp[(size_t)r * nvec + v] = val[q];
+            }
         }
     }
 }
@@ -193,9 +317,8 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec,
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
                            cudaStream_t st) {
     const int nvec = s.d * s.esize / 16;
-    permute_kernel<<<(s.T + 7) / 8, 256, 0, st>>>(s.T, s.k, nvec, (const uint4*)x, slot,
-                                                 (uint4*)xp);
-    return cudaGetLastError();
+    return launch_k(permute_kernel, dim3((s.T + 7) / 8), dim3(256), 0, st, s.T, s.k, nvec,
+                    (const uint4*)x, slot, (uint4*)xp);
 }
 
 }  // namespace moe

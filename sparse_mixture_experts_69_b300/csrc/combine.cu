@@ -49,16 +49,18 @@ struct Vec<__nv_bfloat16> {
 // fp32 accumulation in the fixed order j = 0..k-1, then s = 0..S-1. Each lane
 // covers up to VPL 16-byte vectors per pass and issues their loads together.
 template <typename Tv, int VPL>
-__global__ void __launch_bounds__(256) combine_kernel(int T, int d, int k, int S,
+__global__ void __launch_bounds__(256, 4) combine_kernel(int T, int d, int k, int S,
                                                       const Tv* __restrict__ yp,
                                                       const int32_t* __restrict__ slot,
                                                       const float* __restrict__ w,
                                                       const Tv* __restrict__ ys, Tv* __restrict__ y,
                                                       int* status) {
+    pdl_trigger();
     constexpr int VN = Vec<Tv>::N;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
+    pdl_wait();
     const int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
     const float my_w = lane < k ? w[(size_t)t * k + lane] : 0.f;
     const unsigned live = __ballot_sync(0xffffffffu, my_slot >= 0);
@@ -124,25 +126,24 @@ cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, 
                            const void* ys, void* y, int* status, cudaStream_t st) {
     dim3 grid((s.T + 7) / 8), block(256);
     if (s.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16, 4><<<grid, block, 0, st>>>(
-            s.T, s.d, s.k, ys ? s.S : 0, (const __nv_bfloat16*)yp, slot, w,
-            (const __nv_bfloat16*)ys, (__nv_bfloat16*)y, status);
-    else
-        combine_kernel<float, 4><<<grid, block, 0, st>>>(s.T, s.d, s.k, ys ? s.S : 0,
-                                                      (const float*)yp, slot, w,
-                                                      (const float*)ys, (float*)y, status);
-    return cudaGetLastError();
+        return launch_k(combine_kernel<__nv_bfloat16, 2>, grid, block, 0, st, s.T, s.d, s.k,
+                        ys ? s.S : 0, (const __nv_bfloat16*)yp, slot, w, (const __nv_bfloat16*)ys,
+                        (__nv_bfloat16*)y, status);
+    return launch_k(combine_kernel<float, 2>, grid, block, 0, st, s.T, s.d, s.k, ys ? s.S : 0,
+                    (const float*)yp, slot, w, (const float*)ys, (float*)y, status);
 }
 
 // --------------------------------------------------------------- statistics
 // One launch; each block takes kAuxBlockTokens tokens, sums them per expert in
 // shared memory (integers, see aux_common.cuh) and publishes; the last block
 // finalises.
-__global__ void __launch_bounds__(256) aux_kernel(int T, int E, int k,
+__global__ void __launch_bounds__(256) aux_kernel(int T, int E, int k, int vec4,
                                                   const float* __restrict__ probs,
                                                   const int32_t* __restrict__ ids,
                                                   const float* __restrict__ w, AuxAcc acc,
                                                   AuxOut out) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ unsigned long long sm64[];
     unsigned long long* sP = sm64;
     unsigned long long* sI = sm64 + E;
@@ -155,21 +156,34 @@ __global__ void __launch_bounds__(256) aux_kernel(int T, int E, int k,
     __syncthreads();
     const int t0 = blockIdx.x * kAuxBlockTokens;
     const int nt = min(kAuxBlockTokens, T - t0);
-    // column sums of probs: thread -> (column e, every rstep-th row)
-    if (E <= (int)blockDim.x) {
-        const int rstep = (int)blockDim.x / E;
-        const int e = (int)threadIdx.x % E, r0 = (int)threadIdx.x / E;
-        if (r0 < rstep) {
-            unsigned long long acc_p = 0;
-#pragma unroll 8
-            for (int r = r0; r < nt; r += rstep) acc_p += to_fix(__ldg(&probs[(size_t)(t0 + r) * E + e]));
-            atomicAdd(&sP[e], acc_p);
+    // column sums of probs. With E a multiple of 4 whose quads divide the
+    // block, each thread keeps one column quad (float4 loads) over every
+    // (blockDim / (E/4))-th row in registers, then adds once to shared memory.
+    const int E4 = E >> 2;
+    if (vec4 && E4 <= (int)blockDim.x && (int)blockDim.x % E4 == 0) {
+        const int q = (int)threadIdx.x % E4, r0 = (int)threadIdx.x / E4;
+        const int rstep = (int)blockDim.x / E4;
+        unsigned long long a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+        const float4* p4 = reinterpret_cast<const float4*>(probs);
+#pragma unroll 4
+        for (int r = r0; r < nt; r += rstep) {
+            const float4 v = __ldg(&p4[(size_t)(t0 + r) * E4 + q]);
+            a0 += to_fix(v.x);
+            a1 += to_fix(v.y);
+            a2 += to_fix(v.z);
+            a3 += to_fix(v.w);
+        }
+        if (r0 < nt) {
+            atomicAdd(&sP[4 * q], a0);
+            atomicAdd(&sP[4 * q + 1], a1);
+            atomicAdd(&sP[4 * q + 2], a2);
+            atomicAdd(&sP[4 * q + 3], a3);
         }
     } else {
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             unsigned long long acc_p = 0;
-            for (int r = 0; r < nt; ++r) acc_p += to_fix(probs[(size_t)(t0 + r) * E + e]);
-            sP[e] = acc_p;
+            for (int r = 0; r < nt; ++r) acc_p += to_fix(__ldg(&probs[(size_t)(t0 + r) * E + e]));
+            atomicAdd(&sP[e], acc_p);
         }
     }
     for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
@@ -188,14 +202,17 @@ cudaError_t launch_aux(const Shape& s, const float* probs, const int32_t* ids, c
     const int nblk = (s.T + kAuxBlockTokens - 1) / kAuxBlockTokens;
     const AuxOut out{f, P, I, out3, s.w_imp};
     const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int)) + 8;
-    aux_kernel<<<nblk, 256, smem, st>>>(s.T, s.E, s.k, probs, ids, w, aux_acc_at(acc_mem, s.E),
-                                        out);
-    return cudaGetLastError();
+    // float4 loads need 16-byte aligned rows
+    const int vec4 = (s.E % 4 == 0) && (reinterpret_cast<uintptr_t>(probs) % 16 == 0);
+    return launch_k(aux_kernel, dim3(nblk), dim3(256), smem, st, s.T, s.E, s.k, vec4, probs, ids,
+                    w, aux_acc_at(acc_mem, s.E), out);
 }
 
 // -------------------------------------------------------------- bias update
 __global__ void bias_update_kernel(int T, int E, int k, const int32_t* __restrict__ counts,
                                    float* __restrict__ bias, float rate) {
+    pdl_trigger();
+    pdl_wait();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E) return;
     const long long diff = (long long)counts[e] * E - (long long)T * k;
@@ -207,8 +224,8 @@ __global__ void bias_update_kernel(int T, int E, int k, const int32_t* __restric
 
 cudaError_t launch_bias_update(const Shape& s, const int32_t* counts, float* bias, float rate,
                                cudaStream_t st) {
-    bias_update_kernel<<<(s.E + 255) / 256, 256, 0, st>>>(s.T, s.E, s.k, counts, bias, rate);
-    return cudaGetLastError();
+    return launch_k(bias_update_kernel, dim3((s.E + 255) / 256), dim3(256), 0, st, s.T, s.E, s.k,
+                    counts, bias, rate);
 }
 
 }  // namespace moe

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(GroupedGemm p) {
     __shared__ float As[SK][SB + 4];
     __shared__ float Bs[SK][SB + 4];
     __shared__ float Bu[GLU ? SK : 1][SB + 4];
+    pdl_trigger();
+    pdl_wait();
     build_tile_table(p, SB, mt_start);
     __syncthreads();
     const int G = p.E + p.S;
@@ -96,15 +98,12 @@ cudaError_t launch_grouped_gemm_simt(const Shape& s, const GroupedGemm& g, cudaS
     const int G = g.E + g.S;
     const size_t smem = sizeof(int) * (size_t)(G + 1);
     const long long nt = (g.N + SB - 1) / SB;
-    long long mt = (long long)g.rows_a0 / SB + g.E + (long long)g.S * ((g.T + SB - 1) / SB);
+    long long mt = (long long)g.max_rows0 / SB + g.E + (long long)g.S * ((g.T + SB - 1) / SB);
     long long bound = mt * nt;
     if (bound < 1) bound = 1;
     const int grid = (int)(bound < 4LL * num_sms() ? bound : 4LL * num_sms());
-    if (g.glu)
-        grouped_gemm_simt_kernel<true><<<grid, 256, smem, st>>>(g);
-    else
-        grouped_gemm_simt_kernel<false><<<grid, 256, smem, st>>>(g);
-    return cudaGetLastError();
+    if (g.glu) return launch_k(grouped_gemm_simt_kernel<true>, dim3(grid), dim3(256), smem, st, g);
+    return launch_k(grouped_gemm_simt_kernel<false>, dim3(grid), dim3(256), smem, st, g);
 }
 
 }  // namespace moe

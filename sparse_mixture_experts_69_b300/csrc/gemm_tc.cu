@@ -30,9 +30,6 @@
 #ifndef MOE_TC_PROMO
 #define MOE_TC_PROMO 2  // L2 promotion of TMA loads: 0 none, 1 128 B, 2 256 B
 #endif
-#ifndef MOE_TC_HINT
-#define MOE_TC_HINT 0  // 1: weight tiles evict-first, activation tiles evict-last
-#endif
 #ifndef MOE_TC_ROT
 #define MOE_TC_ROT 0  // 1: each tile starts its k loop at a tile-dependent block
 #endif
@@ -78,8 +75,13 @@ struct Cfg {
     // M=128, N=BN, D=f32, A=B=bf16, both K-major
     static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-    static constexpr size_t smem_bytes(int G) {
-        return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (size_t)(G + 1);
+    // the router epilogue stages 32x32 fp32 blocks per epilogue warp (padded rows)
+    static constexpr int STAGING_BYTES = 4 * 32 * 33 * 4;
+    // layout after the stages: barriers (256 B), tile table [G+1], then (router
+    // only) the staging area
+    static constexpr size_t smem_bytes(int G, bool staging) {
+        return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (size_t)(G + 1) +
+               (staging ? 16 + STAGING_BYTES : 0);
     }
 };
 
@@ -140,24 +142,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
-}
-__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                                 int x, int y, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -305,6 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* mt_start = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+    float* staging = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(mt_start + p.E + p.S + 1) + 15) & ~(uintptr_t)15);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.E + p.S;
@@ -312,6 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = (p.N + ncol_tile - 1) / ncol_tile;
     const int nkb = (p.K + BK - 1) / BK;
 
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA0);
+        prefetch_tmap(&tmA1);
+        prefetch_tmap(&tmB0);
+        prefetch_tmap(&tmB1);
+    }
+    pdl_trigger();
+    pdl_wait();
     build_tile_table(p, BM, mt_start);
     __syncthreads();
     const int total = mt_start[G] * nt;
@@ -330,10 +324,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        prefetch_tmap(&tmA0);
-        prefetch_tmap(&tmA1);
-        prefetch_tmap(&tmB0);
-        prefetch_tmap(&tmB1);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -347,8 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol_a = MOE_TC_HINT ? policy_evict_last() : 0;
-            const uint64_t pol_b = MOE_TC_HINT ? policy_evict_first() : 0;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;
@@ -377,21 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int hk = 0; hk < KH; ++hk) {
                         const int kx = kb * BK + hk * BKH;
-                        uint8_t* a_dst = sA + stage * C::A_BYTES + hk * C::A_HALF;
-                        uint8_t* b_dst = sB + stage * C::B_BYTES + hk * C::B_HALF;
-                        if (MOE_TC_HINT) {
-                            tma_load_2d_hint(a_dst, ma, &full[stage], kx, gt.a_row, pol_a);
+                        tma_load_2d(sA + stage * C::A_BYTES + hk * C::A_HALF, ma, &full[stage], kx,
+                                    gt.a_row);
 #pragma unroll
-                            for (int h = 0; h < C::B_LOADS; ++h)
-                                tma_load_2d_hint(b_dst + h * C::B_BOX_ROWS * 128, mb, &full[stage],
-                                                 kx, brow[h], pol_b);
-                        } else {
-                            tma_load_2d(a_dst, ma, &full[stage], kx, gt.a_row);
-#pragma unroll
-                            for (int h = 0; h < C::B_LOADS; ++h)
-                                tma_load_2d(b_dst + h * C::B_BOX_ROWS * 128, mb, &full[stage], kx,
-                                            brow[h]);
-                        }
+                        for (int h = 0; h < C::B_LOADS; ++h)
+                            tma_load_2d(sB + stage * C::B_BYTES + hk * C::B_HALF +
+                                            h * C::B_BOX_ROWS * 128,
+                                        mb, &full[stage], kx, brow[h]);
                     }
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -473,23 +453,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool rv = row < gt.rows;
             const bool routed = gt.g < p.E;
             if (EPI == EPI_ROUTER) {
-                const int t = gt.out_row + row;
+                // thread = row; stage 32 rows x 32 columns, then each warp writes
+                // whole 128-byte row segments (lane = column)
+                float* stg = staging + q * 32 * 33;
+                const int rows_here = min(32, gt.rows - 32 * q);
+                const int E_r = args.E_router;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     float v[32];
                     tmem_ld32(taddr + c, v);
-                    const int n0 = gt.n_tile * BN + c;
-                    if (rv) {
-                        for (int i = 0; i < 32; ++i) {
-                            const int n = n0 + i;
-                            if (n >= p.N) break;
-                            if (n < args.E_router)
-                                args.logits[(size_t)t * args.E_router + n] =
-                                    v[i] + (args.offset ? args.offset[n] : 0.f);
-                            else
-                                args.zn[(size_t)t * args.E_router + (n - args.E_router)] = v[i];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = v[i];
+                    __syncwarp();
+                    const int n = gt.n_tile * BN + c + lane;
+                    if (n < p.N) {
+                        const bool is_logit = n < E_r;
+                        const float off = (is_logit && args.offset) ? args.offset[n] : 0.f;
+                        float* dst = is_logit ? args.logits + n : args.zn + (n - E_r);
+                        for (int r = 0; r < rows_here; ++r) {
+                            const size_t t = (size_t)(gt.out_row + 32 * q + r);
+                            dst[t * E_r] = stg[r * 33 + lane] + off;
                         }
                     }
+                    __syncwarp();
                 }
             } else {
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(routed ? p.out0 : p.out1);
@@ -580,19 +566,19 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     if (!make_map(&mB0, p.B0 ? p.B0 : p.B1, p.B0 ? brows0 : brows1, p.K, C::B_BOX_ROWS) ||
         !make_map(&mB1, p.B1 ? p.B1 : p.B0, p.B1 ? brows1 : brows0, p.K, C::B_BOX_ROWS))
         return cudaErrorInvalidValue;
-    const size_t smem = C::smem_bytes(G);
+    const size_t smem = C::smem_bytes(G, EPI == EPI_ROUTER);
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<BN, EPI>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     // upper bound of the tile count, from host-known sizes
     const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
     const long long nt = (p.N + ncol_tile - 1) / ncol_tile;
-    long long mt = (long long)p.rows_a0 / BM + p.E + (long long)p.S * ((p.T + BM - 1) / BM);
+    long long mt = (long long)p.max_rows0 / BM + p.E + (long long)p.S * ((p.T + BM - 1) / BM);
     if (p.E == 0) mt = (long long)p.S * ((p.T + BM - 1) / BM);
     const long long bound = std::max<long long>(1, mt * nt);
     const int grid = (int)std::min<long long>(bound, num_sms());
-    grouped_gemm_tc_kernel<BN, EPI><<<grid, kThreads, smem, st>>>(mA0, mA1, mB0, mB1, a);
-    return cudaGetLastError();
+    return launch_k(grouped_gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kThreads), smem, st, mA0,
+                    mA1, mB0, mB1, a);
 }
 
 }  // namespace tc
@@ -616,6 +602,7 @@ cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const
     p.a1_row0 = 0;
     p.a1_stride = 0;
     p.rows_a0 = 0;
+    p.max_rows0 = 0;
     p.rows_a1 = s.T;
     p.N = Nr;
     p.K = s.d;

@@ -25,7 +25,7 @@ __device__ __forceinline__ int group_rows(const GroupedGemm& p, int g, int* a_ro
                                           bool* bad) {
     if (g < p.E) {
         int lo = p.offsets[g], hi = p.offsets[g + 1];
-        if (lo < 0 || hi < lo || hi > p.rows_a0) {
+        if (lo < 0 || hi < lo || hi > p.max_rows0) {
             *bad = true;
             *a_row = 0;
             *out_row = 0;

@@ -46,6 +46,7 @@ WsLayout ws_layout(const Shape& s) {
     L.status = take(256);
     L.aux_acc = take(E * (8 + 8 + 4) + 16);
     L.blk_hist = take(nblk * E * 4);
+    L.cap_ticket = take(16);
     L.zero_end = off;
     L.zn = take(T * E * 4);
     L.wgT = take(2 * E * d * es);
@@ -179,7 +180,8 @@ moe_status dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const void
                          int32_t* slot, void* xp, int32_t* row_token, bool hist_ready,
                          cudaStream_t st) {
     int* status = at<int>(ws, L.status);
-    MOE_CUDA(launch_capacity(s, ids, at<int32_t>(ws, L.blk_hist), at<int32_t>(ws, L.blk_base),
+    MOE_CUDA(launch_capacity(s, ids, at<int32_t>(ws, L.blk_hist),
+                             at<unsigned int>(ws, L.cap_ticket), at<int32_t>(ws, L.blk_base),
                              counts, kept, offsets, slot, row_token, status, hist_ready, st));
     MOE_CUDA(launch_permute(s, x, slot, xp, st));
     return MOE_OK;
@@ -199,6 +201,7 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     up.a1_row0 = 0;
     up.a1_stride = 0;
     up.rows_a0 = s.R_max;
+    up.max_rows0 = s.R_max;
     up.rows_a1 = s.T;
     up.N = s.F;
     up.K = s.d;
@@ -221,6 +224,7 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     dn.a1_row0 = s.R_max;
     dn.a1_stride = s.T;
     dn.rows_a0 = s.R_max;
+    dn.max_rows0 = s.R_max;
     dn.rows_a1 = s.R_max + s.S * s.T;
     dn.N = s.d;
     dn.K = s.F;

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -34,6 +36,7 @@ struct WsLayout {
     size_t status;     // int32 status word (+ padding)
     size_t aux_acc;    // statistics accumulators: [2E] u64, [E] u32, ticket
     size_t blk_hist;   // [E][nblk] i32 capacity histogram counters
+    size_t cap_ticket; // u32 ticket of the fused scan + slot kernel
     size_t zero_end;   // end of the zero-between-calls prefix
     size_t zn;         // [T,E] f32 noise logits x.Wnoise
     size_t wgT;        // [Nr,d] dtype: Wg^T (rows 0..E-1) and Wnoise^T (E..2E-1)
@@ -57,7 +60,7 @@ struct WsLayout {
 };
 
 constexpr int kCapBlockTokens = 256;  // tokens per block of the capacity kernels
-constexpr int kAuxBlockTokens = 256;  // tokens per block of the statistics kernel
+constexpr int kAuxBlockTokens = 64;   // tokens per block of the statistics kernel
 
 WsLayout ws_layout(const Shape& s);
 
@@ -94,9 +97,9 @@ cudaError_t launch_router_select_fused(const Shape& s, const float* logits, cons
 // hist_ready: blk_hist already holds the per-block histograms (the fused router
 // kernel counted them), so only the scan and slot kernels run.
 cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_hist,
-                            int32_t* blk_base, int32_t* counts, int32_t* kept, int32_t* offsets,
-                            int32_t* slot, int32_t* row_token, int* status, bool hist_ready,
-                            cudaStream_t st);
+                            unsigned int* cap_ticket, int32_t* blk_base, int32_t* counts,
+                            int32_t* kept, int32_t* offsets, int32_t* slot, int32_t* row_token,
+                            int* status, bool hist_ready, cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
                            cudaStream_t st);
 
@@ -108,7 +111,8 @@ struct GroupedGemm {
     // shared groups s < S: rows a1_row0 + s*a1_stride .. + T of A1; out1 rows s*T ..
     int S, T;
     int a1_row0, a1_stride;
-    int rows_a0;        // rows of A0 (bounds: R_max)
+    int rows_a0;        // rows of the A0 matrix
+    int max_rows0;      // bound of offsets[E] (R_max): rows of out0
     int rows_a1;        // rows of A1
     int N;              // output columns
     int K;              // reduction length
@@ -132,6 +136,34 @@ cudaError_t launch_bias_update(const Shape& s, const int32_t* counts, float* bia
                                cudaStream_t st);
 
 int num_sms();
+
+// ------------------------------------------------- programmatic dependent launch
+// Every kernel is launched with programmatic stream serialisation: it may be
+// scheduled while the previous kernel on the stream is still finishing. Each
+// kernel therefore does only parameter-only set-up, calls pdl_trigger() (its
+// own dependents may start launching once all of its blocks have started),
+// then pdl_wait(), which returns when the previous kernel has completed and
+// its writes are visible, before it reads or writes any global memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------ device helpers
 __device__ __forceinline__ float warp_max(float v) {

@@ -18,6 +18,8 @@ namespace moe {
 template <typename Tv>
 __global__ void transpose_router_w_kernel(int d, int E, const Tv* __restrict__ Wg,
                                           const Tv* __restrict__ Wn, Tv* __restrict__ wgT) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ Tv tile[32][33];
     const Tv* src = blockIdx.z == 0 ? Wg : Wn;
     const int i0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
@@ -37,12 +39,11 @@ cudaError_t launch_transpose_router_w(const Shape& s, const void* Wg, const void
                                       void* wgT, cudaStream_t st) {
     dim3 grid((s.E + 31) / 32, (s.d + 31) / 32, Wnoise ? 2 : 1), block(32, 8);
     if (s.dtype == MOE_BF16)
-        transpose_router_w_kernel<uint16_t><<<grid, block, 0, st>>>(
-            s.d, s.E, (const uint16_t*)Wg, (const uint16_t*)Wnoise, (uint16_t*)wgT);
+        return launch_k(transpose_router_w_kernel<uint16_t>, grid, block, 0, st, s.d, s.E,
+                        (const uint16_t*)Wg, (const uint16_t*)Wnoise, (uint16_t*)wgT);
     else
-        transpose_router_w_kernel<float><<<grid, block, 0, st>>>(
-            s.d, s.E, (const float*)Wg, (const float*)Wnoise, (float*)wgT);
-    return cudaGetLastError();
+        return launch_k(transpose_router_w_kernel<float>, grid, block, 0, st, s.d, s.E,
+                        (const float*)Wg, (const float*)Wnoise, (float*)wgT);
 }
 
 // ------------------------------------------------------- float32 router GEMM
@@ -52,6 +53,8 @@ __global__ void __launch_bounds__(256) router_gemm_f32_kernel(
     int T, int d, int E, int Nr, const float* __restrict__ x, const float* __restrict__ Wg,
     const float* __restrict__ Wn, const float* __restrict__ offset, float* __restrict__ logits,
     float* __restrict__ zn) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float As[16][64 + 1];
     __shared__ float Bs[16][64 + 1];
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -103,9 +106,8 @@ cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const
                                    const float* Wnoise, const float* offset, float* logits,
                                    float* zn, cudaStream_t st) {
     dim3 grid((Nr + 63) / 64, (s.T + 63) / 64);
-    router_gemm_f32_kernel<<<grid, 256, 0, st>>>(s.T, s.d, s.E, Nr, x, Wg, Wnoise, offset,
-                                                 logits, zn);
-    return cudaGetLastError();
+    return launch_k(router_gemm_f32_kernel, grid, dim3(256), 0, st, s.T, s.d, s.E, Nr, x, Wg,
+                    Wnoise, offset, logits, zn);
 }
 
 // ------------------------------------------------------------------ selection
@@ -234,8 +236,10 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (
 // Standalone selection: one warp per token.
 template <int EPL>
 __global__ void __launch_bounds__(256) router_select_kernel(SelectArgs a) {
+    pdl_trigger();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= a.T) return;
+    pdl_wait();
     float pr[EPL];
     int id;
     float w;
@@ -254,13 +258,12 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
     a.probs = probs; a.sel = sel; a.ids = ids; a.w = w; a.status = status;
     const int warps = 8;
     dim3 grid((s.T + warps - 1) / warps), block(32 * warps);
-    if (s.E <= 32) router_select_kernel<1><<<grid, block, 0, st>>>(a);
-    else if (s.E <= 64) router_select_kernel<2><<<grid, block, 0, st>>>(a);
-    else if (s.E <= 128) router_select_kernel<4><<<grid, block, 0, st>>>(a);
-    else if (s.E <= 256) router_select_kernel<8><<<grid, block, 0, st>>>(a);
-    else if (s.E <= 512) router_select_kernel<16><<<grid, block, 0, st>>>(a);
-    else router_select_kernel<32><<<grid, block, 0, st>>>(a);
-    return cudaGetLastError();
+    if (s.E <= 32) return launch_k(router_select_kernel<1>, grid, block, 0, st, a);
+    if (s.E <= 64) return launch_k(router_select_kernel<2>, grid, block, 0, st, a);
+    if (s.E <= 128) return launch_k(router_select_kernel<4>, grid, block, 0, st, a);
+    if (s.E <= 256) return launch_k(router_select_kernel<8>, grid, block, 0, st, a);
+    if (s.E <= 512) return launch_k(router_select_kernel<16>, grid, block, 0, st, a);
+    return launch_k(router_select_kernel<32>, grid, block, 0, st, a);
 }
 
 // Layer path: selection fused with the capacity histogram and the
@@ -270,9 +273,11 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
 // kernel zeroes those counters after reading them) and its gate to the
 // block's importance sum.
 template <int EPL>
-__global__ void __launch_bounds__(256) router_select_fused_kernel(SelectArgs a, int32_t* blk_hist,
+__global__ void __launch_bounds__(512) router_select_fused_kernel(SelectArgs a, int32_t* blk_hist,
                                                                   int nblk_cap, AuxAcc acc,
                                                                   AuxOut out) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ unsigned long long sm64[];
     const int E = a.E;
     unsigned long long* sP = sm64;
@@ -324,20 +329,21 @@ cudaError_t launch_router_select_fused(const Shape& s, const float* logits, cons
     const int nblk_cap = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
     const AuxAcc acc = aux_acc_at(acc_mem, s.E);
     const AuxOut out{f, P, I, out3, s.w_imp};
-    const int warps = 8;
-    const int grid = std::min((s.T + warps - 1) / warps, 4 * num_sms());
+    // one block per SM keeps the number of blocks adding to the same statistics
+    // counters (global atomics) small; warps stride over the tokens
+    const int warps = 16;
+    const int grid = std::min((s.T + warps - 1) / warps, num_sms());
     const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int)) + 8;
-#define MOE_SEL_FUSED(EPL)                                                                   \
-    router_select_fused_kernel<EPL><<<grid, 32 * warps, smem, st>>>(a, blk_hist, nblk_cap, acc, \
-                                                                    out)
+#define MOE_SEL_FUSED(EPL)                                                                  \
+    return launch_k(router_select_fused_kernel<EPL>, dim3(grid), dim3(32 * warps), smem, st, a, \
+                    blk_hist, nblk_cap, acc, out)
     if (s.E <= 32) MOE_SEL_FUSED(1);
-    else if (s.E <= 64) MOE_SEL_FUSED(2);
-    else if (s.E <= 128) MOE_SEL_FUSED(4);
-    else if (s.E <= 256) MOE_SEL_FUSED(8);
-    else if (s.E <= 512) MOE_SEL_FUSED(16);
-    else MOE_SEL_FUSED(32);
+    if (s.E <= 64) MOE_SEL_FUSED(2);
+    if (s.E <= 128) MOE_SEL_FUSED(4);
+    if (s.E <= 256) MOE_SEL_FUSED(8);
+    if (s.E <= 512) MOE_SEL_FUSED(16);
+    MOE_SEL_FUSED(32);
 #undef MOE_SEL_FUSED
-    return cudaGetLastError();
 }
 
 }  // namespace moe
