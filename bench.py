@@ -450,8 +450,12 @@ def main():
     e2e_value = world * T * K2 / e2e_s
 
     # layer path: [Wg transpose (bf16)], router GEMM, fused selection + histogram +
-    # statistics, capacity scan, slots, permute, up GEMM, down GEMM, combine
-    launches_per_step = (9 if c.dtype == 1 else 8) + (1 if wl.bias_rate else 0)
+    # statistics, capacity scan + slots (one launch up to 256 token blocks),
+    # permute, up GEMM, down GEMM, [combine: skipped for bf16 top-1 without
+    # shared experts, where the down GEMM writes y], [bias update]
+    scatter = c.dtype == 1 and c.top_k == 1 and c.n_shared == 0
+    launches_per_step = ((1 if c.dtype == 1 else 0) + 2 + (1 if (T + 255) // 256 <= 256 else 2)
+                         + 1 + 2 + (0 if scatter else 1) + (1 if wl.bias_rate else 0))
 
     if rank != 0:
         return 0

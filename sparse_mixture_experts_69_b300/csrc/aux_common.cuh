@@ -15,12 +15,20 @@
 
 namespace moe {
 
+// Totals are kept in `groups` interleaved copies ([groups][E] each); block b
+// adds into copy b % groups, which spreads the global atomics of many blocks
+// over more addresses. The last block sums the copies in a fixed order.
 struct AuxAcc {
-    unsigned long long* P;  // [E]
-    unsigned long long* I;  // [E]
-    unsigned int* cnt;      // [E]
+    unsigned long long* P;  // [groups][E]
+    unsigned long long* I;  // [groups][E]
+    unsigned int* cnt;      // [groups][E]
     unsigned int* ticket;   // [1]
+    int groups;
 };
+
+constexpr int kAuxGroups = 8;  // copies used with a caller workspace
+
+__host__ __device__ inline size_t aux_acc_bytes(int E, int groups) { return (size_t)groups * E * 20 + 16; }
 
 struct AuxOut {
     float* f;      // [E] or NULL
@@ -30,13 +38,14 @@ struct AuxOut {
     float w_imp;
 };
 
-// acc_mem layout: [E] u64 P, [E] u64 I, [E] u32 count, u32 ticket
-inline AuxAcc aux_acc_at(void* acc_mem, int E) {
+// acc_mem layout: [groups][E] u64 P, [groups][E] u64 I, [groups][E] u32 count, u32 ticket
+__host__ __device__ inline AuxAcc aux_acc_at(void* acc_mem, int E, int groups) {
     AuxAcc a;
+    a.groups = groups;
     a.P = static_cast<unsigned long long*>(acc_mem);
-    a.I = a.P + E;
-    a.cnt = reinterpret_cast<unsigned int*>(a.I + E);
-    a.ticket = a.cnt + E;
+    a.I = a.P + (size_t)groups * E;
+    a.cnt = reinterpret_cast<unsigned int*>(a.I + (size_t)groups * E);
+    a.ticket = a.cnt + (size_t)groups * E;
     return a;
 }
 
@@ -54,96 +63,151 @@ static __device__ __forceinline__ unsigned long long to_fix(float v) {
     return sh <= -24 ? 0ull : m >> (-sh);
 }
 
-// Sum of one float per thread, in a fixed order. scratch: 33 floats.
-static __device__ float block_sum_fixed(float v, float* scratch) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Totals of expert e over the group copies (exact integer sums). With the
+// usual group count every load is issued before the first add.
+static __device__ __forceinline__ void aux_fold(const AuxAcc& acc, int E, int e,
+                                                unsigned long long& pe, unsigned long long& ie,
+                                                unsigned int& ce) {
+    pe = 0;
+    ie = 0;
+    ce = 0;
+    if (acc.groups == kAuxGroups) {
+        unsigned long long vp[kAuxGroups], vi[kAuxGroups];
+        unsigned int vc[kAuxGroups];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float tot = 0.f;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += scratch[w];
-        scratch[32] = tot;
+        for (int g = 0; g < kAuxGroups; ++g) {
+            vp[g] = __ldcg(&acc.P[(size_t)g * E + e]);
+            vi[g] = __ldcg(&acc.I[(size_t)g * E + e]);
+            vc[g] = __ldcg(&acc.cnt[(size_t)g * E + e]);
+        }
+#pragma unroll
+        for (int g = 0; g < kAuxGroups; ++g) {
+            pe += vp[g];
+            ie += vi[g];
+            ce += vc[g];
+        }
+    } else {
+        for (int g = 0; g < acc.groups; ++g) {
+            pe += __ldcg(&acc.P[(size_t)g * E + e]);
+            ie += __ldcg(&acc.I[(size_t)g * E + e]);
+            ce += __ldcg(&acc.cnt[(size_t)g * E + e]);
+        }
     }
-    __syncthreads();
-    const float tot = scratch[32];
-    __syncthreads();
-    return tot;
 }
 
-// Called by every thread of every block once the block's shared-memory totals
-// sP/sI/sC are final (after a __syncthreads). Adds them to the global
-// accumulators; the last block computes the statistics and resets.
-// The last block avoids FP64 (slow on this part): with I_e the integer gate
-// sums and N = sum_e I_e, the importance deviations E I_e - N are exact in
-// int64, so CV^2 = sum_e (E I_e - N)^2 / (E N^2) loses nothing to
-// cancellation, and aux = E / (T^2 k 2^32) * sum_e count_e * P_e (fixed
-// point) is a sum of positive terms.
-static __device__ void aux_publish_and_finalize(int T, int E, int k, AuxAcc acc, AuxOut out,
-                                                const unsigned long long* sP,
-                                                const unsigned long long* sI,
-                                                const unsigned int* sC) {
-    __shared__ float red[33];
-    __shared__ long long s_nsum[32];
-    __shared__ long long s_n;
-    __shared__ int is_last;
+// Adds a block's shared-memory totals (final: after a barrier) into its group
+// copy of the global accumulators. Integer atomics: order does not matter.
+static __device__ __forceinline__ void aux_publish(int E, const AuxAcc& acc,
+                                                   const unsigned long long* sP,
+                                                   const unsigned long long* sI,
+                                                   const unsigned int* sC) {
+    const size_t g = (size_t)(blockIdx.x % acc.groups) * E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        if (sP[e]) atomicAdd(&acc.P[e], sP[e]);
-        if (sI[e]) atomicAdd(&acc.I[e], sI[e]);
-        if (sC[e]) atomicAdd(&acc.cnt[e], sC[e]);
+        if (sP[e]) atomicAdd(&acc.P[g + e], sP[e]);
+        if (sI[e]) atomicAdd(&acc.I[g + e], sI[e]);
+        if (sC[e]) atomicAdd(&acc.cnt[g + e], sC[e]);
     }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) is_last = atomicAdd(acc.ticket, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    const float inv_fix = 2.3283064365386963e-10f;  // 2^-32
-    const float invT = 1.f / (float)T, invTk = 1.f / ((float)T * (float)k);
-    // N = sum of the gate sums (exact, int64), fixed-order reduction
-    long long nloc = 0;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) nloc += (long long)__ldcg(&acc.I[e]);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+}
+
+// Turns the global totals into f, P, importance, aux and CV^2, then zeroes the
+// accumulators and the ticket. Run by `nthreads` threads (local ids tid,
+// whole warps) of one block, synchronised by `bar`, after every contribution
+// is visible.
+// It avoids FP64 (slow on this part): with I_e the integer gate sums and
+// N = sum_e I_e, the importance deviations E I_e - N are exact in int64, so
+// CV^2 = sum_e (E I_e - N)^2 / (E N^2) loses nothing to cancellation, and
+// aux = E / (T^2 k 2^32) * sum_e count_e * P_e (fixed point) is a sum of
+// positive terms. Each thread keeps its first expert's totals in registers,
+// so there is one round of loads when E <= nthreads.
+template <typename Bar>
+static __device__ void aux_finalize(int T, int E, int k, const AuxAcc& acc, const AuxOut& out,
+                                    int tid, int nthreads, Bar bar) {
+    __shared__ long long s_n[32];
+    __shared__ float s_a[32], s_b[32];
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+    unsigned long long pe0 = 0, ie0 = 0;
+    unsigned int ce0 = 0;
+    if (tid < E) aux_fold(acc, E, tid, pe0, ie0, ce0);
+    long long nloc = (long long)ie0;
+    for (int e = tid + nthreads; e < E; e += nthreads) {
+        unsigned long long pe, ie;
+        unsigned int ce;
+        aux_fold(acc, E, e, pe, ie, ce);
+        nloc += (long long)ie;
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) nloc += __shfl_xor_sync(0xffffffffu, nloc, o);
-    if (lane == 0) s_nsum[warp] = nloc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        long long n = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) n += s_nsum[w];
-        s_n = n;
-    }
-    __syncthreads();
-    const long long N = s_n;
+    if (lane == 0) s_n[warp] = nloc;
+    bar();
+    long long N = 0;
+    for (int w = 0; w < nwarps; ++w) N += s_n[w];  // same order in every thread
+    const float inv_fix = 2.3283064365386963e-10f;  // 2^-32
+    const float invT = 1.f / (float)T, invTk = 1.f / ((float)T * (float)k);
     float s_fp = 0.f, s_dev = 0.f;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const unsigned long long pe_fix = __ldcg(&acc.P[e]);
-        const unsigned long long ie_fix = __ldcg(&acc.I[e]);
-        const unsigned int ce = __ldcg(&acc.cnt[e]);
-        const float pe = (float)pe_fix * inv_fix * invT;
+    for (int e = tid; e < E; e += nthreads) {
+        unsigned long long pe = pe0, ie = ie0;
+        unsigned int ce = ce0;
+        if (e >= nthreads) aux_fold(acc, E, e, pe, ie, ce);
+        const float p = (float)pe * inv_fix * invT;
         if (out.f) out.f[e] = (float)ce * invTk;
-        if (out.P) out.P[e] = pe;
-        if (out.I) out.I[e] = (float)ie_fix * inv_fix;
-        s_fp += (float)ce * invTk * pe;
-        const float dev = (float)((long long)ie_fix * E - N);
+        if (out.P) out.P[e] = p;
+        if (out.I) out.I[e] = (float)ie * inv_fix;
+        s_fp += (float)ce * invTk * p;
+        const float dev = (float)((long long)ie * E - N);
         s_dev += dev * dev;
     }
-    const float sum_fp = block_sum_fixed(s_fp, red);
-    const float sum_dev = block_sum_fixed(s_dev, red);
-    if (threadIdx.x == 0) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        s_fp += __shfl_xor_sync(0xffffffffu, s_fp, o);
+        s_dev += __shfl_xor_sync(0xffffffffu, s_dev, o);
+    }
+    if (lane == 0) {
+        s_a[warp] = s_fp;
+        s_b[warp] = s_dev;
+    }
+    bar();
+    if (tid == 0) {
+        float sum_fp = 0.f, sum_dev = 0.f;
+        for (int w = 0; w < nwarps; ++w) {
+            sum_fp += s_a[w];
+            sum_dev += s_b[w];
+        }
         const float n = (float)N;
         const float cv2 = sum_dev / ((float)E * n * n);
         out.out3[0] = sum_fp * (float)E;
         out.out3[1] = cv2;
         out.out3[2] = out.w_imp * cv2;
+        *acc.ticket = 0;
     }
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        acc.P[e] = 0;
-        acc.I[e] = 0;
-        acc.cnt[e] = 0;
+    // every load of the accumulators is done (the barrier above): clear them
+    for (int i = tid; i < acc.groups * E; i += nthreads) {
+        acc.P[i] = 0;
+        acc.I[i] = 0;
+        acc.cnt[i] = 0;
     }
-    if (threadIdx.x == 0) *acc.ticket = 0;
+}
+
+struct BlockBar {
+    __device__ void operator()() const { __syncthreads(); }
+};
+
+// Publish, then the last of the `participants` blocks (default: the whole
+// grid, counted with the ticket) finalises. Every thread of every
+// participating block calls this once the shared-memory totals are final.
+static __device__ void aux_publish_and_finalize(int T, int E, int k, AuxAcc acc, AuxOut out,
+                                                const unsigned long long* sP,
+                                                const unsigned long long* sI,
+                                                const unsigned int* sC, int participants = -1) {
+    __shared__ int is_last;
+    aux_publish(E, acc, sP, sI, sC);
+    __threadfence();
+    __syncthreads();
+    const unsigned n_part = participants > 0 ? (unsigned)participants : gridDim.x;
+    if (threadIdx.x == 0) is_last = atomicAdd(acc.ticket, 1u) == n_part - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    aux_finalize(T, E, k, acc, out, threadIdx.x, blockDim.x, BlockBar{});
 }
 
 }  // namespace moe

@@ -282,7 +282,8 @@ cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_his
 __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec,
                                                       const uint4* __restrict__ x,
                                                       const int32_t* __restrict__ slot,
-                                                      uint4* __restrict__ xp) {
+                                                      uint4* __restrict__ xp,
+                                                      uint4* __restrict__ y_zero) {
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -290,6 +291,10 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec,
     pdl_wait();
     const int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
     unsigned live = __ballot_sync(0xffffffffu, my_slot >= 0);
+    if (y_zero && !live) {  // dropped everywhere: its output row is zero
+        for (int v = lane; v < nvec; v += 32) y_zero[(size_t)t * nvec + v] = make_uint4(0, 0, 0, 0);
+        return;
+    }
     const uint4* src = x + (size_t)t * nvec;
     // the loop bound is warp-uniform so every shuffle has all lanes present;
     // each lane loads up to 4 vectors before storing them
@@ -315,10 +320,10 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec,
 }
 
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
-                           cudaStream_t st) {
+                           void* y_zero, cudaStream_t st) {
     const int nvec = s.d * s.esize / 16;
     return launch_k(permute_kernel, dim3((s.T + 7) / 8), dim3(256), 0, st, s.T, s.k, nvec,
-                    (const uint4*)x, slot, (uint4*)xp);
+                    (const uint4*)x, slot, (uint4*)xp, (uint4*)y_zero);
 }
 
 }  // namespace moe

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(256) aux_kernel(int T, int E, int k, int vec4,
 }
 
 cudaError_t launch_aux(const Shape& s, const float* probs, const int32_t* ids, const float* w,
-                       void* acc_mem, float* f, float* P, float* I, float* out3,
+                       void* acc_mem, int acc_groups, float* f, float* P, float* I, float* out3,
                        cudaStream_t st) {
     const int nblk = (s.T + kAuxBlockTokens - 1) / kAuxBlockTokens;
     const AuxOut out{f, P, I, out3, s.w_imp};
@@ -205,7 +205,7 @@ cudaError_t launch_aux(const Shape& s, const float* probs, const int32_t* ids, c
     // float4 loads need 16-byte aligned rows
     const int vec4 = (s.E % 4 == 0) && (reinterpret_cast<uintptr_t>(probs) % 16 == 0);
     return launch_k(aux_kernel, dim3(nblk), dim3(256), smem, st, s.T, s.E, s.k, vec4, probs, ids,
-                    w, aux_acc_at(acc_mem, s.E), out);
+                    w, aux_acc_at(acc_mem, s.E, acc_groups), out);
 }
 
 // -------------------------------------------------------------- bias update

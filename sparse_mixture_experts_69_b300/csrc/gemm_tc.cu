@@ -21,6 +21,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "aux_common.cuh"
 #include "group_table.cuh"
 
 // Compile-time tuning knobs (defaults are the measured best on B300).
@@ -159,6 +160,10 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
+// barrier among the 128 epilogue threads (warps 2..5) only
+struct EpilogueBar {
+    __device__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+};
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -291,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* mt_start = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
     float* staging = reinterpret_cast<float*>(
         (reinterpret_cast<uintptr_t>(mt_start + p.E + p.S + 1) + 15) & ~(uintptr_t)15);
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.E + p.S;
     const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
@@ -309,7 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     build_tile_table(p, BM, mt_start);
     __syncthreads();
     const int total = mt_start[G] * nt;
-    if ((int)blockIdx.x >= total) return;  // no work: leave before any allocation
+    // no work: leave before any allocation (CTA 0 stays when it owes the
+    // statistics finalisation)
+    if ((int)blockIdx.x >= total && !(p.fin_acc_mem && blockIdx.x == 0)) return;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -440,6 +446,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
+        if (p.fin_acc_mem && blockIdx.x == 0) {
+            // the statistics sums are complete (previous kernels); finalise them
+            // while the first accumulator is still being computed
+            const AuxAcc acc = aux_acc_at(p.fin_acc_mem, p.E, kAuxGroups);
+            const AuxOut out{p.fin_f, p.fin_P, p.fin_I, p.fin_out3, p.fin_w_imp};
+            aux_finalize(p.T, p.E, p.fin_k, acc, out, threadIdx.x - 64, 128, EpilogueBar{});
+        }
         const int q = warp & 3;
         const int row = 32 * q + lane;
         int local = 0;
@@ -492,6 +505,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     const int act = p.glu ? -1 : p.act;
+                    float scale = 1.f;
+                    if (routed && p.scatter_rows) {
+                        // top-1 combine: this row is token t's output, times its gate
+                        const int t = rv ? p.scatter_rows[gt.out_row + row] : 0;
+                        orow = reinterpret_cast<__nv_bfloat16*>(p.scatter_out) + (size_t)t * p.N;
+                        scale = rv ? p.scatter_scale[t] : 0.f;
+                    }
 #pragma unroll 1
                     for (int c = 0; c < BN; c += 32) {
                         float v[32];
@@ -499,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int n0 = gt.n_tile * BN + c;
                         if (rv && n0 < p.N) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = act_apply(act, v[i]);
+                            for (int i = 0; i < 32; ++i) v[i] = act_apply(act, v[i]) * scale;
                             store_bf16_row<32>(orow + n0, v, p.N - n0);
                         }
                     }
@@ -514,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+
 }
 
 // ---------------------------------------------------------------- host side

@@ -5,7 +5,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "moe_internal.cuh"
+#include "aux_common.cuh"
 
 namespace moe {
 
@@ -44,7 +44,7 @@ WsLayout ws_layout(const Shape& s) {
     const size_t es = s.esize;
     const size_t nblk = (T + kCapBlockTokens - 1) / kCapBlockTokens;
     L.status = take(256);
-    L.aux_acc = take(E * (8 + 8 + 4) + 16);
+    L.aux_acc = take(aux_acc_bytes((int)E, kAuxGroups));
     L.blk_hist = take(nblk * E * 4);
     L.cap_ticket = take(16);
     L.zero_end = off;
@@ -164,10 +164,12 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x
                                         st));
     }
     if (aux_out3) {
+        // bf16: the up GEMM (tcgen05) finalises the statistics later in the layer
         MOE_CUDA(launch_router_select_fused(s, logits, zn, noisy ? noise : nullptr, bias, probs,
                                             ids, w, status, at<int32_t>(ws, L.blk_hist),
                                             at<void>(ws, L.aux_acc), aux_vecs, aux_vecs + s.E,
-                                            aux_vecs + 2 * s.E, aux_out3, st));
+                                            aux_vecs + 2 * s.E, aux_out3,
+                                            s.dtype == MOE_BF16, st));
     } else {
         MOE_CUDA(launch_router_select(s, logits, zn, noisy ? noise : nullptr, bias, probs, sel,
                                       ids, w, 0, nullptr, nullptr, status, st));
@@ -178,18 +180,24 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x
 moe_status dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const void* x,
                          const int32_t* ids, int32_t* counts, int32_t* kept, int32_t* offsets,
                          int32_t* slot, void* xp, int32_t* row_token, bool hist_ready,
-                         cudaStream_t st) {
+                         void* y_zero, cudaStream_t st) {
     int* status = at<int>(ws, L.status);
     MOE_CUDA(launch_capacity(s, ids, at<int32_t>(ws, L.blk_hist),
                              at<unsigned int>(ws, L.cap_ticket), at<int32_t>(ws, L.blk_base),
                              counts, kept, offsets, slot, row_token, status, hist_ready, st));
-    MOE_CUDA(launch_permute(s, x, slot, xp, st));
+    MOE_CUDA(launch_permute(s, x, slot, xp, y_zero, st));
     return MOE_OK;
 }
 
+// scatter (top-1, no shared experts, bf16): the down GEMM writes y[token] =
+// gate * output directly through row_token instead of yp (no combine pass).
+// fin_aux_vecs / fin_out3 (layer path, bf16): the up GEMM finalises the
+// statistics the selection kernel accumulated.
 moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
                     const int32_t* offsets, const void* W1, const void* W2, const void* x,
-                    const void* W1s, const void* W2s, void* yp, void* ys, cudaStream_t st) {
+                    const void* W1s, const void* W2s, void* yp, void* ys,
+                    const int32_t* scatter_rows, const float* scatter_gate, void* y,
+                    float* fin_aux_vecs, float* fin_out3, cudaStream_t st) {
     int* status = at<int>(ws, L.status);
     void* h = at<void>(ws, L.h);
     void* h_shared = static_cast<char*>(h) + (size_t)s.R_max * s.F * s.esize;
@@ -214,6 +222,15 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     up.B1 = s.S ? W1s : nullptr;
     up.out0 = h;
     up.out1 = h_shared;
+    if (fin_out3) {
+        up.fin_acc_mem = at<void>(ws, L.aux_acc);
+        up.fin_f = fin_aux_vecs;
+        up.fin_P = fin_aux_vecs + s.E;
+        up.fin_I = fin_aux_vecs + 2 * s.E;
+        up.fin_out3 = fin_out3;
+        up.fin_k = s.k;
+        up.fin_w_imp = s.w_imp;
+    }
     up.status = status;
     MOE_CUDA(launch_grouped_gemm(s, up, st));
     GroupedGemm dn{};
@@ -237,6 +254,9 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     dn.B1 = s.S ? W2s : nullptr;
     dn.out0 = yp;
     dn.out1 = s.S ? ys : nullptr;
+    dn.scatter_rows = scatter_rows;
+    dn.scatter_scale = scatter_gate;
+    dn.scatter_out = y;
     dn.status = status;
     MOE_CUDA(launch_grouped_gemm(s, dn, st));
     return MOE_OK;
@@ -325,7 +345,7 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int3
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_UNSUPPORTED;
     return dispatch_impl(s, L, ws, x, topk_ids, counts, kept, offsets, slot, xp, row_token,
-                         false, (cudaStream_t)stream);
+                         false, nullptr, (cudaStream_t)stream);
 }
 
 MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
@@ -341,7 +361,8 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const i
     if (!aligned16(xp) || !aligned16(W1) || !aligned16(W2) || !aligned16(yp)) return MOE_ERR_UNSUPPORTED;
     if (s.S > 0 && (!aligned16(x) || !aligned16(W1s) || !aligned16(W2s) || !aligned16(ys)))
         return MOE_ERR_UNSUPPORTED;
-    return ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, (cudaStream_t)stream);
+    return ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, nullptr, nullptr, nullptr,
+                    nullptr, nullptr, (cudaStream_t)stream);
 }
 
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot,
@@ -368,7 +389,8 @@ MOE_API moe_status moe_aux_stats(const moe_config* cfg, const float* probs,
     MOE_TRY(make_shape(cfg, &s));
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
     if (!probs || !topk_ids || !topk_w || !out3) return MOE_ERR_INVALID_ARG;
-    MOE_CUDA(launch_aux(s, probs, topk_ids, topk_w, at<void>(ws, L.aux_acc), f, P, importance,
+    MOE_CUDA(launch_aux(s, probs, topk_ids, topk_w, at<void>(ws, L.aux_acc), kAuxGroups, f, P,
+                        importance,
                         out3, (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -418,9 +440,17 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
     // expert GEMMs, combine
     MOE_TRY(route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
                        nullptr, ids, w, av, o3, st));
-    MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token, true, st));
-    MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, st));
-    MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
+    // top-1 without shared experts: each token has at most one expert row, so the
+    // down GEMM writes y itself (dropped tokens are zeroed by the slot kernel)
+    const bool scatter = s.k == 1 && s.S == 0 && s.dtype == MOE_BF16;
+    MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token, true,
+                          scatter ? y : nullptr, st));
+    MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys,
+                     scatter ? row_token : nullptr, scatter ? w : nullptr,
+                     scatter ? y : nullptr, s.dtype == MOE_BF16 ? av : nullptr,
+                     s.dtype == MOE_BF16 ? o3 : nullptr, st));
+    if (!scatter)
+        MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
     return MOE_OK;
 }
 
@@ -492,6 +522,6 @@ extern "C" MOE_API moe_status moe_aux_stats_noalloc(const moe_config* cfg, const
     cudaStream_t st = (cudaStream_t)stream;
     // the array keeps whatever the previous call left: start this call from zero
     MOE_CUDA(cudaMemsetAsync(scratch, 0, (size_t)s.E * 20 + 16, st));
-    MOE_CUDA(launch_aux(s, probs, topk_ids, topk_w, scratch, f, P, importance, out3, st));
+    MOE_CUDA(launch_aux(s, probs, topk_ids, topk_w, scratch, 1, f, P, importance, out3, st));
     return MOE_OK;
 }

@@ -34,7 +34,7 @@ struct Shape {
 struct WsLayout {
     // regions that must read zero between calls come first (moe_workspace_reset)
     size_t status;     // int32 status word (+ padding)
-    size_t aux_acc;    // statistics accumulators: [2E] u64, [E] u32, ticket
+    size_t aux_acc;    // statistics accumulators (aux_acc_bytes(E, kAuxGroups))
     size_t blk_hist;   // [E][nblk] i32 capacity histogram counters
     size_t cap_ticket; // u32 ticket of the fused scan + slot kernel
     size_t zero_end;   // end of the zero-between-calls prefix
@@ -87,11 +87,13 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
                                  cudaStream_t st);
 
 // Layer path: selection + capacity histogram + statistics in one kernel
+// defer_final: only add the statistics sums; a later kernel of the layer (the
+// up GEMM) turns them into f, P, importance, aux and CV^2.
 cudaError_t launch_router_select_fused(const Shape& s, const float* logits, const float* zn,
                                        const float* noise, const float* bias, float* probs,
                                        int32_t* ids, float* w, int* status, int32_t* blk_hist,
                                        void* acc_mem, float* f, float* P, float* I, float* out3,
-                                       cudaStream_t st);
+                                       bool defer_final, cudaStream_t st);
 
 // Capacity: histogram -> scan -> slots; then the permute of x rows into xp
 // hist_ready: blk_hist already holds the per-block histograms (the fused router
@@ -100,8 +102,10 @@ cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_his
                             unsigned int* cap_ticket, int32_t* blk_base, int32_t* counts,
                             int32_t* kept, int32_t* offsets, int32_t* slot, int32_t* row_token,
                             int* status, bool hist_ready, cudaStream_t st);
+// y_zero (top-1 layers whose combine is done by the down GEMM): the output row
+// of a token whose only assignment was dropped is zeroed here.
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
-                           cudaStream_t st);
+                           void* y_zero, cudaStream_t st);
 
 // Grouped expert GEMMs. Up: h = act(A W1^T); down: out = h W2^T.
 struct GroupedGemm {
@@ -122,6 +126,21 @@ struct GroupedGemm {
     const void* A0; const void* A1;  // A matrices [rows, K] dtype
     const void* B0; const void* B1;  // B matrices [groups * b_rows_group, K] dtype
     void* out0; void* out1;          // [rows, N] dtype
+    // top-1 layers without shared experts (tcgen05 only): routed output row r goes
+    // to row scatter_rows[r] (its token) of scatter_out, times scatter_scale[token]
+    const int32_t* scatter_rows;
+    const float* scatter_scale;
+    void* scatter_out;
+    // layer path (tcgen05 only): statistics accumulators the previous kernels
+    // filled; CTA 0's epilogue warps finalise them while waiting for their first
+    // accumulator (fin_acc_mem == NULL: nothing to do)
+    void* fin_acc_mem;
+    float* fin_f;
+    float* fin_P;
+    float* fin_I;
+    float* fin_out3;
+    int fin_k;
+    float fin_w_imp;
     int* status;
 };
 cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream_t st);
@@ -129,8 +148,10 @@ cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream
 // Combine, statistics, bias
 cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, const float* w,
                            const void* ys, void* y, int* status, cudaStream_t st);
+// acc_groups: interleaved copies of the statistics accumulators in acc_mem
+// (aux_acc_bytes(E, acc_groups) bytes, zero between calls)
 cudaError_t launch_aux(const Shape& s, const float* probs, const int32_t* ids, const float* w,
-                       void* acc_mem, float* f, float* P, float* I, float* out3,
+                       void* acc_mem, int acc_groups, float* f, float* P, float* I, float* out3,
                        cudaStream_t st);
 cudaError_t launch_bias_update(const Shape& s, const int32_t* counts, float* bias, float rate,
                                cudaStream_t st);

@@ -267,15 +267,16 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
 }
 
 // Layer path: selection fused with the capacity histogram and the
-// load-balance statistics. Warps stride over tokens; per expert each lane
-// keeps a running fixed-point sum of its probabilities, and each chosen
+// load-balance statistics. One token per warp (the loop also covers grids
+// smaller than T/8); per expert each lane keeps a fixed-point sum of its
+// probabilities, and each chosen
 // (token, expert) adds 1 to blk_hist[e][token / kCapBlockTokens] (the scan
 // kernel zeroes those counters after reading them) and its gate to the
 // block's importance sum.
 template <int EPL>
 __global__ void __launch_bounds__(512) router_select_fused_kernel(SelectArgs a, int32_t* blk_hist,
                                                                   int nblk_cap, AuxAcc acc,
-                                                                  AuxOut out) {
+                                                                  AuxOut out, int defer_final) {
     pdl_trigger();
     pdl_wait();
     extern __shared__ unsigned long long sm64[];
@@ -313,30 +314,33 @@ __global__ void __launch_bounds__(512) router_select_fused_kernel(SelectArgs a, 
         if (e < E && regP[i]) atomicAdd(&sP[e], regP[i]);
     }
     __syncthreads();
-    aux_publish_and_finalize(a.T, E, a.k, acc, out, sP, sI, sC);
+    if (defer_final)  // a later kernel finalises the statistics
+        aux_publish(E, acc, sP, sI, sC);
+    else
+        aux_publish_and_finalize(a.T, E, a.k, acc, out, sP, sI, sC);
 }
 
 cudaError_t launch_router_select_fused(const Shape& s, const float* logits, const float* zn,
                                        const float* noise, const float* bias, float* probs,
                                        int32_t* ids, float* w, int* status, int32_t* blk_hist,
                                        void* acc_mem, float* f, float* P, float* I, float* out3,
-                                       cudaStream_t st) {
+                                       bool defer_final, cudaStream_t st) {
     SelectArgs a;
     a.T = s.T; a.E = s.E; a.k = s.k; a.renorm = s.renorm; a.from_scores = 0;
     a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
     a.sel_in = nullptr; a.probs_in = nullptr;
     a.probs = probs; a.sel = nullptr; a.ids = ids; a.w = w; a.status = status;
     const int nblk_cap = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
-    const AuxAcc acc = aux_acc_at(acc_mem, s.E);
+    const AuxAcc acc = aux_acc_at(acc_mem, s.E, kAuxGroups);
     const AuxOut out{f, P, I, out3, s.w_imp};
-    // one block per SM keeps the number of blocks adding to the same statistics
-    // counters (global atomics) small; warps stride over the tokens
+    // one token per warp, 16 warps per block; blocks spread their statistics
+    // over kAuxGroups copies
     const int warps = 16;
-    const int grid = std::min((s.T + warps - 1) / warps, num_sms());
+    const int grid = (s.T + warps - 1) / warps;
     const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int)) + 8;
 #define MOE_SEL_FUSED(EPL)                                                                  \
     return launch_k(router_select_fused_kernel<EPL>, dim3(grid), dim3(32 * warps), smem, st, a, \
-                    blk_hist, nblk_cap, acc, out)
+                    blk_hist, nblk_cap, acc, out, defer_final ? 1 : 0)
     if (s.E <= 32) MOE_SEL_FUSED(1);
     if (s.E <= 64) MOE_SEL_FUSED(2);
     if (s.E <= 128) MOE_SEL_FUSED(4);

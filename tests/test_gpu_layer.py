@@ -93,6 +93,11 @@ def test_switch_full(cuda_device):
     o3 = np32(o["out3"])
     assert o3[0] == pytest.approx(st["aux"], rel=TOL_AUX)
     assert o3[1] == pytest.approx(st["cv2"], rel=TOL_AUX)
+    av = np32(o["aux_vecs"])
+    if not diff:
+        np.testing.assert_allclose(av[0], st["f"], rtol=1e-6)
+        np.testing.assert_allclose(av[2], st["I"], rtol=TOL_AUX)
+    np.testing.assert_allclose(av[1], st["P"], rtol=TOL_AUX)
 
 
 @pytest.mark.parametrize("name,n_tok", [("mixtral", 12), ("deepseek", 8), ("decode", 16)])
