@@ -61,6 +61,12 @@ def _load():
             "oracle_combine": (None, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P]),
             "oracle_aux_stats": (None, [_I, _I, _I, _P, _P, _P, _D, _P, _P, _P, _P]),
             "oracle_bias_update": (None, [_I, _I, _I, _P, _F, _P]),
+            "oracle_select_candidates": (None, [_I, _I, _I, _I, _P, _P, _I, _P, _P]),
+            "oracle_capacity_policy": (None, [_I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P,
+                                              _P, _P]),
+            "oracle_expert_choice": (None, [_I, _I, _I, _P, _P, _P, _P]),
+            "oracle_combine_expert_choice": (None, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P]),
+            "oracle_seq_aux_stats": (None, [_I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -237,3 +243,80 @@ def ffn_for_tokens(x, tok, ids, slot, W1_of, W2_of, act, round_dtype, S=0, W1s_o
     for s in range(S):
         Os[s] = expert_ffn(x[list(tok)], W1s_of(s), W2s_of(s), act, round_dtype)
     return O, Os
+
+
+# ------------------------------------------------------- overflow policies
+
+def select_candidates(s, p, k: int, n_cand: int, renorm: bool = True):
+    """Top-n_cand candidates (the first k are the top-k choice); every gate
+    uses the top-k denominator. Returns ids [T,n_cand] int32, w [T,n_cand] double."""
+    s, p = _f32(s), _f32(p)
+    T, E = s.shape
+    ids = np.empty((T, n_cand), np.int32)
+    w = np.empty((T, n_cand), np.float64)
+    _load().oracle_select_candidates(T, E, k, n_cand, _ptr(s), _ptr(p), int(renorm), _ptr(ids),
+                                     _ptr(w))
+    return ids, w
+
+
+def capacity_policy(ids, k: int, E: int, C: int, priority: int = 0, pad: bool = False):
+    """Capacity with re-routing over ids [T,n_cand] (n_cand >= k) in token
+    (priority 0) or rank (priority 1) order; pad gives every expert C rows.
+    Returns dict counts, kept, offsets, slot, row_token (-1 on padding rows)."""
+    ids = _i32(ids)
+    T, n_cand = ids.shape
+    counts = np.empty(E, np.int32)
+    kept = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    slot = np.empty((T, n_cand), np.int32)
+    rows = max(T * n_cand, E * C if pad else 0, 1)
+    row_token = np.full(rows, -1, np.int32)
+    _load().oracle_capacity_policy(T, k, n_cand, E, C, _ptr(ids), int(priority), int(pad),
+                                   _ptr(counts), _ptr(kept), _ptr(offsets), _ptr(slot),
+                                   _ptr(row_token))
+    R = int(offsets[E])
+    return dict(counts=counts, kept=kept, offsets=offsets, slot=slot, row_token=row_token[:R])
+
+
+def expert_choice(p, C: int):
+    """Each expert takes its C most probable tokens (lower index wins ties),
+    rows in token order. Returns dict row_token [E*C], row_w [E*C] double,
+    tok_row [T,E] int32 (-1 where not chosen)."""
+    p = _f32(p)
+    T, E = p.shape
+    row_token = np.empty(max(E * C, 1), np.int32)
+    row_w = np.empty(max(E * C, 1), np.float64)
+    tok_row = np.empty((T, E), np.int32)
+    _load().oracle_expert_choice(T, E, C, _ptr(p), _ptr(row_token), _ptr(row_w), _ptr(tok_row))
+    return dict(row_token=row_token[:E * C], row_w=row_w[:E * C], tok_row=tok_row)
+
+
+def combine_expert_choice(tok_row, p, O, Os=None, round_dtype: int = ROUND_NONE):
+    """y[t] = sum over experts e choosing t (ascending e) of p[t,e] O[row] + sum_s Os[s,t].
+    O [E*C,d] double. Returns double [T,d]."""
+    tok_row, p = _i32(tok_row), _f32(p)
+    O = np.ascontiguousarray(O, np.float64)
+    T, E = tok_row.shape
+    d = O.shape[1]
+    S = 0 if Os is None else Os.shape[0]
+    Os = None if Os is None else np.ascontiguousarray(Os, np.float64)
+    y = np.empty((T, d), np.float64)
+    _load().oracle_combine_expert_choice(T, d, E, S, _ptr(tok_row), _ptr(p), _ptr(O), _ptr(Os),
+                                         int(round_dtype), _ptr(y))
+    return y
+
+
+def seq_aux_stats(p, ids, k: int, seq_offsets):
+    """Switch aux loss inside each sequence. ids [T,stride] (first k columns
+    are the top-k choice). Returns dict f, P ([n_seq,E] double), aux [n_seq], mean."""
+    p, ids, so = _f32(p), _i32(ids), _i32(seq_offsets)
+    T, E = p.shape
+    stride = ids.shape[1]
+    n_seq = so.size - 1
+    f = np.empty((max(n_seq, 1), E), np.float64)
+    P = np.empty((max(n_seq, 1), E), np.float64)
+    aux = np.empty(max(n_seq, 1), np.float64)
+    mean = ctypes.c_double()
+    _load().oracle_seq_aux_stats(E, int(k), stride, _ptr(p), _ptr(ids), n_seq, _ptr(so),
+                                 _ptr(f), _ptr(P), _ptr(aux), ctypes.byref(mean))
+    return dict(f=f[:n_seq], P=P[:n_seq], aux=aux[:n_seq], mean=mean.value)

@@ -30,6 +30,16 @@
  *               sum_x G(x), CV = sigma/mu, L = w * CV^2.
  *   bias update heavensheep.xyz notes / ld246.com Q3: an over-used expert's
  *               bias goes down, an idle expert's goes up.
+ *   overflow    "MoE notes", section Expert capacity: once an expert is
+ *   policies    full, later tokens go to their next candidate expert, and a
+ *               token whose candidates are all full skips the layer;
+ *               mkbk-pku.cn MoE notes, capacity section: drop, second-choice
+ *               re-routing, or padding every expert to its capacity.
+ *   expert      heavensheep.xyz notes, Routing Function ("expert choose
+ *   choice      token" balances the load); xutianle.me CS336-04, section 3
+ *               (routing can be reversed: experts select tokens).
+ *   sequence    heavensheep.xyz notes, Training: the same balance
+ *   statistics  statistics taken inside each sequence instead of the batch.
  *
  * Inputs arrive as float (bf16 values are widened exactly by the caller).
  * Rounding of intermediates to the storage dtype is optional (round_dtype:
@@ -142,6 +152,29 @@ void oracle_select(int T, int E, int k, const float* s, const float* p, int reno
     free(prow);
 }
 
+/* Top-n_cand candidates per token (n_cand >= k): the first k are the
+ * KeepTopK choice, the rest are the next candidates in score order, tried
+ * when a choice is full. Every candidate's gate uses the denominator of the
+ * top-k choice: w_j = p_j / sum_{j'<k} p_j' (renorm=1) or p_j (renorm=0), so
+ * the capacity stage never changes a gate value, only which candidates are
+ * kept. ids and w are [T,n_cand]. */
+void oracle_select_candidates(int T, int E, int k, int n_cand, const float* s, const float* p,
+                              int renorm, int32_t* ids, double* w) {
+    double* srow = (double*)malloc(sizeof(double) * E);
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) srow[e] = s[(size_t)t * E + e];
+        int32_t* id = ids + (size_t)t * n_cand;
+        topk_row(E, n_cand, srow, id);
+        double den = 0.0;
+        for (int j = 0; j < k; ++j) den += (double)p[(size_t)t * E + id[j]];
+        for (int j = 0; j < n_cand; ++j) {
+            double pj = (double)p[(size_t)t * E + id[j]];
+            w[(size_t)t * n_cand + j] = renorm ? pj / den : pj;
+        }
+    }
+    free(srow);
+}
+
 /* ----------------------------------------------------------------- router */
 
 /* Router for T tokens.
@@ -243,6 +276,115 @@ void oracle_capacity(int T, int k, int E, int C, const int32_t* ids, int32_t* co
     free(local);
 }
 
+/* Capacity with an overflow policy. Each token needs k experts and holds
+ * n_cand >= k candidates ids[t,0..n_cand-1] in rank order. Candidates are
+ * visited one at a time in the priority order
+ *   priority 0 (token order): token by token, each token's candidates in rank order
+ *   priority 1 (rank order):  rank by rank, each rank's tokens in token order
+ * and a visit does: if the token still needs an expert, it tries the candidate;
+ * the try succeeds when the expert holds fewer than C rows, and the candidate
+ * takes the expert's next row. A failed try moves the token on to its next
+ * candidate (re-routing); a token that runs out of candidates keeps fewer than
+ * k experts (with n_cand == k this is plain dropping).
+ * Outputs:
+ *   counts[e]  top-k choices (candidates 0..k-1) naming e, before capacity
+ *   kept[e]    rows taken by expert e
+ *   offsets    pad == 0: exclusive prefix sum of kept (E+1 entries);
+ *              pad == 1: offsets[e] = e C (every expert's block is C rows)
+ *   slot[t,j]  row of a kept candidate, -1 otherwise ([T,n_cand])
+ *   row_token  token of each kept row */
+void oracle_capacity_policy(int T, int k, int n_cand, int E, int C, const int32_t* ids,
+                            int priority, int pad, int32_t* counts, int32_t* kept,
+                            int32_t* offsets, int32_t* slot, int32_t* row_token) {
+    const size_t n = (size_t)T * n_cand;
+    int32_t* local = (int32_t*)malloc(sizeof(int32_t) * (n ? n : 1));
+    int32_t* need = (int32_t*)malloc(sizeof(int32_t) * (T ? T : 1));
+    for (int e = 0; e < E; ++e) {
+        counts[e] = 0;
+        kept[e] = 0;
+    }
+    for (int t = 0; t < T; ++t) {
+        need[t] = k;
+        for (int j = 0; j < k; ++j) counts[ids[(size_t)t * n_cand + j]] += 1;
+    }
+    for (size_t a = 0; a < n; ++a) local[a] = -1;
+    for (size_t v = 0; v < n; ++v) {
+        int t, j;
+        if (priority == 0) {
+            t = (int)(v / n_cand);
+            j = (int)(v % n_cand);
+        } else {
+            j = (int)(v / T);
+            t = (int)(v % T);
+        }
+        if (need[t] == 0) continue;
+        size_t a = (size_t)t * n_cand + j;
+        int e = ids[a];
+        if (kept[e] < C) {
+            local[a] = kept[e];
+            kept[e] += 1;
+            need[t] -= 1;
+        }
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = pad ? (e + 1) * C : offsets[e] + kept[e];
+    for (size_t a = 0; a < n; ++a) {
+        if (local[a] < 0) {
+            slot[a] = -1;
+        } else {
+            int row = offsets[ids[a]] + local[a];
+            slot[a] = row;
+            row_token[row] = (int32_t)(a / n_cand);
+        }
+    }
+    free(local);
+    free(need);
+}
+
+/* Expert-choice routing: expert e takes the C tokens with the largest
+ * probability p[t,e] (ties: the lower token index first). Expert e's rows are
+ * e C .. e C + C - 1, holding its chosen tokens in increasing token order; the
+ * gate of a row is p[token,e]. C must not exceed T.
+ *   row_token [E*C], row_w [E*C], tok_row [T,E] (row of (t,e) or -1). */
+typedef struct {
+    double p;
+    int t;
+} oracle_pt;
+static int cmp_pt_desc(const void* a, const void* b) {
+    const oracle_pt* x = (const oracle_pt*)a;
+    const oracle_pt* y = (const oracle_pt*)b;
+    if (x->p > y->p) return -1;
+    if (x->p < y->p) return 1;
+    return x->t < y->t ? -1 : (x->t > y->t);
+}
+static int cmp_int(const void* a, const void* b) {
+    int x = *(const int*)a, y = *(const int*)b;
+    return x < y ? -1 : (x > y);
+}
+void oracle_expert_choice(int T, int E, int C, const float* p, int32_t* row_token, double* row_w,
+                          int32_t* tok_row) {
+    oracle_pt* col = (oracle_pt*)malloc(sizeof(oracle_pt) * (T ? T : 1));
+    int* chosen = (int*)malloc(sizeof(int) * (C ? C : 1));
+    for (size_t i = 0; i < (size_t)T * E; ++i) tok_row[i] = -1;
+    for (int e = 0; e < E; ++e) {
+        for (int t = 0; t < T; ++t) {
+            col[t].p = (double)p[(size_t)t * E + e];
+            col[t].t = t;
+        }
+        qsort(col, T, sizeof(oracle_pt), cmp_pt_desc);
+        for (int i = 0; i < C; ++i) chosen[i] = col[i].t;
+        qsort(chosen, C, sizeof(int), cmp_int);
+        for (int i = 0; i < C; ++i) {
+            int r = e * C + i, t = chosen[i];
+            row_token[r] = t;
+            row_w[r] = (double)p[(size_t)t * E + e];
+            tok_row[(size_t)t * E + e] = r;
+        }
+    }
+    free(col);
+    free(chosen);
+}
+
 /* Dispatch: xp[slot[t,j]] = x[t] for every kept assignment. */
 void oracle_dispatch(int T, int d, int k, const float* x, const int32_t* slot, float* xp) {
     for (int t = 0; t < T; ++t)
@@ -315,6 +457,24 @@ void oracle_combine(int n, int d, int k, int S, const double* w, const int32_t* 
         }
 }
 
+/* Expert-choice combine: y[t] = sum over experts e (ascending) that chose t
+ * of p[t,e] * O[tok_row[t,e],:]  +  sum_s Os[s,t,:]. O is [E*C,d]. */
+void oracle_combine_expert_choice(int T, int d, int E, int S, const int32_t* tok_row,
+                                  const float* p, const double* O, const double* Os,
+                                  int round_dtype, double* y) {
+    for (int t = 0; t < T; ++t)
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int e = 0; e < E; ++e) {
+                int r = tok_row[(size_t)t * E + e];
+                if (r < 0) continue;
+                acc += (double)p[(size_t)t * E + e] * O[(size_t)r * d + i];
+            }
+            for (int s2 = 0; s2 < S; ++s2) acc += Os[((size_t)s2 * T + t) * d + i];
+            y[(size_t)t * d + i] = round_to(acc, round_dtype);
+        }
+}
+
 /* -------------------------------------------------------------- statistics */
 
 /* Load-balance statistics over the batch.
@@ -355,6 +515,47 @@ void oracle_aux_stats(int T, int E, int k, const float* p, const int32_t* ids, c
     out3[0] = aux;
     out3[1] = cv2;
     out3[2] = w_imp * cv2;
+}
+
+/* Sequence-level balance statistics: the Switch aux loss of the batch,
+ * taken inside each sequence. Sequence q holds tokens seq_offsets[q] ..
+ * seq_offsets[q+1]-1 (T_q of them):
+ *   f[q,e]  = (top-k choices of its tokens naming e) / (T_q k)
+ *   P[q,e]  = mean over its tokens of p[t,e]
+ *   aux[q]  = E * sum_e f[q,e] P[q,e]
+ *   mean    = mean of aux[q] over the non-empty sequences (0 if none)
+ * An empty sequence has f = P = aux = 0. ids has `stride` columns per token;
+ * its first k are the top-k choice. */
+void oracle_seq_aux_stats(int E, int k, int stride, const float* p, const int32_t* ids,
+                          int n_seq, const int32_t* seq_offsets, double* f, double* P,
+                          double* aux, double* mean) {
+    double total = 0.0;
+    int nonempty = 0;
+    for (int q = 0; q < n_seq; ++q) {
+        int t0 = seq_offsets[q], t1 = seq_offsets[q + 1];
+        double* fq = f + (size_t)q * E;
+        double* Pq = P + (size_t)q * E;
+        for (int e = 0; e < E; ++e) {
+            fq[e] = 0.0;
+            Pq[e] = 0.0;
+        }
+        aux[q] = 0.0;
+        if (t1 <= t0) continue;
+        for (int t = t0; t < t1; ++t) {
+            for (int j = 0; j < k; ++j) fq[ids[(size_t)t * stride + j]] += 1.0;
+            for (int e = 0; e < E; ++e) Pq[e] += (double)p[(size_t)t * E + e];
+        }
+        double a = 0.0;
+        for (int e = 0; e < E; ++e) {
+            fq[e] /= (double)(t1 - t0) * (double)k;
+            Pq[e] /= (double)(t1 - t0);
+            a += fq[e] * Pq[e];
+        }
+        aux[q] = (double)E * a;
+        total += aux[q];
+        nonempty += 1;
+    }
+    *mean = nonempty ? total / nonempty : 0.0;
 }
 
 /* Loss-free balance: bias[e] -= rate when expert e took more than the mean
