@@ -75,6 +75,13 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 typedef enum { MOE_RELU = 0, MOE_GELU = 1, MOE_SWIGLU = 2 } moe_act;
+/* Who chooses ("MoE notes" / heavensheep.xyz, Routing Function): tokens pick
+ * their top-k experts, or each expert picks its C most probable tokens. */
+typedef enum { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_routing;
+/* Order in which token-choice assignments claim expert capacity: token by
+ * token (each token's candidates in rank order), or rank by rank (every
+ * token's first choice before any second choice). */
+typedef enum { MOE_PRIORITY_TOKEN = 0, MOE_PRIORITY_RANK = 1 } moe_priority;
 
 /* Problem statement of one MoE layer call. */
 typedef struct {
@@ -89,13 +96,28 @@ typedef struct {
     int32_t dtype;           /* moe_dtype of x, weights, h, expert outputs, y  */
     int32_t act;             /* moe_act; SwiGLU = silu(gate) * up              */
     float importance_weight; /* w in L_importance = w * CV^2                   */
+    /* Overflow policy ("MoE notes", Expert capacity: a full expert sends the
+     * token to its next candidate; mkbk-pku.cn MoE notes: drop, second-choice
+     * re-routing, or padding to capacity). Zero-initialised fields give the
+     * default: drop, token order, packed rows, token choice. */
+    int32_t reroute;         /* r >= 0 extra candidates a token tries, in rank
+                                order, when a choice is full; 0 = drop.
+                                n_cand = k + r <= min(E, 32)                   */
+    int32_t priority;        /* moe_priority                                   */
+    int32_t pad_to_capacity; /* 1: expert e owns rows e*C .. e*C+C-1, unused
+                                ones zero, and the expert GEMMs run on all
+                                E*C rows (fixed shapes, wasted FLOPs)          */
+    int32_t routing;         /* moe_routing                                    */
 } moe_config;
+
+/* Terms used below: n_cand = top_k + reroute candidates per token. R_max =
+ * E*C when pad_to_capacity or expert choice, else min(T*k, E*C). */
 
 /* Human-readable name of a status code (static string). */
 MOE_API const char* moe_status_string(moe_status status);
 
-/* Capacity C and the row bound R_max = min(T*k, E*C) of the expert-sorted
- * buffers (xp, yp, row_token). Host only. */
+/* Capacity C and the row bound R_max of the expert-sorted buffers (xp, yp,
+ * row_token). Host only. */
 MOE_API moe_status moe_capacity(const moe_config* cfg, int32_t* capacity, int32_t* rows_max);
 
 /* Bytes of workspace any entry point below needs for this configuration.
@@ -120,10 +142,16 @@ MOE_API moe_status moe_workspace_reset(const moe_config* cfg, void* ws, size_t w
  *   logits  out  [T,E] float32          z = x.Wg (+ offset), fp32 accumulation
  *   probs   out  [T,E] float32          p = softmax(H), max subtracted, fp32
  *   sel_scores   [T,E] float32 or NULL  out: the scores top-k ranked (H, or p + bias)
- *   topk_ids out [T,k] int32            descending score, lower index wins ties
- *   topk_w   out [T,k] float32          gates from the unbiased p
+ *   topk_ids out [T,n_cand] int32       descending score, lower index wins ties;
+ *                                       the first k are the top-k choice, the
+ *                                       rest the re-route candidates in order
+ *   topk_w   out [T,n_cand] float32     gates from the unbiased p: p_j / (sum of
+ *                                       p over the first k) with renorm_topk,
+ *                                       else p_j; capacity never changes them
  * from_scores = 1 skips the logits: top-k is taken on the caller's sel_scores
- * (input) and gates on the caller's probs (input); x, Wg, logits are unused. */
+ * (input) and gates on the caller's probs (input); x, Wg, logits are unused.
+ * With routing = MOE_EXPERT_CHOICE topk_ids and topk_w may be NULL (the
+ * probabilities are what moe_expert_choice_dispatch needs). */
 MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* Wg,
                              const void* Wnoise, const float* noise, const float* logit_offset,
                              const float* sel_bias, float* logits, float* probs,
@@ -131,15 +159,29 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* W
                              int32_t from_scores, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Capacity and dispatch ("MoE notes", Expert capacity; mkbk-pku.cn MoE notes,
- * bucketize + contiguous packing). Assignments are served in token order
- * (within a token, in rank order); the first C of each expert are kept.
- *   x         [T,d] dtype, topk_ids [T,k] int32 (distinct per token, in [0,E))
- *   counts    out [E] int32    assignments per expert before the cap
- *   kept      out [E] int32    min(counts, C)
- *   offsets   out [E+1] int32  exclusive prefix sum of kept; R = offsets[E]
- *   slot      out [T,k] int32  row of the assignment in xp, -1 if dropped
- *   xp        out [R_max,d] dtype  xp[slot[t,j]] = x[t]; rows >= R untouched
- *   row_token out [R_max] int32    token of each row < R */
+ * bucketize + contiguous packing, capacity section).
+ * Candidates are visited in the priority order (cfg->priority); a visit by a
+ * token that still needs an expert succeeds if the expert holds fewer than C
+ * rows, and the candidate takes the expert's next row; after a failed visit
+ * the token moves on to its next candidate (reroute > 0), and a token that
+ * runs out of candidates keeps fewer than k experts. With reroute = 0 and
+ * token priority this is plain dropping in token order: the first C
+ * assignments of each expert are kept.
+ *   x         [T,d] dtype, topk_ids [T,n_cand] int32 (distinct per token, in [0,E))
+ *   counts    out [E] int32    top-k choices (first k candidates) per expert,
+ *                              before capacity
+ *   kept      out [E] int32    rows taken by each expert (min(counts, C) when
+ *                              reroute = 0)
+ *   offsets   out [E+1] int32  exclusive prefix sum of kept, or e*C with
+ *                              pad_to_capacity; R = offsets[E]
+ *   slot      out [T,n_cand] int32  row of a kept candidate in xp, -1 otherwise
+ *   xp        out [R_max,d] dtype  xp[slot[t,j]] = x[t]; with pad_to_capacity
+ *                              the unused rows of each block are zeroed,
+ *                              otherwise rows >= R are untouched
+ *   row_token out [R_max] int32    token of each kept row
+ * Re-routing or rank priority supports E <= 512 and T <= 131072 and returns
+ * MOE_ERR_UNSUPPORTED beyond; its device loop is bounded and records
+ * MOE_ERR_TIMEOUT if it ever fails to settle. */
 MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_ids,
                                 int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot,
                                 void* xp, int32_t* row_token, void* ws, size_t ws_bytes,
@@ -163,7 +205,8 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const i
  *        + sum_s ys[s,t]
  * accumulated in fp32 in a fixed order (deterministic), stored in dtype.
  * Dropped assignments add nothing and the gates are not renormalised.
- *   yp [R_max,d], slot [T,k], topk_w [T,k], ys [S,T,d] or NULL, y out [T,d]. */
+ *   yp [R_max,d], slot [T,n_cand], topk_w [T,n_cand], ys [S,T,d] or NULL,
+ *   y out [T,d]. */
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot,
                                const float* topk_w, const void* ys, void* y, void* ws,
                                size_t ws_bytes, moe_stream_t stream);
@@ -177,6 +220,7 @@ MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int3
  *            cv2 = (population std of importance / its mean)^2,
  *            L_imp = importance_weight * cv2 }
  * f, P, importance: out [E] float32 or NULL; out3: out [3] float32.
+ * topk_ids / topk_w are [T,n_cand]; only the first k columns are used.
  * Reduction order is fixed (deterministic). */
 MOE_API moe_status moe_aux_stats(const moe_config* cfg, const float* probs,
                                  const int32_t* topk_ids, const float* topk_w, float* f,
@@ -192,10 +236,13 @@ MOE_API moe_status moe_bias_update(const moe_config* cfg, const int32_t* counts,
 /* The whole layer: route -> dispatch -> expert FFN -> combine -> statistics.
  * Inputs as in moe_route and moe_expert_ffn. Outputs:
  *   y         [T,d] dtype
- *   topk_ids  [T,k] int32 or NULL, topk_w [T,k] float32 or NULL
+ *   topk_ids  [T,n_cand] int32 or NULL, topk_w [T,n_cand] float32 or NULL
  *   counts    [E] int32 or NULL (before capacity)
  *   aux_vecs  [3,E] float32 or NULL: rows f, P, importance
  *   out3      [3] float32 or NULL: aux, cv2, L_imp
+ * With routing = MOE_EXPERT_CHOICE the layer runs moe_expert_choice_dispatch
+ * and moe_expert_choice_combine instead; topk_ids, topk_w, counts, aux_vecs
+ * and out3 must then be NULL (the token-choice statistics do not apply).
  * Intermediates (logits, probs, slots, xp, h, yp, ys) live in ws. */
 MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const void* Wg,
                                  const void* Wnoise, const float* noise,
@@ -204,6 +251,54 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
                                  const void* W2s, void* y, int32_t* topk_ids, float* topk_w,
                                  int32_t* counts, float* aux_vecs, float* out3, void* ws,
                                  size_t ws_bytes, moe_stream_t stream);
+
+/* Expert-choice routing (heavensheep.xyz MoE notes, Routing Function: experts
+ * choose tokens, which balances the load; xutianle.me CS336-04, section 3).
+ * Expert e takes the C tokens with the largest probs[t,e] (the lower token
+ * index first among equal values). Its rows are e*C .. e*C+C-1 and hold its
+ * chosen tokens in increasing token order; the gate of a row is
+ * probs[token,e]. A token may be chosen by several experts or by none.
+ *   x         [T,d] dtype;  probs [T,E] float32 (from moe_route)
+ *   offsets   out [E+1] int32   e*C (for moe_expert_ffn)
+ *   row_token out [E*C] int32   token of each row
+ *   row_w     out [E*C] float32 gate of each row
+ *   tok_row   out [T,E] int32   row of (t,e), -1 if e did not choose t
+ *   xp        out [E*C,d] dtype xp[r] = x[row_token[r]]
+ * Supports T <= 32768 (MOE_ERR_UNSUPPORTED beyond). */
+MOE_API moe_status moe_expert_choice_dispatch(const moe_config* cfg, const void* x,
+                                              const float* probs, int32_t* offsets,
+                                              int32_t* row_token, float* row_w,
+                                              int32_t* tok_row, void* xp, void* ws,
+                                              size_t ws_bytes, moe_stream_t stream);
+
+/* Expert-choice combine:
+ *   y[t] = sum over experts e that chose t, in increasing e, of
+ *          probs[t,e] * yp[tok_row[t,e]]  +  sum_s ys[s,t]
+ * in fp32 (deterministic), stored in dtype; a token no expert chose gets the
+ * shared experts only (zero without them).
+ *   yp [E*C,d] dtype, tok_row [T,E], probs [T,E], ys [S,T,d] or NULL, y out [T,d]. */
+MOE_API moe_status moe_expert_choice_combine(const moe_config* cfg, const void* yp,
+                                             const int32_t* tok_row, const float* probs,
+                                             const void* ys, void* y, void* ws, size_t ws_bytes,
+                                             moe_stream_t stream);
+
+/* Sequence-level balance statistics (heavensheep.xyz MoE notes, Training: the
+ * batch balance term taken inside each sequence, so that no single sequence
+ * is skewed). Sequence q holds tokens seq_offsets[q] .. seq_offsets[q+1]-1
+ * (T_q of them):
+ *   f_seq[q,e] = (top-k choices of its tokens naming e) / (T_q k)
+ *   P_seq[q,e] = mean over its tokens of probs[t,e]
+ *   aux_seq[q] = E * sum_e f_seq[q,e] P_seq[q,e]   (0 for an empty sequence)
+ *   aux_mean   = mean of aux_seq over the non-empty sequences (0 if none)
+ * probs [T,E] float32, topk_ids [T,n_cand] (first k columns used),
+ * seq_offsets [n_seq+1] int32 device, non-decreasing from 0 to T (device
+ * check: MOE_ERR_DEVICE_ARG); f_seq, P_seq [n_seq,E] float32 or NULL;
+ * aux_seq [n_seq] float32; aux_mean [1] float32. Deterministic. */
+MOE_API moe_status moe_seq_aux_stats(const moe_config* cfg, const float* probs,
+                                     const int32_t* topk_ids, const int32_t* seq_offsets,
+                                     int32_t n_seq, float* f_seq, float* P_seq, float* aux_seq,
+                                     float* aux_mean, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream);
 
 /* Statistics without a workspace. The pages have no counterpart to this call.
  *

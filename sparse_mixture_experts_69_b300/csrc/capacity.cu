@@ -63,7 +63,7 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 
 // One block of 1024 threads. Warp w scans experts w, w+32, ...
 __global__ void __launch_bounds__(1024) cap_scan_kernel(
-    int nblk, int E, int C, int32_t* __restrict__ blk_hist, int32_t* __restrict__ blk_base,
+    int nblk, int E, int C, int pad, int32_t* __restrict__ blk_hist, int32_t* __restrict__ blk_base,
     int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets) {
     pdl_trigger();
     pdl_wait();
@@ -103,8 +103,8 @@ __global__ void __launch_bounds__(1024) cap_scan_kernel(
         wsum[lane] = si - s;
     }
     __syncthreads();
-    if (e < E) offsets[e] = wsum[warp] + incl - v;
-    if (e == E - 1) offsets[E] = wsum[warp] + incl;
+    if (e < E) offsets[e] = pad ? e * C : wsum[warp] + incl - v;
+    if (e == E - 1) offsets[E] = pad ? E * C : wsum[warp] + incl;
 }
 
 // Dynamic smem: mask[8][E] lane bitmasks (bit l of mask[w][e]: lane l of warp w chose e)
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kCapBlockTokens) cap_slot_kernel(
 constexpr int kMaxFusedCapBlocks = 256;
 
 __global__ void __launch_bounds__(kCapBlockTokens) cap_scan_slot_kernel(
-    int T, int k, int E, int C, int nblk, const int32_t* __restrict__ ids,
+    int T, int k, int E, int C, int pad, int nblk, const int32_t* __restrict__ ids,
     int32_t* __restrict__ blk_hist, unsigned int* __restrict__ ticket,
     int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
     int32_t* __restrict__ slot, int32_t* __restrict__ row_token) {
@@ -210,10 +210,10 @@ __global__ void __launch_bounds__(kCapBlockTokens) cap_scan_slot_kernel(
     int acc = wbase + incl - run;
     for (int e = lo; e < hi; ++e) {
         const int kv = s_off[e];
-        s_off[e] = acc;
+        s_off[e] = pad ? e * C : acc;
         acc += kv;
     }
-    if (threadIdx.x == blockDim.x - 1) s_off[E] = acc;
+    if (threadIdx.x == blockDim.x - 1) s_off[E] = pad ? E * C : acc;
     __syncthreads();
     if (b == 0)
         for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
@@ -264,11 +264,11 @@ cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_his
         const size_t smem = (size_t)(kCapBlockTokens / 32) * s.E * sizeof(unsigned) +
                             (size_t)(2 * s.E + 1) * sizeof(int);
         return launch_k(cap_scan_slot_kernel, dim3(nblk), dim3(kCapBlockTokens), smem, st, s.T,
-                        s.k, s.E, s.C, nblk, ids, blk_hist, cap_ticket, counts, kept, offsets,
-                        slot, row_token);
+                        s.k, s.E, s.C, s.pad, nblk, ids, blk_hist, cap_ticket, counts, kept,
+                        offsets, slot, row_token);
     }
-    err = launch_k(cap_scan_kernel, dim3(1), dim3(1024), 0, st, nblk, s.E, s.C, blk_hist, blk_base,
-                   counts, kept, offsets);
+    err = launch_k(cap_scan_kernel, dim3(1), dim3(1024), 0, st, nblk, s.E, s.C, s.pad, blk_hist,
+                   blk_base, counts, kept, offsets);
     if (err != cudaSuccess) return err;
     const size_t smem = (size_t)(kCapBlockTokens / 32) * s.E * sizeof(unsigned);
     return launch_k(cap_slot_kernel, dim3(nblk), dim3(kCapBlockTokens), smem, st, s.T, s.k, s.E,
@@ -279,17 +279,21 @@ cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_his
 // ---------------------------------------------------------------- permute
 // One warp per token: read the row once (16-byte vectors), write it to each of
 // the token's kept rows. Algorithmic bytes: T d b read + R d b written.
-__global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec,
+__global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec, int rows,
                                                       const uint4* __restrict__ x,
                                                       const int32_t* __restrict__ slot,
                                                       uint4* __restrict__ xp,
-                                                      uint4* __restrict__ y_zero) {
+                                                      uint4* __restrict__ y_zero, int* status) {
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
     pdl_wait();
-    const int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
+    int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
+    if (my_slot >= rows) {  // never produced by the capacity kernels: skip and report
+        flag_status(status, DEV_BAD_ARG | DEV_SITE_PERMUTE_ROW);
+        my_slot = -1;
+    }
     unsigned live = __ballot_sync(0xffffffffu, my_slot >= 0);
     if (y_zero && !live) {  // dropped everywhere: its output row is zero
         for (int v = lane; v < nvec; v += 32) y_zero[(size_t)t * nvec + v] = make_uint4(0, 0, 0, 0);
@@ -320,10 +324,10 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec,
 }
 
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
-                           void* y_zero, cudaStream_t st) {
+                           void* y_zero, int* status, cudaStream_t st) {
     const int nvec = s.d * s.esize / 16;
-    return launch_k(permute_kernel, dim3((s.T + 7) / 8), dim3(256), 0, st, s.T, s.k, nvec,
-                    (const uint4*)x, slot, (uint4*)xp, (uint4*)y_zero);
+    return launch_k(permute_kernel, dim3((s.T + 7) / 8), dim3(256), 0, st, s.T, s.nc, nvec,
+                    s.R_max, (const uint4*)x, slot, (uint4*)xp, (uint4*)y_zero, status);
 }
 
 }  // namespace moe

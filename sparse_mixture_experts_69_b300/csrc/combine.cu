@@ -126,10 +126,10 @@ cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, 
                            const void* ys, void* y, int* status, cudaStream_t st) {
     dim3 grid((s.T + 7) / 8), block(256);
     if (s.dtype == MOE_BF16)
-        return launch_k(combine_kernel<__nv_bfloat16, 2>, grid, block, 0, st, s.T, s.d, s.k,
+        return launch_k(combine_kernel<__nv_bfloat16, 2>, grid, block, 0, st, s.T, s.d, s.nc,
                         ys ? s.S : 0, (const __nv_bfloat16*)yp, slot, w, (const __nv_bfloat16*)ys,
                         (__nv_bfloat16*)y, status);
-    return launch_k(combine_kernel<float, 2>, grid, block, 0, st, s.T, s.d, s.k, ys ? s.S : 0,
+    return launch_k(combine_kernel<float, 2>, grid, block, 0, st, s.T, s.d, s.nc, ys ? s.S : 0,
                     (const float*)yp, slot, w, (const float*)ys, (float*)y, status);
 }
 
@@ -137,7 +137,8 @@ cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, 
 // One launch; each block takes kAuxBlockTokens tokens, sums them per expert in
 // shared memory (integers, see aux_common.cuh) and publishes; the last block
 // finalises.
-__global__ void __launch_bounds__(256) aux_kernel(int T, int E, int k, int vec4,
+// ids and w hold `stride` columns per token; the first k are the top-k choice.
+__global__ void __launch_bounds__(256) aux_kernel(int T, int E, int k, int stride, int vec4,
                                                   const float* __restrict__ probs,
                                                   const int32_t* __restrict__ ids,
                                                   const float* __restrict__ w, AuxAcc acc,
@@ -187,9 +188,10 @@ __global__ void __launch_bounds__(256) aux_kernel(int T, int E, int k, int vec4,
         }
     }
     for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
-        const int e = ids[(size_t)t0 * k + i];
+        const size_t a = (size_t)(t0 + i / k) * stride + i % k;
+        const int e = ids[a];
         if (e < 0 || e >= E) continue;
-        atomicAdd(&sI[e], to_fix(w[(size_t)t0 * k + i]));
+        atomicAdd(&sI[e], to_fix(w[a]));
         atomicAdd(&sC[e], 1u);
     }
     __syncthreads();
@@ -204,8 +206,8 @@ cudaError_t launch_aux(const Shape& s, const float* probs, const int32_t* ids, c
     const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int)) + 8;
     // float4 loads need 16-byte aligned rows
     const int vec4 = (s.E % 4 == 0) && (reinterpret_cast<uintptr_t>(probs) % 16 == 0);
-    return launch_k(aux_kernel, dim3(nblk), dim3(256), smem, st, s.T, s.E, s.k, vec4, probs, ids,
-                    w, aux_acc_at(acc_mem, s.E, acc_groups), out);
+    return launch_k(aux_kernel, dim3(nblk), dim3(256), smem, st, s.T, s.E, s.k, s.nc, vec4, probs,
+                    ids, w, aux_acc_at(acc_mem, s.E, acc_groups), out);
 }
 
 // -------------------------------------------------------------- bias update

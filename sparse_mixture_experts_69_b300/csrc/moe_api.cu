@@ -40,21 +40,26 @@ WsLayout ws_layout(const Shape& s) {
         off = align256(off + std::max<size_t>(bytes, 1));
         return o;
     };
-    const size_t T = s.T, E = s.E, k = s.k, d = s.d, F = s.F, S = s.S, R = s.R_max;
+    const size_t T = s.T, E = s.E, d = s.d, F = s.F, S = s.S, R = s.R_max;
     const size_t es = s.esize;
     const size_t nblk = (T + kCapBlockTokens - 1) / kCapBlockTokens;
     L.status = take(256);
     L.aux_acc = take(aux_acc_bytes((int)E, kAuxGroups));
     L.blk_hist = take(nblk * E * 4);
     L.cap_ticket = take(16);
+    L.seq_ticket = take(16);
     L.zero_end = off;
     L.zn = take(T * E * 4);
     L.wgT = take(2 * E * d * es);
     L.logits = take(T * E * 4);
     L.probs = take(T * E * 4);
-    L.ids = take(T * k * 4);
-    L.w = take(T * k * 4);
-    L.slot = take(T * k * 4);
+    const size_t nc = s.nc;
+    const bool ec = s.routing == MOE_EXPERT_CHOICE;
+    L.ids = take(T * nc * 4);
+    L.w = take(T * nc * 4);
+    L.slot = take(T * nc * 4);
+    L.tok_row = take(ec ? T * E * 4 : 0);
+    L.row_w = take(ec ? R * 4 : 0);
     L.counts = take(E * 4);
     L.kept = take(E * 4);
     L.offsets = take((E + 1) * 4);
@@ -88,18 +93,33 @@ moe_status make_shape(const moe_config* c, Shape* s) {
     if (c->renorm_topk != 0 && c->renorm_topk != 1) return MOE_ERR_INVALID_ARG;
     if (!isfinite(c->capacity_factor) || !isfinite(c->importance_weight))
         return MOE_ERR_INVALID_ARG;
-    if (c->n_experts > 1024 || c->top_k > 32 || c->n_shared > 64) return MOE_ERR_UNSUPPORTED;
+    if (c->reroute < 0 || c->priority < MOE_PRIORITY_TOKEN || c->priority > MOE_PRIORITY_RANK ||
+        (c->pad_to_capacity != 0 && c->pad_to_capacity != 1) || c->routing < MOE_TOKEN_CHOICE ||
+        c->routing > MOE_EXPERT_CHOICE)
+        return MOE_ERR_INVALID_ARG;
+    const bool ec = c->routing == MOE_EXPERT_CHOICE;
+    if (ec && (c->reroute != 0 || c->priority != MOE_PRIORITY_TOKEN)) return MOE_ERR_INVALID_ARG;
+    if ((long long)c->top_k + c->reroute > c->n_experts) return MOE_ERR_INVALID_ARG;
+    if (c->n_experts > 1024 || c->top_k + c->reroute > 32 || c->n_shared > 64)
+        return MOE_ERR_UNSUPPORTED;
     if (c->d_model % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    // capacity with re-routing or rank priority runs in one thread-block cluster
+    const bool policy = !ec && (c->reroute > 0 || c->priority == MOE_PRIORITY_RANK);
+    if (policy && (c->n_experts > 512 || c->T > 131072)) return MOE_ERR_UNSUPPORTED;
+    // expert choice keeps one expert's column of probabilities in shared memory
+    if (ec && c->T > 32768) return MOE_ERR_UNSUPPORTED;
     const long long T = c->T, E = c->n_experts, k = c->top_k, S = c->n_shared;
+    const long long nc = k + c->reroute;
     long long C = T;
     if (c->capacity_factor > 0.f) {
         C = (long long)ceil((double)T * (double)c->capacity_factor / (double)E);
         if (C > T) C = T;  // no expert can receive more than T tokens
     }
-    const long long R = std::min(T * k, E * C);
+    const long long R = (ec || c->pad_to_capacity) ? E * C : std::min(T * k, E * C);
     const long long F1 = c->act == MOE_SWIGLU ? 2LL * c->d_ff : c->d_ff;
     // row indices and TMA coordinates are 32-bit
-    if (T * k >= (1LL << 31) || R + S * T >= (1LL << 31) || E * F1 >= (1LL << 31) ||
+    if (T * nc >= (1LL << 31) || T * E >= (1LL << 31) || R + S * T >= (1LL << 31) ||
+        E * F1 >= (1LL << 31) ||
         E * (long long)c->d_model >= (1LL << 31))
         return MOE_ERR_UNSUPPORTED;
     s->T = c->T;
@@ -114,6 +134,10 @@ moe_status make_shape(const moe_config* c, Shape* s) {
     s->dtype = c->dtype;
     s->act = c->act;
     s->renorm = c->renorm_topk;
+    s->nc = (int)nc;
+    s->priority = c->priority;
+    s->pad = ec ? 0 : c->pad_to_capacity;
+    s->routing = c->routing;
     s->w_imp = c->importance_weight;
     s->esize = c->dtype == MOE_BF16 ? 2 : 4;
     return MOE_OK;
@@ -142,6 +166,10 @@ T* at(void* ws, size_t off) {
         if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
     } while (0)
 
+// Re-routing or rank priority: the cluster capacity kernel (policy.cu);
+// otherwise the plain token-order dropping kernels (capacity.cu).
+bool uses_policy(const Shape& s) { return s.nc > s.k || s.priority != MOE_PRIORITY_TOKEN; }
+
 // -------------------------------------------------------------- stage bodies
 // aux: if non-NULL ([3E] f, P, importance followed by out3 at aux_out3), the
 // selection kernel also counts the capacity histogram and the statistics.
@@ -166,7 +194,8 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x
     if (aux_out3) {
         // bf16: the up GEMM (tcgen05) finalises the statistics later in the layer
         MOE_CUDA(launch_router_select_fused(s, logits, zn, noisy ? noise : nullptr, bias, probs,
-                                            ids, w, status, at<int32_t>(ws, L.blk_hist),
+                                            ids, w, status,
+                                            uses_policy(s) ? nullptr : at<int32_t>(ws, L.blk_hist),
                                             at<void>(ws, L.aux_acc), aux_vecs, aux_vecs + s.E,
                                             aux_vecs + 2 * s.E, aux_out3,
                                             s.dtype == MOE_BF16, st));
@@ -182,10 +211,29 @@ moe_status dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const void
                          int32_t* slot, void* xp, int32_t* row_token, bool hist_ready,
                          void* y_zero, cudaStream_t st) {
     int* status = at<int>(ws, L.status);
-    MOE_CUDA(launch_capacity(s, ids, at<int32_t>(ws, L.blk_hist),
-                             at<unsigned int>(ws, L.cap_ticket), at<int32_t>(ws, L.blk_base),
-                             counts, kept, offsets, slot, row_token, status, hist_ready, st));
-    MOE_CUDA(launch_permute(s, x, slot, xp, y_zero, st));
+    // padded blocks: rows no token takes must read zero, so clear the block
+    // buffer first (the permute then fills the taken rows)
+    if (s.pad)
+        MOE_CUDA(cudaMemsetAsync(xp, 0, (size_t)s.R_max * s.d * s.esize, st));
+    if (uses_policy(s)) {
+        MOE_CUDA(launch_capacity_policy(s, ids, counts, kept, offsets, slot, row_token, status,
+                                        st));
+    } else {
+        MOE_CUDA(launch_capacity(s, ids, at<int32_t>(ws, L.blk_hist),
+                                 at<unsigned int>(ws, L.cap_ticket), at<int32_t>(ws, L.blk_base),
+                                 counts, kept, offsets, slot, row_token, status, hist_ready, st));
+    }
+    MOE_CUDA(launch_permute(s, x, slot, xp, y_zero, status, st));
+    return MOE_OK;
+}
+
+// Expert choice: select per expert, gather the chosen rows.
+moe_status ec_dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const void* x,
+                            const float* probs, int32_t* offsets, int32_t* row_token,
+                            float* row_w, int32_t* tok_row, void* xp, cudaStream_t st) {
+    MOE_CUDA(launch_expert_choice_select(s, probs, offsets, row_token, row_w, tok_row,
+                                         at<int>(ws, L.status), st));
+    MOE_CUDA(launch_gather_rows(s, s.E * s.C, x, row_token, xp, st));
     return MOE_OK;
 }
 
@@ -317,7 +365,9 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* W
     MOE_TRY(make_shape(cfg, &s));
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
     cudaStream_t st = (cudaStream_t)stream;
-    if (!topk_ids || !topk_w || !probs) return MOE_ERR_INVALID_ARG;
+    if (!probs) return MOE_ERR_INVALID_ARG;
+    if ((!topk_ids || !topk_w) && !(s.routing == MOE_EXPERT_CHOICE && !topk_ids && !topk_w))
+        return MOE_ERR_INVALID_ARG;
     if (from_scores) {
         if (!sel_scores) return MOE_ERR_INVALID_ARG;
         MOE_CUDA(launch_router_select(s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
@@ -343,6 +393,7 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int3
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
     if (!x || !topk_ids || !counts || !kept || !offsets || !slot || !xp || !row_token)
         return MOE_ERR_INVALID_ARG;
+    if (s.routing == MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_UNSUPPORTED;
     return dispatch_impl(s, L, ws, x, topk_ids, counts, kept, offsets, slot, xp, row_token,
                          false, nullptr, (cudaStream_t)stream);
@@ -373,6 +424,7 @@ MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int3
     MOE_TRY(make_shape(cfg, &s));
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
     if (!yp || !slot || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+    if (s.routing == MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
     if (s.S > 0 && !ys) return MOE_ERR_INVALID_ARG;
     if (!aligned16(yp) || !aligned16(y) || (ys && !aligned16(ys))) return MOE_ERR_UNSUPPORTED;
     MOE_CUDA(launch_combine(s, yp, slot, topk_w, s.S ? ys : nullptr, y, at<int>(ws, L.status),
@@ -436,21 +488,87 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
     void* ys = at<void>(ws, L.ys);
     float* av = aux_vecs ? aux_vecs : at<float>(ws, L.aux_vecs);
     float* o3 = out3 ? out3 : at<float>(ws, L.out3);
+    if (s.routing == MOE_EXPERT_CHOICE) {
+        if (topk_ids || topk_w || counts || aux_vecs || out3) return MOE_ERR_INVALID_ARG;
+        int32_t* tok_row = at<int32_t>(ws, L.tok_row);
+        float* row_w = at<float>(ws, L.row_w);
+        MOE_TRY(route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
+                           nullptr, nullptr, nullptr, nullptr, nullptr, st));
+        MOE_TRY(ec_dispatch_impl(s, L, ws, x, probs, offsets, row_token, row_w, tok_row, xp, st));
+        MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, nullptr, nullptr,
+                         nullptr, nullptr, nullptr, st));
+        MOE_CUDA(launch_expert_choice_combine(s, yp, tok_row, probs, s.S ? ys : nullptr, y, st));
+        return MOE_OK;
+    }
     // route + capacity histogram + statistics, then scan/slots, permute,
     // expert GEMMs, combine
     MOE_TRY(route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
                        nullptr, ids, w, av, o3, st));
     // top-1 without shared experts: each token has at most one expert row, so the
-    // down GEMM writes y itself (dropped tokens are zeroed by the slot kernel)
-    const bool scatter = s.k == 1 && s.S == 0 && s.dtype == MOE_BF16;
-    MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token, true,
-                          scatter ? y : nullptr, st));
+    // down GEMM writes y itself (dropped tokens are zeroed by the slot kernel).
+    // Not with re-route candidates (a token's gate depends on which candidate
+    // is kept) or padding (padding rows belong to no token).
+    const bool scatter = s.k == 1 && s.nc == 1 && !s.pad && s.S == 0 && s.dtype == MOE_BF16;
+    MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token,
+                          !uses_policy(s), scatter ? y : nullptr, st));
     MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys,
                      scatter ? row_token : nullptr, scatter ? w : nullptr,
                      scatter ? y : nullptr, s.dtype == MOE_BF16 ? av : nullptr,
                      s.dtype == MOE_BF16 ? o3 : nullptr, st));
     if (!scatter)
         MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_expert_choice_dispatch(const moe_config* cfg, const void* x,
+                                              const float* probs, int32_t* offsets,
+                                              int32_t* row_token, float* row_w,
+                                              int32_t* tok_row, void* xp, void* ws,
+                                              size_t ws_bytes, moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    if (s.routing != MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+    if (!x || !probs || !offsets || !row_token || !row_w || !tok_row || !xp)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_UNSUPPORTED;
+    return ec_dispatch_impl(s, L, ws, x, probs, offsets, row_token, row_w, tok_row, xp,
+                            (cudaStream_t)stream);
+}
+
+MOE_API moe_status moe_expert_choice_combine(const moe_config* cfg, const void* yp,
+                                             const int32_t* tok_row, const float* probs,
+                                             const void* ys, void* y, void* ws, size_t ws_bytes,
+                                             moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    if (s.routing != MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+    if (!yp || !tok_row || !probs || !y) return MOE_ERR_INVALID_ARG;
+    if (s.S > 0 && !ys) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(yp) || !aligned16(y) || (ys && !aligned16(ys))) return MOE_ERR_UNSUPPORTED;
+    MOE_CUDA(launch_expert_choice_combine(s, yp, tok_row, probs, s.S ? ys : nullptr, y,
+                                          (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_seq_aux_stats(const moe_config* cfg, const float* probs,
+                                     const int32_t* topk_ids, const int32_t* seq_offsets,
+                                     int32_t n_seq, float* f_seq, float* P_seq, float* aux_seq,
+                                     float* aux_mean, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream) {
+    Shape s;
+    WsLayout L;
+    MOE_TRY(make_shape(cfg, &s));
+    MOE_TRY(check_ws(s, ws, ws_bytes, &L));
+    if (!probs || !topk_ids || !seq_offsets || !aux_seq || !aux_mean || n_seq < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (n_seq > (1 << 30) || (long long)n_seq * s.E >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    MOE_CUDA(launch_seq_aux(s, probs, topk_ids, seq_offsets, n_seq, f_seq, P_seq, aux_seq,
+                            aux_mean, at<unsigned int>(ws, L.seq_ticket), at<int>(ws, L.status),
+                            (cudaStream_t)stream));
     return MOE_OK;
 }
 

@@ -15,13 +15,27 @@ namespace moe {
 // ---------------------------------------------------------------- status word
 // Bits OR-ed by kernels into the first int of the workspace.
 enum : int { DEV_TIMEOUT = 1, DEV_NONFINITE = 2, DEV_BAD_ARG = 4 };
+// Bits above DEV_BAD_ARG name the check that set it (a row index out of
+// range, an expert id out of range, ...); moe_read_device_error reports
+// them all as MOE_ERR_DEVICE_ARG.
+enum : int {
+    DEV_SITE_PERMUTE_ROW = 1 << 8,
+    DEV_SITE_POLICY_ROW = 1 << 10,
+    DEV_SITE_POLICY_ID = 1 << 11,
+    DEV_SITE_POLICY_RANK = 1 << 12,
+    DEV_SITE_POLICY_SMEM = 1 << 13,
+};
 
 // ------------------------------------------------------------- shape helpers
 struct Shape {
     int T, d, E, k, F, S;
     int F1;       // rows of one expert's W1: 2F for SwiGLU, else F
     int C;        // capacity
-    int R_max;    // min(T k, E C): rows of xp / yp / row_token
+    int R_max;    // rows of xp / yp / row_token: min(T k, E C), or E C when padded / expert choice
+    int nc;       // candidates per token: k + reroute
+    int priority; // MOE_PRIORITY_TOKEN / MOE_PRIORITY_RANK
+    int pad;      // pad every expert's row block to C
+    int routing;  // MOE_TOKEN_CHOICE / MOE_EXPERT_CHOICE
     int dtype;    // MOE_F32 / MOE_BF16
     int act;
     int renorm;
@@ -37,14 +51,17 @@ struct WsLayout {
     size_t aux_acc;    // statistics accumulators (aux_acc_bytes(E, kAuxGroups))
     size_t blk_hist;   // [E][nblk] i32 capacity histogram counters
     size_t cap_ticket; // u32 ticket of the fused scan + slot kernel
+    size_t seq_ticket; // u32 ticket of the sequence-statistics kernel
     size_t zero_end;   // end of the zero-between-calls prefix
     size_t zn;         // [T,E] f32 noise logits x.Wnoise
     size_t wgT;        // [Nr,d] dtype: Wg^T (rows 0..E-1) and Wnoise^T (E..2E-1)
     size_t logits;     // [T,E] f32 (layer only)
     size_t probs;      // [T,E] f32 (layer only)
-    size_t ids;        // [T,k] i32 (layer only)
-    size_t w;          // [T,k] f32 (layer only)
-    size_t slot;       // [T,k] i32 (layer only)
+    size_t ids;        // [T,nc] i32 (layer only)
+    size_t w;          // [T,nc] f32 (layer only)
+    size_t slot;       // [T,nc] i32 (layer only)
+    size_t tok_row;    // [T,E] i32 (expert choice, layer only)
+    size_t row_w;      // [R_max] f32 (expert choice, layer only)
     size_t counts;     // [E] i32 (layer only)
     size_t kept;       // [E] i32 (layer only)
     size_t offsets;    // [E+1] i32 (layer only)
@@ -104,8 +121,27 @@ cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_his
                             int* status, bool hist_ready, cudaStream_t st);
 // y_zero (top-1 layers whose combine is done by the down GEMM): the output row
 // of a token whose only assignment was dropped is zeroed here.
+// Capacity with re-routing and/or rank priority: one thread-block cluster
+// (see policy.cu). ids [T,nc]; slot [T,nc]; offsets e*C when s.pad.
+cudaError_t launch_capacity_policy(const Shape& s, const int32_t* ids, int32_t* counts,
+                                   int32_t* kept, int32_t* offsets, int32_t* slot,
+                                   int32_t* row_token, int* status, cudaStream_t st);
+// Expert choice (expert_choice.cu)
+cudaError_t launch_expert_choice_select(const Shape& s, const float* probs, int32_t* offsets,
+                                        int32_t* row_token, float* row_w, int32_t* tok_row,
+                                        int* status, cudaStream_t st);
+cudaError_t launch_gather_rows(const Shape& s, int rows, const void* x, const int32_t* row_token,
+                               void* xp, cudaStream_t st);
+cudaError_t launch_expert_choice_combine(const Shape& s, const void* yp, const int32_t* tok_row,
+                                         const float* probs, const void* ys, void* y,
+                                         cudaStream_t st);
+// Sequence-level statistics (seq_stats.cu)
+cudaError_t launch_seq_aux(const Shape& s, const float* probs, const int32_t* ids,
+                           const int32_t* seq_offsets, int n_seq, float* f_seq, float* P_seq,
+                           float* aux_seq, float* aux_mean, unsigned int* ticket, int* status,
+                           cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
-                           void* y_zero, cudaStream_t st);
+                           void* y_zero, int* status, cudaStream_t st);
 
 // Grouped expert GEMMs. Up: h = act(A W1^T); down: out = h W2^T.
 struct GroupedGemm {

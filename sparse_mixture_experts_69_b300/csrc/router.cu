@@ -112,7 +112,7 @@ cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const
 
 // ------------------------------------------------------------------ selection
 struct SelectArgs {
-    int T, E, k, renorm, from_scores;
+    int T, E, k, nc, renorm, from_scores;  // nc >= k candidates are written
     const float* logits;   // [T,E] z
     const float* zn;       // [T,E] x.Wnoise or NULL
     const float* noise;    // [T,E] or NULL
@@ -121,8 +121,8 @@ struct SelectArgs {
     const float* probs_in; // from_scores: [T,E]
     float* probs;          // out [T,E]
     float* sel;            // out [T,E] or NULL
-    int32_t* ids;          // out [T,k]
-    float* w;              // out [T,k]
+    int32_t* ids;          // out [T,nc]
+    float* w;              // out [T,nc]
     int* status;
 };
 
@@ -131,8 +131,9 @@ __device__ __forceinline__ float softplus_f(float u) {
 }
 
 // One token by one warp; lane l holds experts l, l+32, ... (EPL per lane).
-// On return pr[] holds this lane's probabilities, and lanes j < k hold the
-// j-th chosen expert (my_id) and its gate (my_w).
+// On return pr[] holds this lane's probabilities, and lanes j < nc hold the
+// j-th candidate (my_id) and its gate (my_w): p_j over the sum of p of the
+// first k candidates (renorm), else p_j.
 template <int EPL>
 __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (&pr)[EPL],
                                              int& my_id, float& my_w) {
@@ -188,11 +189,11 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (
     }
     if (__any_sync(0xffffffffu, nonfinite) && lane == 0) flag_status(a.status, DEV_NONFINITE);
 
-    // top-k: k rounds of a warp arg-max ordered by (score desc, index asc)
+    // top-nc: nc rounds of a warp arg-max ordered by (score desc, index asc)
     unsigned taken = 0;
     float my_p = 0.f, psum = 0.f;
     my_id = 0;
-    for (int j = 0; j < a.k; ++j) {
+    for (int j = 0; j < a.nc; ++j) {
         float bv = 0.f;
         int be = INT_MAX;
 #pragma unroll
@@ -220,16 +221,16 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (
             if (i == slot_i) mine = pr[i];
         if (lane == owner) taken |= 1u << slot_i;
         const float pj = __shfl_sync(0xffffffffu, mine, owner);
-        psum += pj;
+        if (j < a.k) psum += pj;
         if (lane == j) {
             my_id = be;
             my_p = pj;
         }
     }
     my_w = a.renorm ? my_p / psum : my_p;
-    if (lane < a.k) {
-        a.ids[(size_t)t * a.k + lane] = my_id;
-        a.w[(size_t)t * a.k + lane] = my_w;
+    if (lane < a.nc && a.ids) {
+        a.ids[(size_t)t * a.nc + lane] = my_id;
+        a.w[(size_t)t * a.nc + lane] = my_w;
     }
 }
 
@@ -252,7 +253,8 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
                                  const float* sel_in, const float* probs_in, int* status,
                                  cudaStream_t st) {
     SelectArgs a;
-    a.T = s.T; a.E = s.E; a.k = s.k; a.renorm = s.renorm; a.from_scores = from_scores;
+    a.T = s.T; a.E = s.E; a.k = s.k; a.nc = s.nc; a.renorm = s.renorm;
+    a.from_scores = from_scores;
     a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
     a.sel_in = sel_in; a.probs_in = probs_in;
     a.probs = probs; a.sel = sel; a.ids = ids; a.w = w; a.status = status;
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(512) router_select_fused_kernel(SelectArgs a, 
         if (lane < a.k) {
             atomicAdd(&sI[id], to_fix(w));
             atomicAdd(&sC[id], 1u);
-            atomicAdd(&blk_hist[(size_t)id * nblk_cap + t / kCapBlockTokens], 1);
+            if (blk_hist) atomicAdd(&blk_hist[(size_t)id * nblk_cap + t / kCapBlockTokens], 1);
         }
     }
 #pragma unroll
@@ -326,7 +328,7 @@ cudaError_t launch_router_select_fused(const Shape& s, const float* logits, cons
                                        void* acc_mem, float* f, float* P, float* I, float* out3,
                                        bool defer_final, cudaStream_t st) {
     SelectArgs a;
-    a.T = s.T; a.E = s.E; a.k = s.k; a.renorm = s.renorm; a.from_scores = 0;
+    a.T = s.T; a.E = s.E; a.k = s.k; a.nc = s.nc; a.renorm = s.renorm; a.from_scores = 0;
     a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
     a.sel_in = nullptr; a.probs_in = nullptr;
     a.probs = probs; a.sel = nullptr; a.ids = ids; a.w = w; a.status = status;

@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_RELU, MOE_GELU, MOE_SWIGLU = 0, 1, 2
+MOE_TOKEN_CHOICE, MOE_EXPERT_CHOICE = 0, 1
+MOE_PRIORITY_TOKEN, MOE_PRIORITY_RANK = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_NONFINITE", 6: "MOE_ERR_TIMEOUT",
           7: "MOE_ERR_DEVICE_ARG"}
@@ -36,7 +38,9 @@ class moe_config(ctypes.Structure):
                 ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("renorm_topk", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
-                ("importance_weight", ctypes.c_float)]
+                ("importance_weight", ctypes.c_float), ("reroute", ctypes.c_int32),
+                ("priority", ctypes.c_int32), ("pad_to_capacity", ctypes.c_int32),
+                ("routing", ctypes.c_int32)]
 
 
 @dataclass
@@ -53,11 +57,21 @@ class Config:
     dtype: int = MOE_BF16
     act: int = MOE_SWIGLU
     importance_weight: float = 1.0
+    reroute: int = 0
+    priority: int = MOE_PRIORITY_TOKEN
+    pad_to_capacity: int = 0
+    routing: int = MOE_TOKEN_CHOICE
 
     def c(self) -> moe_config:
         return moe_config(self.T, self.d_model, self.n_experts, self.top_k, self.d_ff,
                           self.n_shared, self.capacity_factor, self.renorm_topk, self.dtype,
-                          self.act, self.importance_weight)
+                          self.act, self.importance_weight, self.reroute, self.priority,
+                          self.pad_to_capacity, self.routing)
+
+    @property
+    def n_cand(self) -> int:
+        """Candidates per token: top_k + reroute."""
+        return self.top_k + self.reroute
 
     @property
     def torch_dtype(self):
@@ -86,6 +100,10 @@ _SIGS = {
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_P] * 16 + [_P, ctypes.c_size_t, _P]),
     "moe_read_device_error": (ctypes.c_int, [_CFG, _P, ctypes.c_size_t, _P]),
     "moe_aux_stats_noalloc": (ctypes.c_int, [_CFG] + [_P] * 7 + [_P]),
+    "moe_expert_choice_dispatch": (ctypes.c_int, [_CFG] + [_P] * 7 + [_P, ctypes.c_size_t, _P]),
+    "moe_expert_choice_combine": (ctypes.c_int, [_CFG] + [_P] * 5 + [_P, ctypes.c_size_t, _P]),
+    "moe_seq_aux_stats": (ctypes.c_int, [_CFG, _P, _P, _P, ctypes.c_int32] + [_P] * 4 +
+                          [_P, ctypes.c_size_t, _P]),
 }
 
 
@@ -206,6 +224,28 @@ def moe_layer_fwd(cfg: Config, x, Wg, Wnoise, noise, logit_offset, sel_bias, W1,
                                _p(logit_offset), _p(sel_bias), _p(W1), _p(W2), _p(W1s), _p(W2s),
                                _p(y), _p(topk_ids), _p(topk_w), _p(counts), _p(aux_vecs),
                                _p(out3), _p(ws), ws.numel(), _s(stream)), "moe_layer_fwd")
+
+
+def moe_expert_choice_dispatch(cfg: Config, x, probs, offsets, row_token, row_w, tok_row, xp,
+                               ws, stream=None):
+    _check(lib().moe_expert_choice_dispatch(ctypes.byref(cfg.c()), _p(x), _p(probs),
+                                            _p(offsets), _p(row_token), _p(row_w),
+                                            _p(tok_row), _p(xp), _p(ws), ws.numel(), _s(stream)),
+           "moe_expert_choice_dispatch")
+
+
+def moe_expert_choice_combine(cfg: Config, yp, tok_row, probs, ys, y, ws, stream=None):
+    _check(lib().moe_expert_choice_combine(ctypes.byref(cfg.c()), _p(yp), _p(tok_row),
+                                           _p(probs), _p(ys), _p(y), _p(ws), ws.numel(),
+                                           _s(stream)), "moe_expert_choice_combine")
+
+
+def moe_seq_aux_stats(cfg: Config, probs, topk_ids, seq_offsets, n_seq: int, f_seq, P_seq,
+                      aux_seq, aux_mean, ws, stream=None):
+    _check(lib().moe_seq_aux_stats(ctypes.byref(cfg.c()), _p(probs), _p(topk_ids),
+                                   _p(seq_offsets), int(n_seq), _p(f_seq), _p(P_seq),
+                                   _p(aux_seq), _p(aux_mean), _p(ws), ws.numel(), _s(stream)),
+           "moe_seq_aux_stats")
 
 
 def moe_read_device_error(cfg: Config, ws, stream=None) -> int:

@@ -67,11 +67,28 @@ def _cfg(**kw):
     (dict(capacity_factor=float("nan")), 1),
     (dict(d_model=60), 2), (dict(d_ff=100), 2), (dict(n_experts=2048, top_k=2), 2),
     (dict(top_k=33, n_experts=64), 2), (dict(n_shared=65), 2),
+    # overflow policies and expert choice
+    (dict(reroute=-1), 1), (dict(top_k=2, reroute=7), 1), (dict(priority=2), 1),
+    (dict(pad_to_capacity=2), 1), (dict(routing=2), 1),
+    (dict(routing=1, reroute=1), 1), (dict(routing=1, priority=1), 1),
+    (dict(n_experts=64, top_k=8, reroute=25), 2),
+    (dict(n_experts=600, reroute=1), 2), (dict(T=131073, priority=1), 2),
+    (dict(T=32769, routing=1), 2),
 ])
 def test_invalid_configs_rejected(lib, kw, status):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_workspace_size(_cfg(**kw))
     assert ei.value.status == status
+
+
+def test_rows_bound_of_padding_and_expert_choice(lib):
+    # dropping: min(T k, E C); padded or expert choice: E C
+    assert moe.moe_capacity(_cfg(capacity_factor=0.5)) == (4, 32)
+    assert moe.moe_capacity(_cfg(capacity_factor=4.0)) == (32, 128)
+    assert moe.moe_capacity(_cfg(capacity_factor=4.0, pad_to_capacity=1)) == (32, 256)
+    assert moe.moe_capacity(_cfg(capacity_factor=2.0, routing=moe.MOE_EXPERT_CHOICE)) == (16, 128)
+    # candidates widen the per-token arrays in the workspace
+    assert moe.moe_workspace_size(_cfg(reroute=2)) > moe.moe_workspace_size(_cfg())
 
 
 def test_workspace_grows_with_the_problem(lib):
@@ -122,3 +139,31 @@ def test_host_validation_before_any_launch(lib):
                            None, None, None, A, big, None) == 1
     assert L.moe_bias_update(c, None, A, 1e-3, None) == 1
     assert L.moe_bias_update(c, A, A, float("inf"), None) == 1
+
+
+def test_host_validation_of_the_next_entry_points(lib):
+    L = moe.lib()
+    A = 1 << 20
+    ec = _cfg(routing=moe.MOE_EXPERT_CHOICE, capacity_factor=2.0)
+    big = moe.moe_workspace_size(ec)
+    c = ctypes.byref(ec.c())
+    # token-choice calls refuse an expert-choice config and vice versa
+    assert L.moe_dispatch(c, A, A, A, A, A, A, A, A, A, big, None) == 1
+    assert L.moe_combine(c, A, A, A, None, A, A, big, None) == 1
+    tc = _cfg()
+    tbig = moe.moe_workspace_size(tc)
+    assert L.moe_expert_choice_dispatch(ctypes.byref(tc.c()), A, A, A, A, A, A, A, A, tbig,
+                                        None) == 1
+    assert L.moe_expert_choice_combine(ctypes.byref(tc.c()), A, A, A, None, A, A, tbig,
+                                       None) == 1
+    # missing outputs, misaligned rows
+    assert L.moe_expert_choice_dispatch(c, A, A, A, None, A, A, A, A, big, None) == 1
+    assert L.moe_expert_choice_dispatch(c, A + 4, A, A, A, A, A, A, A, big, None) == 2
+    # the layer refuses token-choice outputs under expert choice
+    assert L.moe_layer_fwd(c, A, A, None, None, None, None, A, A, None, None, A, A, None,
+                           None, None, None, A, big, None) == 1
+    # sequence statistics: need at least one sequence and the outputs
+    assert L.moe_seq_aux_stats(ctypes.byref(tc.c()), A, A, A, 0, None, None, A, A, A, tbig,
+                               None) == 1
+    assert L.moe_seq_aux_stats(ctypes.byref(tc.c()), A, A, A, 4, None, None, None, A, A, tbig,
+                               None) == 1
