@@ -292,8 +292,9 @@ MOE_API moe_status moe_expert_choice_combine(const moe_config* cfg, const void* 
  *   aux_mean   = mean of aux_seq over the non-empty sequences (0 if none)
  * probs [T,E] float32, topk_ids [T,n_cand] (first k columns used),
  * seq_offsets [n_seq+1] int32 device, non-decreasing from 0 to T (device
- * check: MOE_ERR_DEVICE_ARG); f_seq, P_seq [n_seq,E] float32 or NULL;
- * aux_seq [n_seq] float32; aux_mean [1] float32. Deterministic. */
+ * check: MOE_ERR_DEVICE_ARG); 1 <= n_seq <= T + 1 (MOE_ERR_UNSUPPORTED
+ * above); f_seq, P_seq [n_seq,E] float32 or NULL; aux_seq [n_seq] float32;
+ * aux_mean [1] float32. Deterministic (integer fixed-point sums). */
 MOE_API moe_status moe_seq_aux_stats(const moe_config* cfg, const float* probs,
                                      const int32_t* topk_ids, const int32_t* seq_offsets,
                                      int32_t n_seq, float* f_seq, float* P_seq, float* aux_seq,

@@ -60,6 +60,7 @@ WsLayout ws_layout(const Shape& s) {
     L.slot = take(T * nc * 4);
     L.tok_row = take(ec ? T * E * 4 : 0);
     L.row_w = take(ec ? R * 4 : 0);
+    L.seq_acc = take(seq_aux_scratch_bytes((int)E, (int)T + 1));
     L.counts = take(E * 4);
     L.kept = take(E * 4);
     L.offsets = take((E + 1) * 4);
@@ -565,10 +566,10 @@ MOE_API moe_status moe_seq_aux_stats(const moe_config* cfg, const float* probs,
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
     if (!probs || !topk_ids || !seq_offsets || !aux_seq || !aux_mean || n_seq < 1)
         return MOE_ERR_INVALID_ARG;
-    if (n_seq > (1 << 30) || (long long)n_seq * s.E >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    if (n_seq > s.T + 1) return MOE_ERR_UNSUPPORTED;  // the workspace holds T + 1 sequences
     MOE_CUDA(launch_seq_aux(s, probs, topk_ids, seq_offsets, n_seq, f_seq, P_seq, aux_seq,
-                            aux_mean, at<unsigned int>(ws, L.seq_ticket), at<int>(ws, L.status),
-                            (cudaStream_t)stream));
+                            aux_mean, at<void>(ws, L.seq_acc), at<unsigned int>(ws, L.seq_ticket),
+                            at<int>(ws, L.status), (cudaStream_t)stream));
     return MOE_OK;
 }
 

@@ -62,6 +62,7 @@ struct WsLayout {
     size_t slot;       // [T,nc] i32 (layer only)
     size_t tok_row;    // [T,E] i32 (expert choice, layer only)
     size_t row_w;      // [R_max] f32 (expert choice, layer only)
+    size_t seq_acc;    // sequence statistics accumulators for up to T + 1 sequences
     size_t counts;     // [E] i32 (layer only)
     size_t kept;       // [E] i32 (layer only)
     size_t offsets;    // [E+1] i32 (layer only)
@@ -136,10 +137,12 @@ cudaError_t launch_expert_choice_combine(const Shape& s, const void* yp, const i
                                          const float* probs, const void* ys, void* y,
                                          cudaStream_t st);
 // Sequence-level statistics (seq_stats.cu)
+// scratch: seq_aux_scratch_bytes(E, n_seq) bytes of workspace, cleared on the stream
+size_t seq_aux_scratch_bytes(int E, int n_seq);
 cudaError_t launch_seq_aux(const Shape& s, const float* probs, const int32_t* ids,
                            const int32_t* seq_offsets, int n_seq, float* f_seq, float* P_seq,
-                           float* aux_seq, float* aux_mean, unsigned int* ticket, int* status,
-                           cudaStream_t st);
+                           float* aux_seq, float* aux_mean, void* scratch, unsigned int* ticket,
+                           int* status, cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
                            void* y_zero, int* status, cudaStream_t st);
 

@@ -26,18 +26,25 @@
 // there, in a handful of passes on the workloads measured (the oracle's pins
 // check this algorithm against the sequential walk).
 //
-// One CTA of 1024 threads runs it, one token per thread in chunks of 1024
-// in token order. A pass ranks every try per expert in priority order: per
-// round (one in token order, one per candidate rank in rank order) and chunk,
-// rank = tries of the expert in earlier rounds and chunks + tries by lower
-// lanes and warps of the chunk (lane bitmasks per warp and expert). A
-// token's tries are recomputed from tau wherever they are needed, so shared
-// memory holds only per-expert arrays and the masks.
+// One thread-block cluster of 8 CTAs x 1024 threads runs it; CTA c owns a
+// contiguous block of tokens. Per pass and per round (one round in token
+// order, one per candidate rank in rank order) each CTA counts its tries per
+// expert, reads the other CTAs' counts through distributed shared memory,
+// and ranks its own tries from per-warp lane bitmasks (chunks of 1024
+// tokens). The CTA whose try gets rank C-1 writes tau_e into every CTA's
+// shared memory. The decision to stop is posted by every CTA into CTA 0 and
+// read back from there, so all CTAs leave the loop together. Every barrier
+// between CTAs is a cluster barrier, preceded by a CTA barrier.
+#include <cooperative_groups.h>
+
 #include "moe_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 
 namespace {
+constexpr int kPolCtas = 8;
 constexpr int kPolThreads = 1024;
 constexpr int kPolWarps = kPolThreads / 32;
 constexpr int kPolMaxPasses = 4096;
@@ -59,11 +66,15 @@ __device__ __forceinline__ unsigned lanemask_lt_pol() {
     return m;
 }
 
+__host__ __device__ constexpr int policy_tokens_per_cta(int T) { return (T + kPolCtas - 1) / kPolCtas; }
+
 // Shared-memory layout of cap_policy_kernel, in 4-byte words: tau, tau_new,
-// total, first [E] each, offs [E+1], then the lane masks [warps][E]. The
-// host sizes the allocation and the kernel checks it with this one function.
-__host__ __device__ constexpr size_t policy_smem_words(int E) {
-    return (size_t)5 * E + 1 + (size_t)kPolWarps * E;
+// cnt[2], base, run, total, first ([E] each, cnt two of them), offs [E+1],
+// the lane masks [warps][E], then the tries of each owned token [tokens per
+// CTA]. The host sizes the allocation and the kernel checks it with this one
+// function.
+__host__ __device__ constexpr size_t policy_smem_words(int E, int T) {
+    return (size_t)9 * E + 1 + (size_t)kPolWarps * E + (size_t)policy_tokens_per_cta(T);
 }
 
 __device__ __forceinline__ unsigned dynamic_smem_bytes() {
@@ -76,19 +87,10 @@ __device__ __forceinline__ int visit_pos(const PolArgs& a, int t, int j) {
     return a.priority == MOE_PRIORITY_TOKEN ? t * a.nc + j : j * a.T + t;
 }
 
-// Bit j set: token t tries candidate j under the fill positions tau (in
-// rank order until k tries succeed). Out-of-range ids are never tried.
-__device__ __forceinline__ unsigned tries_of(const PolArgs& a, const int* tau, int t) {
-    const int32_t* row = a.ids + (size_t)t * a.nc;
-    int need = a.k;
-    unsigned m = 0;
-    for (int j = 0; j < a.nc && need > 0; ++j) {
-        const int e = row[j];
-        if (e < 0 || e >= a.E) continue;
-        m |= 1u << j;
-        if (visit_pos(a, t, j) <= tau[e]) --need;
-    }
-    return m;
+// CTA barrier (warps converged), then the cluster barrier
+__device__ __forceinline__ void cluster_barrier(cg::cluster_group& cl) {
+    __syncthreads();
+    cl.sync();
 }
 }  // namespace
 
@@ -96,29 +98,42 @@ __global__ void __launch_bounds__(kPolThreads, 1) cap_policy_kernel(PolArgs a) {
     pdl_trigger();
     pdl_wait();
     const int T = a.T, E = a.E, nc = a.nc, C = a.C;
-    // the allocation must hold the layout below (uniform exit before any barrier)
-    if (dynamic_smem_bytes() < sizeof(int) * policy_smem_words(E)) {
-        if (threadIdx.x == 0) flag_status(a.status, DEV_BAD_ARG | DEV_SITE_POLICY_SMEM);
+    // every CTA of the cluster sees the same size, so this exit is uniform
+    if (dynamic_smem_bytes() < sizeof(int) * policy_smem_words(E, T)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0)
+            flag_status(a.status, DEV_BAD_ARG | DEV_SITE_POLICY_SMEM);
         return;
     }
+    cg::cluster_group cl = cg::this_cluster();
+    const int c = (int)cl.block_rank();
+    const int Tc = policy_tokens_per_cta(T);
+    const int t_lo = min(T, c * Tc), t_hi = min(T, t_lo + Tc);
+    const int nown = t_hi - t_lo;
     extern __shared__ int sm[];
-    int* tau = sm;             // [E] fill positions of this pass
-    int* tau_new = tau + E;    // [E] fill positions found in this pass
-    int* total = tau_new + E;  // [E] tries of e in earlier rounds and chunks of this pass
-    int* first = total + E;    // [E] tries of the first pass = top-k choices
-    int* offs = first + E;     // [E+1]
+    int* tau = sm;               // [E] fill positions of this pass
+    int* tau_new = tau + E;      // [E] written by whichever CTA holds the C-th try
+    int* cnt = tau_new + E;      // [2][E] this CTA's tries per expert (alternating rounds)
+    int* base = cnt + 2 * E;     // [E] tries at e before this CTA's, in this round
+    int* run = base + E;         // [E] this CTA's tries at e in earlier chunks
+    int* total = run + E;        // [E] tries at e in earlier rounds of this pass
+    int* first = total + E;      // [E] tries of the first pass = top-k choices
+    int* offs = first + E;       // [E+1]
     unsigned* mask = reinterpret_cast<unsigned*>(offs + E + 1);  // [warps][E]
+    unsigned* att = mask + kPolWarps * E;                        // [Tc] tries of each token
+    __shared__ int s_flag[kPolCtas];  // CTA 0's copy: each CTA's "still changing" flag
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned lt = lanemask_lt_pol();
     const int never = T * nc;  // later than every visit position
     for (int e = tid; e < E; e += kPolThreads) {
         tau[e] = never;
         tau_new[e] = never;
+        cnt[e] = 0;
+        cnt[E + e] = 0;
     }
     // ids must be in range and distinct per token; a bad one is never tried
     bool bad = false;
-    for (int t = tid; t < T; t += kPolThreads) {
-        const int32_t* row = a.ids + (size_t)t * nc;
+    for (int tl = tid; tl < nown; tl += kPolThreads) {
+        const int32_t* row = a.ids + (size_t)(t_lo + tl) * nc;
         for (int j = 0; j < nc; ++j) {
             const int e = row[j];
             if (e < 0 || e >= E) bad = true;
@@ -127,56 +142,102 @@ __global__ void __launch_bounds__(kPolThreads, 1) cap_policy_kernel(PolArgs a) {
         }
     }
     if (bad) flag_status(a.status, DEV_BAD_ARG | DEV_SITE_POLICY_ID);
-    __syncthreads();
+    cluster_barrier(cl);  // every CTA's tau_new is initialised before anyone writes into it
 
     const int rounds = a.priority == MOE_PRIORITY_TOKEN ? 1 : nc;
     bool settled = false;
     for (int pass = 0; pass < kPolMaxPasses; ++pass) {
+        // each owned token's tries under the current fill positions
+        for (int tl = tid; tl < nown; tl += kPolThreads) {
+            const int t = t_lo + tl;
+            const int32_t* row = a.ids + (size_t)t * nc;
+            int need = a.k;
+            unsigned m = 0;
+            for (int j = 0; j < nc && need > 0; ++j) {
+                const int e = row[j];
+                if (e < 0 || e >= E) continue;
+                m |= 1u << j;
+                if (visit_pos(a, t, j) <= tau[e]) --need;
+            }
+            att[tl] = m;
+        }
         for (int e = tid; e < E; e += kPolThreads) total[e] = 0;
         __syncthreads();
         for (int rd = 0; rd < rounds; ++rd) {
             const unsigned round_bits = rounds == 1 ? 0xffffffffu : (1u << rd);
-            for (int c0 = 0; c0 < T; c0 += kPolThreads) {
+            int* buf = cnt + (rd & 1) * E;
+            for (int e = tid; e < E; e += kPolThreads) buf[e] = 0;
+            __syncthreads();
+            for (int tl = tid; tl < nown; tl += kPolThreads) {
+                const int32_t* row = a.ids + (size_t)(t_lo + tl) * nc;
+                for (unsigned m = att[tl] & round_bits; m; m &= m - 1)
+                    atomicAdd(&buf[row[__ffs(m) - 1]], 1);
+            }
+            cluster_barrier(cl);  // (A) every CTA's counts of this round are complete
+            for (int e = tid; e < E; e += kPolThreads) {
+                int before = 0, all = 0;
+                for (int r = 0; r < kPolCtas; ++r) {
+                    const int v = *cl.map_shared_rank(buf + e, r);
+                    all += v;
+                    if (r < c) before += v;
+                }
+                base[e] = total[e] + before;
+                total[e] += all;
+                run[e] = 0;
+            }
+            __syncthreads();
+            for (int cs = 0; cs < nown; cs += kPolThreads) {
                 for (int i = tid; i < kPolWarps * E; i += kPolThreads) mask[i] = 0;
                 __syncthreads();
-                const int t = c0 + tid;
-                const unsigned mine = t < T ? tries_of(a, tau, t) & round_bits : 0u;
-                const int32_t* row = a.ids + (size_t)(t < T ? t : 0) * nc;
+                const int tl = cs + tid;
+                const int t = t_lo + (tl < nown ? tl : 0);
+                const unsigned mine = tl < nown ? att[tl] & round_bits : 0u;
+                const int32_t* row = a.ids + (size_t)t * nc;
                 for (unsigned m = mine; m; m &= m - 1)
                     atomicOr(&mask[warp * E + row[__ffs(m) - 1]], 1u << lane);
                 __syncthreads();
                 for (unsigned m = mine; m; m &= m - 1) {
                     const int j = __ffs(m) - 1;
                     const int e = row[j];
-                    int r = total[e] + __popc(mask[warp * E + e] & lt);
+                    int r = base[e] + run[e] + __popc(mask[warp * E + e] & lt);
                     for (int w = 0; w < warp; ++w) r += __popc(mask[w * E + e]);
                     a.slot[(size_t)t * nc + j] = r;
-                    if (r == C - 1) tau_new[e] = visit_pos(a, t, j);  // the one try with rank C-1
+                    if (r == C - 1) {  // the one try with rank C-1: publish the fill position
+                        const int v = visit_pos(a, t, j);
+                        for (int q = 0; q < kPolCtas; ++q) *cl.map_shared_rank(tau_new + e, q) = v;
+                    }
                 }
                 __syncthreads();
                 for (int e = tid; e < E; e += kPolThreads) {
                     int add = 0;
                     for (int w = 0; w < kPolWarps; ++w) add += __popc(mask[w * E + e]);
-                    total[e] += add;
+                    run[e] += add;
                 }
                 __syncthreads();
             }
         }
+        cluster_barrier(cl);  // (B) every fill position of this pass has landed everywhere
         if (pass == 0)
             for (int e = tid; e < E; e += kPolThreads) first[e] = total[e];
         int changed = 0;
         for (int e = tid; e < E; e += kPolThreads) changed |= tau_new[e] != tau[e];
-        if (!__syncthreads_or(changed)) {
+        changed = __syncthreads_or(changed);
+        if (tid == 0) *cl.map_shared_rank(s_flag + c, 0) = changed;
+        cluster_barrier(cl);  // (C) every CTA's flag is in CTA 0
+        int any = 0;
+        for (int r = 0; r < kPolCtas; ++r) any |= *cl.map_shared_rank(s_flag + r, 0);
+        if (!any) {
             settled = true;
             break;
         }
+        // nobody writes tau_new or s_flag again before barrier (A) of the next pass
         for (int e = tid; e < E; e += kPolThreads) {
             tau[e] = tau_new[e];
             tau_new[e] = never;
         }
         __syncthreads();
     }
-    if (!settled && tid == 0) flag_status(a.status, DEV_TIMEOUT);
+    if (!settled && c == 0 && tid == 0) flag_status(a.status, DEV_TIMEOUT);
 
     // rows: kept = min(tries, C), offsets = scan of kept (or e*C when padded)
     if (tid == 0) {
@@ -185,14 +246,17 @@ __global__ void __launch_bounds__(kPolThreads, 1) cap_policy_kernel(PolArgs a) {
             offs[e + 1] = a.pad ? (e + 1) * C : offs[e] + min(total[e], C);
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kPolThreads) {
-        a.counts[e] = first[e];
-        a.kept[e] = min(total[e], C);
-        a.offsets[e] = offs[e];
+    if (c == 0) {
+        for (int e = tid; e < E; e += kPolThreads) {
+            a.counts[e] = first[e];
+            a.kept[e] = min(total[e], C);
+            a.offsets[e] = offs[e];
+        }
+        if (tid == 0) a.offsets[E] = offs[E];
     }
-    if (tid == 0) a.offsets[E] = offs[E];
-    for (int t = tid; t < T; t += kPolThreads) {
-        const unsigned m = tries_of(a, tau, t);  // the tries of the last pass
+    for (int tl = tid; tl < nown; tl += kPolThreads) {
+        const int t = t_lo + tl;
+        const unsigned m = att[tl];
         for (int j = 0; j < nc; ++j) {
             const size_t ai = (size_t)t * nc + j;
             int out = -1;
@@ -212,6 +276,7 @@ __global__ void __launch_bounds__(kPolThreads, 1) cap_policy_kernel(PolArgs a) {
             a.slot[ai] = out;
         }
     }
+    cluster_barrier(cl);  // no CTA exits while another might still address its shared memory
 }
 
 cudaError_t launch_capacity_policy(const Shape& s, const int32_t* ids, int32_t* counts,
@@ -233,11 +298,25 @@ cudaError_t launch_capacity_policy(const Shape& s, const int32_t* ids, int32_t* 
     a.slot = slot;
     a.row_token = row_token;
     a.status = status;
-    const size_t smem = sizeof(int) * policy_smem_words(s.E);
+    const size_t smem = sizeof(int) * policy_smem_words(s.E, s.T);
     cudaError_t err = cudaFuncSetAttribute(cap_policy_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    return launch_k(cap_policy_kernel, dim3(1), dim3(kPolThreads), smem, st, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kPolCtas);
+    cfg.blockDim = dim3(kPolThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPolCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, cap_policy_kernel, a);
 }
 
 }  // namespace moe

@@ -7,72 +7,106 @@
 // expert / (T_q k), P = mean probability, aux_q = E sum_e f P, and the mean
 // of aux_q over the non-empty sequences.
 //
-// One CTA per sequence, 1024 threads. Counts are integer atomics in shared
-// memory. The probability sums give each thread a fixed set of tokens
-// (every 32nd) for one expert column, added in a fixed order, so the result
-// does not depend on scheduling. The last CTA to finish (ticket) averages
-// aux over the sequences in sequence order and resets the ticket.
-#include "moe_internal.cuh"
+// Two launches after the accumulators are cleared:
+//   1. seq_accumulate_kernel: each warp walks 32 consecutive tokens of the
+//      batch (so the whole batch is read once, by many CTAs) and sums the
+//      probabilities of each expert column while the tokens belong to one
+//      sequence, then adds the run to that sequence's accumulator. The sums
+//      are 32.32 fixed-point integers, so the totals do not depend on the
+//      order of the atomics; choice counts are integer atomics.
+//   2. seq_finalize_kernel: one CTA per sequence forms f, P and aux_q from its
+//      accumulators in a fixed order; the last CTA (ticket) averages aux over
+//      the sequences in sequence order and resets the ticket.
+#include "aux_common.cuh"
 
 namespace moe {
 
 namespace {
-constexpr int kSeqThreads = 1024;
-constexpr int kSeqRows = kSeqThreads / 32;
+constexpr int kSeqWarpTokens = 32;
+constexpr int kSeqAccThreads = 128;  // 4 warps: 128 tokens per CTA
+constexpr int kSeqFinThreads = 256;
 }  // namespace
 
-__global__ void __launch_bounds__(kSeqThreads) seq_aux_kernel(
+// Sequence of token t: the largest q with seq_offsets[q] <= t (offsets are
+// non-decreasing; empty sequences are skipped over).
+__device__ __forceinline__ int seq_of(const int32_t* seq_offsets, int n_seq, int t) {
+    int lo = 0, hi = n_seq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seq_offsets[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kSeqAccThreads) seq_accumulate_kernel(
     int T, int E, int k, int nc, const float* __restrict__ probs, const int32_t* __restrict__ ids,
-    const int32_t* __restrict__ seq_offsets, int n_seq, float* __restrict__ f_seq,
-    float* __restrict__ P_seq, float* __restrict__ aux_seq, float* __restrict__ aux_mean,
-    unsigned int* __restrict__ ticket, int* status) {
+    const int32_t* __restrict__ seq_offsets, int n_seq, unsigned long long* __restrict__ accP,
+    unsigned int* __restrict__ accC, int* status) {
     pdl_trigger();
     pdl_wait();
-    extern __shared__ int sm_seq[];
-    int* cnt = sm_seq;                                      // [E]
-    float* psum = reinterpret_cast<float*>(cnt + E);        // [E]
-    __shared__ float part[kSeqRows][33];
-    __shared__ float red[kSeqThreads / 32];
+    const int lane = threadIdx.x & 31;
+    // tokens outside [seq_offsets[0], seq_offsets[n_seq]) belong to no sequence
+    const int first = max(0, seq_offsets[0]), last = min(T, seq_offsets[n_seq]);
+    const int t0 = max(first, (blockIdx.x * (kSeqAccThreads / 32) + (threadIdx.x >> 5)) *
+                                  kSeqWarpTokens);
+    const int t1 = min(last, (blockIdx.x * (kSeqAccThreads / 32) + (threadIdx.x >> 5) + 1) *
+                                 kSeqWarpTokens);
+    if (t0 >= t1) return;
+    // choice counts: lane j < k of the token's row, token by token
+    bool bad = false;
+    {
+        int q = seq_of(seq_offsets, n_seq, t0);
+        for (int t = t0; t < t1; ++t) {
+            while (q + 1 < n_seq && seq_offsets[q + 1] <= t) ++q;
+            if (lane < k) {
+                const int e = ids[(size_t)t * nc + lane];
+                if (e >= 0 && e < E) atomicAdd(&accC[(size_t)q * E + e], 1u);
+                else bad = true;
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(status, DEV_BAD_ARG);
+    // probability sums, 32 experts (one per lane) at a time
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        int q = seq_of(seq_offsets, n_seq, t0);
+        unsigned long long run = 0;
+        for (int t = t0; t < t1; ++t) {
+            if (q + 1 < n_seq && seq_offsets[q + 1] <= t) {  // the run's sequence ended
+                if (e < E && run) atomicAdd(&accP[(size_t)q * E + e], run);
+                run = 0;
+                while (q + 1 < n_seq && seq_offsets[q + 1] <= t) ++q;
+            }
+            if (e < E) run += to_fix(__ldg(&probs[(size_t)t * E + e]));
+        }
+        if (e < E && run) atomicAdd(&accP[(size_t)q * E + e], run);
+    }
+}
+
+__global__ void __launch_bounds__(kSeqFinThreads) seq_finalize_kernel(
+    int T, int E, int k, const int32_t* __restrict__ seq_offsets, int n_seq,
+    const unsigned long long* __restrict__ accP, const unsigned int* __restrict__ accC,
+    float* __restrict__ f_seq, float* __restrict__ P_seq, float* __restrict__ aux_seq,
+    float* __restrict__ aux_mean, unsigned int* __restrict__ ticket, int* status) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float red[kSeqFinThreads / 32];
     __shared__ int s_last;
     const int q = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, row = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int t0 = seq_offsets[q], t1 = seq_offsets[q + 1];
     if (t0 < 0 || t1 < t0 || t1 > T) {
         if (tid == 0) flag_status(status, DEV_BAD_ARG);
         t0 = t1 = 0;  // treated as empty
     }
     const int Tq = t1 - t0;
-    for (int e = tid; e < E; e += kSeqThreads) cnt[e] = 0;
-    __syncthreads();
-    bool bad = false;
-    for (int i = tid; i < Tq * k; i += kSeqThreads) {
-        const int e = ids[(size_t)(t0 + i / k) * nc + i % k];
-        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-        else bad = true;
-    }
-    if (bad) flag_status(status, DEV_BAD_ARG);
-    // probability column sums, 32 experts at a time
-    for (int e0 = 0; e0 < E; e0 += 32) {
-        const int e = e0 + lane;
-        float acc = 0.f;
-        if (e < E)
-            for (int t = t0 + row; t < t1; t += kSeqRows) acc += __ldg(&probs[(size_t)t * E + e]);
-        part[row][lane] = acc;
-        __syncthreads();
-        if (row == 0 && e < E) {
-            float sum = 0.f;
-            for (int r = 0; r < kSeqRows; ++r) sum += part[r][lane];
-            psum[e] = sum;
-        }
-        __syncthreads();
-    }
-    // f, P and the per-expert products, reduced in a fixed tree
     float prod = 0.f;
-    for (int e = tid; e < E; e += kSeqThreads) {
+    for (int e = tid; e < E; e += kSeqFinThreads) {
         float f = 0.f, P = 0.f;
         if (Tq > 0) {
-            f = (float)cnt[e] / ((float)Tq * (float)k);
-            P = psum[e] / (float)Tq;
+            f = (float)accC[(size_t)q * E + e] / ((float)Tq * (float)k);
+            P = (float)((double)accP[(size_t)q * E + e] * (1.0 / 4294967296.0)) / (float)Tq;
         }
         if (f_seq) f_seq[(size_t)q * E + e] = f;
         if (P_seq) P_seq[(size_t)q * E + e] = P;
@@ -80,11 +114,11 @@ __global__ void __launch_bounds__(kSeqThreads) seq_aux_kernel(
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) prod += __shfl_xor_sync(0xffffffffu, prod, o);
-    if (lane == 0) red[row] = prod;
+    if (lane == 0) red[warp] = prod;
     __syncthreads();
     if (tid == 0) {
         float a = 0.f;
-        for (int r = 0; r < kSeqThreads / 32; ++r) a += red[r];
+        for (int r = 0; r < kSeqFinThreads / 32; ++r) a += red[r];
         aux_seq[q] = Tq > 0 ? (float)E * a : 0.f;
         __threadfence();
         s_last = atomicAdd(ticket, 1u) == (unsigned)(n_seq - 1);
@@ -95,7 +129,7 @@ __global__ void __launch_bounds__(kSeqThreads) seq_aux_kernel(
         float total = 0.f;
         int nonempty = 0;
         for (int i = 0; i < n_seq; ++i) {
-            int a0 = seq_offsets[i], a1 = seq_offsets[i + 1];
+            const int a0 = seq_offsets[i], a1 = seq_offsets[i + 1];
             if (a0 < 0 || a1 < a0 || a1 > T) continue;
             if (a1 > a0) {
                 total += __ldcg(&aux_seq[i]);
@@ -107,14 +141,26 @@ __global__ void __launch_bounds__(kSeqThreads) seq_aux_kernel(
     }
 }
 
+size_t seq_aux_scratch_bytes(int E, int n_seq) {
+    return (size_t)n_seq * E * (sizeof(unsigned long long) + sizeof(unsigned int));
+}
+
 cudaError_t launch_seq_aux(const Shape& s, const float* probs, const int32_t* ids,
                            const int32_t* seq_offsets, int n_seq, float* f_seq, float* P_seq,
-                           float* aux_seq, float* aux_mean, unsigned int* ticket, int* status,
-                           cudaStream_t st) {
-    const size_t smem = (size_t)s.E * (sizeof(int) + sizeof(float));
-    return launch_k(seq_aux_kernel, dim3(n_seq), dim3(kSeqThreads), smem, st, s.T, s.E, s.k, s.nc,
-                    probs, ids, seq_offsets, n_seq, f_seq, P_seq, aux_seq, aux_mean, ticket,
-                    status);
+                           float* aux_seq, float* aux_mean, void* scratch, unsigned int* ticket,
+                           int* status, cudaStream_t st) {
+    unsigned long long* accP = static_cast<unsigned long long*>(scratch);
+    unsigned int* accC = reinterpret_cast<unsigned int*>(accP + (size_t)n_seq * s.E);
+    cudaError_t err = cudaMemsetAsync(scratch, 0, seq_aux_scratch_bytes(s.E, n_seq), st);
+    if (err != cudaSuccess) return err;
+    const int warps = (s.T + kSeqWarpTokens - 1) / kSeqWarpTokens;
+    const int per = kSeqAccThreads / 32;
+    err = launch_k(seq_accumulate_kernel, dim3((warps + per - 1) / per), dim3(kSeqAccThreads), 0,
+                   st, s.T, s.E, s.k, s.nc, probs, ids, seq_offsets, n_seq, accP, accC, status);
+    if (err != cudaSuccess) return err;
+    return launch_k(seq_finalize_kernel, dim3(n_seq), dim3(kSeqFinThreads), 0, st, s.T, s.E, s.k,
+                    seq_offsets, n_seq, (const unsigned long long*)accP,
+                    (const unsigned int*)accC, f_seq, P_seq, aux_seq, aux_mean, ticket, status);
 }
 
 }  // namespace moe

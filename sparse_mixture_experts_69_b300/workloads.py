@@ -12,6 +12,12 @@ part of the layer.
            U(-0.1,0.1), one bias update at rate 1e-3, bf16
   decode   T=64    d=4096 E=64  k=6 F=1408  SwiGLU, 2 shared, dropless, bf16
 
+Overflow-policy and routing variants of the Switch layer (same inputs):
+  switch_reroute  a full expert sends the token to its next candidate (1 extra)
+  switch_rank     the same, every token's first choice served before any second
+  switch_pad      plain dropping, every expert's block padded to C = 128 rows
+  switch_ec       expert choice: each expert takes its 128 most probable tokens
+
 Input recipe: x ~ N(0,1); Wg, Wnoise, W1, W2, W1s, W2s ~ N(0, 0.02^2); the
 router noise [T,E] ~ N(0,1) generated on the host side and passed in.
 """
@@ -22,7 +28,8 @@ import dataclasses
 import torch
 
 from . import synth
-from .moe import MOE_BF16, MOE_F32, MOE_GELU, MOE_RELU, MOE_SWIGLU, Config
+from .moe import (MOE_BF16, MOE_EXPERT_CHOICE, MOE_F32, MOE_GELU, MOE_PRIORITY_RANK,
+                  MOE_RELU, MOE_SWIGLU, Config)
 
 W_STD = 0.02
 
@@ -61,6 +68,11 @@ WORKLOADS = {
                                         n_shared=2, capacity_factor=0.0, dtype=MOE_BF16,
                                         act=MOE_SWIGLU)),
 }
+WORKLOADS["switch_reroute"] = WORKLOADS["switch"].with_(name="switch_reroute", reroute=1)
+WORKLOADS["switch_rank"] = WORKLOADS["switch"].with_(name="switch_rank", reroute=1,
+                                                     priority=MOE_PRIORITY_RANK)
+WORKLOADS["switch_pad"] = WORKLOADS["switch"].with_(name="switch_pad", pad_to_capacity=1)
+WORKLOADS["switch_ec"] = WORKLOADS["switch"].with_(name="switch_ec", routing=MOE_EXPERT_CHOICE)
 
 
 def make_inputs(wl: Workload, device="cuda", experts: bool = True) -> dict:
