@@ -72,6 +72,14 @@ def workload_desc(wl):
         s += f" zipf-offset={wl.zipf_s}"
     if wl.sel_bias:
         s += f" sel-bias+update(rate={wl.bias_rate:g})"
+    if c.reroute:
+        s += f" reroute={c.reroute} priority={'rank' if c.priority else 'token'}"
+    elif c.priority:
+        s += " priority=rank"
+    if c.pad_to_capacity:
+        s += " padded-to-capacity"
+    if c.routing == 1:
+        s += " expert-choice"
     return s
 
 
@@ -306,22 +314,24 @@ def main():
 
     wl = WORKLOADS[a.workload].with_(seed=rank)
     c = wl.cfg
-    T, E, k, d = c.T, c.n_experts, c.top_k, c.d_model
+    T, E, k, d, nc = c.T, c.n_experts, c.top_k, c.d_model, c.n_cand
+    ec = c.routing == moe.MOE_EXPERT_CHOICE
     inp = make_inputs(wl, dev)
     ws = moe.workspace(c, dev)
     y = torch.empty((T, d), dtype=c.torch_dtype, device=dev)
-    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
-    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, nc), dtype=torch.int32, device=dev)
+    w = torch.empty((T, nc), dtype=torch.float32, device=dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     aux_vecs = torch.empty((3, E), dtype=torch.float32, device=dev)
     out3 = torch.empty(3, dtype=torch.float32, device=dev)
     bias = inp["sel_bias"].clone() if inp["sel_bias"] is not None else None
     stream = torch.cuda.current_stream(dev)
+    # expert choice: the token-choice outputs (ids, gates, counts, statistics) do not apply
+    tc_out = (None,) * 5 if ec else (ids, w, counts, aux_vecs, out3)
 
     def step(x, noise):
         moe.moe_layer_fwd(c, x, inp["Wg"], inp["Wnoise"], noise, inp["logit_offset"], bias,
-                          inp["W1"], inp["W2"], inp["W1s"], inp["W2s"], y, ids, w, counts,
-                          aux_vecs, out3, ws, stream)
+                          inp["W1"], inp["W2"], inp["W1s"], inp["W2s"], y, *tc_out, ws, stream)
         if wl.bias_rate:
             moe.moe_bias_update(c, counts, bias, wl.bias_rate, stream)
 
@@ -362,48 +372,81 @@ def main():
     probs = torch.empty((T, E), device=dev)
     kept = torch.empty(E, dtype=torch.int32, device=dev)
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    slot = torch.empty((T, k), dtype=torch.int32, device=dev)
+    slot = torch.empty((T, nc), dtype=torch.int32, device=dev)
     row_token = torch.empty(R_max, dtype=torch.int32, device=dev)
     xp = torch.empty((R_max, d), dtype=c.torch_dtype, device=dev)
     yp = torch.empty((R_max, d), dtype=c.torch_dtype, device=dev)
     ys = torch.empty((c.n_shared, T, d), dtype=c.torch_dtype, device=dev) if c.n_shared else None
     fP = torch.empty((3, E), device=dev)
-    # each stage alone, called back to back so the device queue never runs dry
+    row_w = torch.empty(R_max, device=dev)
+    tok_row = torch.empty((T, E), dtype=torch.int32, device=dev) if ec else None
+    n_seq = 8
+    seq_offsets = torch.arange(0, T + 1, T // n_seq, dtype=torch.int32, device=dev)[:n_seq + 1]
+    seq_offsets[-1] = T
+    seq_out = torch.empty((2, n_seq, E), device=dev)
+    seq_aux = torch.empty(n_seq + 1, device=dev)
+    # each stage alone: n calls captured in one CUDA graph and replayed, so the
+    # time is the device's (a single call is host-bound for the small stages)
     def time_calls(fn, n):
         for _ in range(3):
             fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                for _ in range(n):
+                    fn()
+        torch.cuda.synchronize()
+        g.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(stream)
-        for _ in range(n):
-            fn()
+        g.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
 
     n_split = max(20, min(200, a.steps // 10))
-    stage_ms = {
-        "route": time_calls(lambda: moe.moe_route(
-            c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"], bias,
-            logits, probs, None, ids, w, 0, ws, stream), n_split),
-        "dispatch": time_calls(lambda: moe.moe_dispatch(
-            c, inp["x"], ids, counts, kept, offsets, slot, xp, row_token, ws, stream), n_split),
-        "expert_ffn": time_calls(lambda: moe.moe_expert_ffn(
-            c, xp, offsets, inp["W1"], inp["W2"], inp["x"], inp["W1s"], inp["W2s"], yp, ys, ws,
-            stream), n_split),
-        "combine": time_calls(lambda: moe.moe_combine(c, yp, slot, w, ys, y, ws, stream),
-                              n_split),
-        "aux": time_calls(lambda: moe.moe_aux_stats(c, probs, ids, w, fP[0], fP[1], fP[2], out3,
-                                                    ws, stream), n_split),
-    }
+    # the stage calls take torch's current stream, which is the capture stream in time_calls
+    route = lambda: moe.moe_route(
+        c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"], bias, logits,
+        probs, None, None if ec else ids, None if ec else w, 0, ws)
+    ffn = lambda: moe.moe_expert_ffn(c, xp, offsets, inp["W1"], inp["W2"], inp["x"], inp["W1s"],
+                                     inp["W2s"], yp, ys, ws)
+    if ec:
+        stage_ms = {
+            "route": time_calls(route, n_split),
+            "dispatch": time_calls(lambda: moe.moe_expert_choice_dispatch(
+                c, inp["x"], probs, offsets, row_token, row_w, tok_row, xp, ws), n_split),
+            "expert_ffn": time_calls(ffn, n_split),
+            "combine": time_calls(lambda: moe.moe_expert_choice_combine(
+                c, yp, tok_row, probs, ys, y, ws), n_split),
+        }
+    else:
+        stage_ms = {
+            "route": time_calls(route, n_split),
+            "dispatch": time_calls(lambda: moe.moe_dispatch(
+                c, inp["x"], ids, counts, kept, offsets, slot, xp, row_token, ws), n_split),
+            "expert_ffn": time_calls(ffn, n_split),
+            "combine": time_calls(lambda: moe.moe_combine(c, yp, slot, w, ys, y, ws),
+                                  n_split),
+            "aux": time_calls(lambda: moe.moe_aux_stats(c, probs, ids, w, fP[0], fP[1], fP[2],
+                                                        out3, ws), n_split),
+            "seq_aux_8_sequences": time_calls(lambda: moe.moe_seq_aux_stats(
+                c, probs, ids, seq_offsets, n_seq, seq_out[0], seq_out[1], seq_aux[:n_seq],
+                seq_aux[n_seq:], ws), n_split),
+        }
     st = moe.moe_read_device_error(c, ws)
     if st != 0:
         raise RuntimeError("device status after the stage timing: " + moe.moe_status_string(st))
 
-    # algorithmic work of the expert FFN (two grouped-GEMM launches)
-    kept_h = kept.cpu()
-    R = int(kept_h.sum())
-    touched = int((kept_h > 0).sum())
+    # algorithmic work of the expert FFN (two grouped-GEMM launches): rows the
+    # GEMMs run on (padding rows included where the blocks are padded), and the
+    # weights of every expert that owns at least one row
+    R = int(offsets[E].item())
+    touched = E if (ec or c.pad_to_capacity) else int((kept.cpu() > 0).sum())
     es = 2 if c.dtype == 1 else 4
     F, F1, S = c.d_ff, c.F1, c.n_shared
     w_bytes = (touched + S) * (F1 * d + d * F) * es
@@ -432,7 +475,8 @@ def main():
             noise_dev.copy_(noise_host, non_blocking=True)
         step(x_dev, noise_dev)
         y_host.copy_(y, non_blocking=True)
-        o3_host.copy_(out3, non_blocking=True)
+        if not ec:
+            o3_host.copy_(out3, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -450,21 +494,32 @@ def main():
         e2e_s = float(t.item())
     h2d = x_host.numel() * x_host.element_size() + (
         noise_host.numel() * 4 if noise_host is not None else 0)
-    d2h = y_host.numel() * y_host.element_size() + 12
+    d2h = y_host.numel() * y_host.element_size() + (0 if ec else 12)
     e2e_value = world * T * K2 / e2e_s
 
     # layer path: [Wg transpose (bf16)], router GEMM, fused selection + histogram +
     # statistics, capacity scan + slots (one launch up to 256 token blocks),
     # permute, up GEMM, down GEMM, [combine: skipped for bf16 top-1 without
     # shared experts, where the down GEMM writes y], [bias update]
-    scatter = c.dtype == 1 and c.top_k == 1 and c.n_shared == 0
-    launches_per_step = ((1 if c.dtype == 1 else 0) + 2 + (1 if (T + 255) // 256 <= 256 else 2)
-                         + 1 + 2 + (0 if scatter else 1) + (1 if wl.bias_rate else 0))
+    # overflow policies: one capacity kernel instead of scan + slots; expert
+    # choice: select + gather instead of capacity + permute, its own combine
+    scatter = (c.dtype == 1 and c.top_k == 1 and nc == 1 and not c.pad_to_capacity
+               and c.n_shared == 0)
+    policy = nc > k or c.priority != 0
+    route_launches = (1 if c.dtype == 1 else 0) + 2
+    if ec:
+        launches_per_step = route_launches + 2 + 2 + 1
+    else:
+        cap_launches = 1 if policy else (1 if (T + 255) // 256 <= 256 else 2)
+        launches_per_step = (route_launches + cap_launches + 1 + 2 + (0 if scatter else 1)
+                             + (1 if wl.bias_rate else 0))
 
     if rank != 0:
         return 0
     cb = None
-    if not a.no_cpu_baseline and world == 1:
+    # the oracle's per-token sample has no expert-choice counterpart (an expert's
+    # choice depends on the whole batch); that variant reports none
+    if not a.no_cpu_baseline and world == 1 and not ec:
         cb = cpu_baseline(wl, inp)
     clocks = clk.summary()
     line = {

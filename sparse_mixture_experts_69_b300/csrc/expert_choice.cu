@@ -10,9 +10,10 @@
 // Selection, one CTA per expert: the column probs[:,e] is staged in shared
 // memory as float bit patterns (for p >= 0 the unsigned order of the bits
 // is the numeric order), a 4-digit radix select finds the C-th largest value
-// thr and how many of the tokens equal to it are taken, and one ordered pass
-// over the tokens (warp ballots, block prefix counts) takes every token above
-// thr and the first such tokens equal to it, assigning rows in token order.
+// thr and how many of the tokens equal to it are taken, and ordered passes
+// over contiguous per-warp token ranges (warp ballots, scans over warps) take
+// every token above thr and the first such tokens equal to it, assigning
+// rows in token order.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -27,27 +28,25 @@ __device__ __forceinline__ unsigned lanemask_lt_ec() {
     return m;
 }
 
-// Exclusive prefix count of `pred` over the block (thread order) and the
-// block total. Uses wsum[kEcWarps + 1] in shared memory; all threads call it.
-__device__ __forceinline__ int block_prefix(bool pred, int* wsum, int* total) {
+// Exclusive prefix sum over the warps of the block of one value per warp
+// (every lane of a warp passes the same v); all threads call it. Uses
+// wsum[kEcWarps + 1] in shared memory.
+__device__ __forceinline__ int warp_exclusive_scan_over_block(int v, int* wsum) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned b = __ballot_sync(0xffffffffu, pred);
-    if (lane == 0) wsum[warp] = __popc(b);
+    if (lane == 0) wsum[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        const int v = lane < kEcWarps ? wsum[lane] : 0;
-        int incl = v;
+        const int x = lane < kEcWarps ? wsum[lane] : 0;
+        int incl = x;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int n = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += n;
         }
-        if (lane < kEcWarps) wsum[lane] = incl - v;
-        if (lane == 31) wsum[kEcWarps] = incl;
+        if (lane < kEcWarps) wsum[lane] = incl - x;
     }
     __syncthreads();
-    const int r = wsum[warp] + __popc(b & lanemask_lt_ec());
-    *total = wsum[kEcWarps];
+    const int r = wsum[warp];
     __syncthreads();  // wsum is reused by the next call
     return r;
 }
@@ -87,22 +86,53 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(int T, int E, int
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = threadIdx.x; i < 256; i += kEcThreads) hist[i] = 0;
         __syncthreads();
-        for (int t = threadIdx.x; t < T; t += kEcThreads) {
-            const unsigned v = col[t];
-            if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1);
+        // most probabilities share their top bits: aggregate equal digits within
+        // the warp so each distinct digit costs one shared-memory atomic per warp
+        for (int t0 = 0; t0 < T; t0 += kEcThreads) {
+            const int t = t0 + threadIdx.x;
+            const unsigned v = t < T ? col[t] : 0u;
+            const bool in = t < T && (v & pmask) == prefix;
+            const unsigned dg = in ? (v >> shift) & 255u : 256u;  // 256: not counted
+            const unsigned same = __match_any_sync(0xffffffffu, dg);
+            if (in && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&hist[dg], __popc(same));
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int above = 0, dsel = 0;
-            for (int dgt = 255; dgt >= 0; --dgt) {
-                if (above + hist[dgt] >= left) {
-                    dsel = dgt;
-                    break;
-                }
-                above += hist[dgt];
+        // warp 0 finds the digit: lane l holds bins 255-8l .. 248-8l (descending),
+        // a suffix sum over lanes gives each bin the count of values above it
+        if (threadIdx.x < 32) {
+            const int l = threadIdx.x;
+            int h[8], sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                h[i] = hist[255 - 8 * l - i];
+                sum += h[i];
             }
-            s_digit = (unsigned)dsel;
-            s_left = left - above;
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (l >= o) incl += n;
+            }
+            int above = incl - sum;  // values in the bins of lower lanes (larger digits)
+            int found = -1, above_found = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (found < 0 && above + h[i] >= left) {
+                    found = 255 - 8 * l - i;
+                    above_found = above;
+                }
+                above += h[i];
+            }
+            // the largest digit whose cumulative count reaches `left` is in the
+            // lowest lane that found one
+            const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
+            const int src = hit ? __ffs(hit) - 1 : 31;
+            const int dsel = __shfl_sync(0xffffffffu, found, src);
+            const int ab = __shfl_sync(0xffffffffu, above_found, src);
+            if (l == 0) {
+                s_digit = (unsigned)(dsel < 0 ? 0 : dsel);
+                s_left = left - ab;
+            }
         }
         __syncthreads();
         prefix |= s_digit << shift;
@@ -110,21 +140,45 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(int T, int E, int
         left = s_left;
         __syncthreads();
     }
-    // tokens above thr are all taken; of those equal to it, the first `left`
+    // tokens above thr are all taken; of those equal to it, the first `left` in
+    // token order. Warp w owns the contiguous tokens [w*L, (w+1)*L): it counts
+    // its ties, then (after a scan over warps gives each warp its tie base)
+    // its takes, then (after a second scan) writes its rows in token order.
     const unsigned thr = prefix;
-    int ties_before = 0, rows_before = 0;
-    for (int t0 = 0; t0 < T; t0 += kEcThreads) {
-        const int t = t0 + threadIdx.x;
-        const unsigned v = t < T ? col[t] : 0u;
-        const bool tie = t < T && v == thr;
-        int nties;
-        const int tie_rank = ties_before + block_prefix(tie, wsum, &nties);
-        const bool take = t < T && (v > thr || (tie && tie_rank < left));
-        int ntake;
-        const int i = rows_before + block_prefix(take, wsum, &ntake);
-        if (t < T) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned lt = lanemask_lt_ec();
+    const int L = (T + kEcWarps - 1) / kEcWarps;
+    const int w0 = min(T, warp * L), w1 = min(T, w0 + L);
+    int nties = 0;
+    for (int t0 = w0; t0 < w1; t0 += 32) {
+        const int t = t0 + lane;
+        nties += __popc(__ballot_sync(0xffffffffu, t < w1 && col[t] == thr));
+    }
+    const int tie_base0 = warp_exclusive_scan_over_block(nties, wsum);
+    int tie_base = tie_base0;
+    int ntake = 0;
+    for (int t0 = w0; t0 < w1; t0 += 32) {
+        const int t = t0 + lane;
+        const unsigned v = t < w1 ? col[t] : 0u;
+        const bool tie = t < w1 && v == thr;
+        const unsigned tb = __ballot_sync(0xffffffffu, tie);
+        const bool take = t < w1 && (v > thr || (tie && tie_base + __popc(tb & lt) < left));
+        tie_base += __popc(tb);
+        ntake += __popc(__ballot_sync(0xffffffffu, take));
+    }
+    tie_base = tie_base0;
+    int row_base = warp_exclusive_scan_over_block(ntake, wsum);
+    for (int t0 = w0; t0 < w1; t0 += 32) {
+        const int t = t0 + lane;
+        const unsigned v = t < w1 ? col[t] : 0u;
+        const bool tie = t < w1 && v == thr;
+        const unsigned tb = __ballot_sync(0xffffffffu, tie);
+        const bool take = t < w1 && (v > thr || (tie && tie_base + __popc(tb & lt) < left));
+        tie_base += __popc(tb);
+        const unsigned kb = __ballot_sync(0xffffffffu, take);
+        if (t < w1) {
             if (take) {
-                const int r = e * C + i;
+                const int r = e * C + row_base + __popc(kb & lt);
                 row_token[r] = t;
                 row_w[r] = __uint_as_float(v);
                 tok_row[(size_t)t * E + e] = r;
@@ -132,8 +186,7 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(int T, int E, int
                 tok_row[(size_t)t * E + e] = -1;
             }
         }
-        ties_before += nties;
-        rows_before += ntake;
+        row_base += __popc(kb);
     }
     if (threadIdx.x == 0) {
         offsets[e] = e * C;

@@ -166,6 +166,50 @@ __global__ void __launch_bounds__(kPolThreads, 1) cap_policy_kernel(PolArgs a) {
         for (int rd = 0; rd < rounds; ++rd) {
             const unsigned round_bits = rounds == 1 ? 0xffffffffu : (1u << rd);
             int* buf = cnt + (rd & 1) * E;
+            if (nown <= kPolThreads) {
+                // one chunk: the lane masks of this round give the counts too
+                for (int i = tid; i < kPolWarps * E; i += kPolThreads) mask[i] = 0;
+                __syncthreads();
+                const unsigned mine = tid < nown ? att[tid] & round_bits : 0u;
+                const int t = t_lo + (tid < nown ? tid : 0);
+                const int32_t* row = a.ids + (size_t)t * nc;
+                for (unsigned m = mine; m; m &= m - 1)
+                    atomicOr(&mask[warp * E + row[__ffs(m) - 1]], 1u << lane);
+                __syncthreads();
+                for (int e = tid; e < E; e += kPolThreads) {
+                    int n = 0;
+                    for (int w = 0; w < kPolWarps; ++w) n += __popc(mask[w * E + e]);
+                    buf[e] = n;
+                }
+                cluster_barrier(cl);  // (A) every CTA's counts of this round are complete
+                for (int e = tid; e < E; e += kPolThreads) {
+                    int v[kPolCtas];  // the eight remote loads issued together
+#pragma unroll
+                    for (int r = 0; r < kPolCtas; ++r) v[r] = *cl.map_shared_rank(buf + e, r);
+                    int before = 0, all = 0;
+#pragma unroll
+                    for (int r = 0; r < kPolCtas; ++r) {
+                        all += v[r];
+                        if (r < c) before += v[r];
+                    }
+                    base[e] = total[e] + before;
+                    total[e] += all;
+                }
+                __syncthreads();
+                for (unsigned m = mine; m; m &= m - 1) {
+                    const int j = __ffs(m) - 1;
+                    const int e = row[j];
+                    int r = base[e] + __popc(mask[warp * E + e] & lt);
+                    for (int w = 0; w < warp; ++w) r += __popc(mask[w * E + e]);
+                    a.slot[(size_t)t * nc + j] = r;
+                    if (r == C - 1) {  // the one try with rank C-1: publish the fill position
+                        const int v = visit_pos(a, t, j);
+                        for (int q = 0; q < kPolCtas; ++q) *cl.map_shared_rank(tau_new + e, q) = v;
+                    }
+                }
+                __syncthreads();  // the masks are cleared again by the next round
+                continue;
+            }
             for (int e = tid; e < E; e += kPolThreads) buf[e] = 0;
             __syncthreads();
             for (int tl = tid; tl < nown; tl += kPolThreads) {

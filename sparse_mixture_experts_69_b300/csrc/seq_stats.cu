@@ -22,8 +22,9 @@
 namespace moe {
 
 namespace {
-constexpr int kSeqWarpTokens = 32;
-constexpr int kSeqAccThreads = 128;  // 4 warps: 128 tokens per CTA
+constexpr int kSeqWarpTokens = 8;
+constexpr int kSeqAccThreads = 128;  // 4 warps: 32 tokens per CTA
+constexpr int kSeqBatch = 8;         // probabilities loaded together before they are added
 constexpr int kSeqFinThreads = 256;
 }  // namespace
 
@@ -53,10 +54,11 @@ __global__ void __launch_bounds__(kSeqAccThreads) seq_accumulate_kernel(
     const int t1 = min(last, (blockIdx.x * (kSeqAccThreads / 32) + (threadIdx.x >> 5) + 1) *
                                  kSeqWarpTokens);
     if (t0 >= t1) return;
+    const int q0 = seq_of(seq_offsets, n_seq, t0);
     // choice counts: lane j < k of the token's row, token by token
     bool bad = false;
     {
-        int q = seq_of(seq_offsets, n_seq, t0);
+        int q = q0;
         for (int t = t0; t < t1; ++t) {
             while (q + 1 < n_seq && seq_offsets[q + 1] <= t) ++q;
             if (lane < k) {
@@ -67,18 +69,28 @@ __global__ void __launch_bounds__(kSeqAccThreads) seq_accumulate_kernel(
         }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(status, DEV_BAD_ARG);
-    // probability sums, 32 experts (one per lane) at a time
+    // probability sums, 32 experts (one per lane) at a time; kSeqBatch tokens'
+    // values are loaded together, then added token by token
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        int q = seq_of(seq_offsets, n_seq, t0);
+        int q = q0;
         unsigned long long run = 0;
-        for (int t = t0; t < t1; ++t) {
-            if (q + 1 < n_seq && seq_offsets[q + 1] <= t) {  // the run's sequence ended
-                if (e < E && run) atomicAdd(&accP[(size_t)q * E + e], run);
-                run = 0;
-                while (q + 1 < n_seq && seq_offsets[q + 1] <= t) ++q;
+        for (int tb = t0; tb < t1; tb += kSeqBatch) {
+            float v[kSeqBatch];
+#pragma unroll
+            for (int u = 0; u < kSeqBatch; ++u)
+                v[u] = (e < E && tb + u < t1) ? __ldg(&probs[(size_t)(tb + u) * E + e]) : 0.f;
+#pragma unroll
+            for (int u = 0; u < kSeqBatch; ++u) {
+                const int t = tb + u;
+                if (t >= t1) break;
+                if (q + 1 < n_seq && seq_offsets[q + 1] <= t) {  // the run's sequence ended
+                    if (e < E && run) atomicAdd(&accP[(size_t)q * E + e], run);
+                    run = 0;
+                    while (q + 1 < n_seq && seq_offsets[q + 1] <= t) ++q;
+                }
+                run += to_fix(v[u]);
             }
-            if (e < E) run += to_fix(__ldg(&probs[(size_t)t * E + e]));
         }
         if (e < E && run) atomicAdd(&accP[(size_t)q * E + e], run);
     }
