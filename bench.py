@@ -53,6 +53,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, pg, device) -> float:
+    """The largest value over all ranks: a job's time is its slowest rank's."""
+    if pg is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def tokens_per_s(world: int, T: int, steps: int, ms_total: float) -> float:
+    """Whole-job throughput: every rank processes T tokens per step."""
+    return world * T * steps / (ms_total / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -356,15 +370,11 @@ def main():
         torch.cuda.synchronize()
     barrier()
     ms = ev0.elapsed_time(ev1)
-    ms_max = ms
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, pg, dev)
     st = moe.moe_read_device_error(c, ws)
     if st != 0:
         raise RuntimeError("device status after timing: " + moe.moe_status_string(st))
-    value = world * T * a.steps / (ms_max / 1e3)
+    value = tokens_per_s(world, T, a.steps, ms_max)
 
     # ------------------------------------------------ per-stage split (same calls, stage APIs)
     C, R_max = moe.moe_capacity(c)
@@ -488,14 +498,11 @@ def main():
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
     barrier()
-    if pg:
-        t = torch.tensor([e2e_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, pg, dev)
     h2d = x_host.numel() * x_host.element_size() + (
         noise_host.numel() * 4 if noise_host is not None else 0)
     d2h = y_host.numel() * y_host.element_size() + (0 if ec else 12)
-    e2e_value = world * T * K2 / e2e_s
+    e2e_value = tokens_per_s(world, T, K2, e2e_s * 1e3)
 
     # layer path: [Wg transpose (bf16)], router GEMM, fused selection + histogram +
     # statistics, capacity scan + slots (one launch up to 256 token blocks),
