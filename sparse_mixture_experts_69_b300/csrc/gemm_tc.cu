@@ -35,11 +35,7 @@
 #define MOE_TC_ROT 0  // 1: each tile starts its k loop at a tile-dependent block
 #endif
 #ifndef MOE_TC_BN_ACT
-#define MOE_TC_BN_ACT 256  // output tile width of the ReLU/GELU up GEMMs
-#endif
-
-#ifndef MOE_TC_BN_DOWN
-#define MOE_TC_BN_DOWN 256  // output tile width of the down GEMMs (no activation)
+#define MOE_TC_BN_ACT 256  // output tile width of the ReLU/GELU/plain expert GEMMs
 #endif
 #ifndef MOE_TC_SMEM
 #define MOE_TC_SMEM (192 * 1024)  // shared memory for the pipeline stages
@@ -612,7 +608,6 @@ cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStr
     tc::TcArgs a{};
     a.p = g;
     if (g.glu) return tc::launch<256, tc::EPI_GLU>(a, st);
-    if (g.act < 0) return tc::launch<MOE_TC_BN_DOWN, tc::EPI_ACT>(a, st);
     return tc::launch<MOE_TC_BN_ACT, tc::EPI_ACT>(a, st);
 }
 
