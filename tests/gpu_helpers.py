@@ -98,3 +98,41 @@ def run_layer(wl, inp, device, ws=None):
     st = moe.moe_read_device_error(c, ws)
     assert st == 0, moe.moe_status_string(st)
     return o, ws
+
+
+def layer_vs_oracle(wl, device, inp=None):
+    """Run moe_layer_fwd on workload `wl` and compare y on every token with
+    the oracle fed the GPU's routing (identical router outputs): capacity,
+    expert FFNs and combine are the oracle's. Returns (outputs, inputs)."""
+    import oracle
+    from sparse_mixture_experts_69_b300.workloads import make_inputs
+
+    c = wl.cfg
+    if inp is None:
+        inp = make_inputs(wl, device)
+    T, E, d, nc = c.T, c.n_experts, c.d_model, c.n_cand
+    y = torch.empty((T, d), dtype=c.torch_dtype, device=device)
+    ids = torch.empty((T, nc), dtype=torch.int32, device=device)
+    w = torch.empty((T, nc), device=device)
+    counts = torch.empty(E, dtype=torch.int32, device=device)
+    ws = moe.workspace(c, device)
+    moe.moe_layer_fwd(c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"],
+                      inp["sel_bias"], inp["W1"], inp["W2"], inp["W1s"], inp["W2s"], y, ids, w,
+                      counts, None, None, ws)
+    st = moe.moe_read_device_error(c, ws)
+    assert st == 0, moe.moe_status_string(st)
+    ids_h = ids.cpu().numpy()
+    C, _ = moe.moe_capacity(c)
+    cap = oracle.capacity_policy(ids_h, c.top_k, E, C, priority=c.priority,
+                                 pad=bool(c.pad_to_capacity))
+    np.testing.assert_array_equal(counts.cpu().numpy(), cap["counts"])
+    rd = oracle.ROUND_BF16 if c.dtype == moe.MOE_BF16 else oracle.ROUND_F32
+    cpu = lambda t: None if t is None else t.cpu()
+    W1, W2, W1s, W2s = cpu(inp["W1"]), cpu(inp["W2"]), cpu(inp["W1s"]), cpu(inp["W2s"])
+    O, Os = oracle.ffn_for_tokens(cpu(inp["x"]), list(range(T)), ids_h, cap["slot"],
+                                  lambda e: W1[e], lambda e: W2[e], c.act, rd, c.n_shared,
+                                  (lambda s: W1s[s]) if c.n_shared else None,
+                                  (lambda s: W2s[s]) if c.n_shared else None)
+    y_ref = oracle.combine(np.asarray(np32(w), np.float64), cap["slot"], O, Os, rd)
+    assert_maxabs(np32(y), y_ref, TOL_Y[c.dtype], "y")
+    return dict(y=y, ids=ids, w=w, counts=counts, slot=cap["slot"], y_ref=y_ref), inp
