@@ -284,11 +284,14 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec, in
                                                       const int32_t* __restrict__ slot,
                                                       uint4* __restrict__ xp,
                                                       uint4* __restrict__ y_zero, int* status) {
+    // the expert GEMM that follows reads the offsets before its own wait, so
+    // dependents launch only after this kernel's wait (the capacity kernel
+    // that wrote them is then complete)
+    pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
-    pdl_wait();
     int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
     if (my_slot >= rows) {  // never produced by the capacity kernels: skip and report
         flag_status(status, DEV_BAD_ARG | DEV_SITE_PERMUTE_ROW);

@@ -210,11 +210,14 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int rows, int nvec,
                                                           const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ row_token,
                                                           uint4* __restrict__ xp) {
+    // the expert GEMM that follows reads the offsets before its own wait, so
+    // dependents launch only after this kernel's wait (the selection kernel
+    // that wrote them is then complete)
+    pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= rows) return;
-    pdl_wait();
     const int t = row_token[r];
     const uint4* src = x + (size_t)t * nvec;
     for (int v = lane; v < nvec; v += 32) xp[(size_t)r * nvec + v] = __ldg(src + v);

@@ -273,6 +273,32 @@ __device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float (
 }
 
 // ------------------------------------------------------------------ kernel
+// First B row of each B box of tile gt: SwiGLU tiles take 128 gate rows and
+// the matching 128 up rows; other tiles take BN consecutive rows.
+template <int BN, int EPI>
+__device__ __forceinline__ void b_tile_rows(const GroupedGemm& p, const GroupTile& gt,
+                                            int (&brow)[Cfg<BN>::B_LOADS]) {
+#pragma unroll
+    for (int h = 0; h < Cfg<BN>::B_LOADS; ++h) {
+        if (EPI == EPI_GLU)
+            brow[h] = gt.b_row + h * p.N + gt.n_tile * 128;
+        else
+            brow[h] = gt.b_row + gt.n_tile * BN + h * Cfg<BN>::B_BOX_ROWS;
+    }
+}
+// The B tile of k block kb into one ring stage.
+template <int BN>
+__device__ __forceinline__ void load_b_stage(uint8_t* sB_stage, const CUtensorMap* mb,
+                                             uint64_t* bar, int kb,
+                                             const int (&brow)[Cfg<BN>::B_LOADS]) {
+#pragma unroll
+    for (int hk = 0; hk < KH; ++hk)
+#pragma unroll
+        for (int h = 0; h < Cfg<BN>::B_LOADS; ++h)
+            tma_load_2d(sB_stage + hk * Cfg<BN>::B_HALF + h * Cfg<BN>::B_BOX_ROWS * 128, mb, bar,
+                        kb * BK + hk * BKH, brow[h]);
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0,
@@ -308,14 +334,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmB0);
         prefetch_tmap(&tmB1);
     }
-    pdl_trigger();
-    pdl_wait();
-    build_tile_table(p, BM, mt_start);
+    // early launch: the offsets are final and B is never written by the
+    // preceding kernels, so the tile table and the first B tiles do not wait
+    // for the preceding kernel (A, the outputs and TMEM do)
+    const bool early = p.early != 0;
+    if (!early) pdl_wait();
+    if (early)
+        build_tile_table<true>(p, BM, mt_start);
+    else
+        build_tile_table<false>(p, BM, mt_start);
     __syncthreads();
     const int total = mt_start[G] * nt;
     // no work: leave before any allocation (CTA 0 stays when it owes the
-    // statistics finalisation)
-    if ((int)blockIdx.x >= total && !(p.fin_acc_mem && blockIdx.x == 0)) return;
+    // statistics finalisation); every CTA passes the wait before it exits, so
+    // this kernel completes only after the preceding one has
+    if ((int)blockIdx.x >= total && !(p.fin_acc_mem && blockIdx.x == 0)) {
+        if (early) pdl_wait();
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -331,6 +367,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    __syncthreads();
+    // first ring stages: expected bytes and B tiles (A follows after the wait)
+    int prefilled = 0;
+    if (early && threadIdx.x == 0) {
+        for (int tile = blockIdx.x; tile < total && prefilled < C::STAGES; tile += gridDim.x) {
+            const GroupTile gt = decode_tile<true>(p, mt_start, nt, BM, tile);
+            const CUtensorMap* mb = gt.g < p.E ? &tmB0 : &tmB1;
+            int brow[C::B_LOADS];
+            b_tile_rows<BN, EPI>(p, gt, brow);
+            for (int kb0 = 0; kb0 < nkb && prefilled < C::STAGES; ++kb0) {
+                const int rot = MOE_TC_ROT ? tile % nkb : 0;
+                const int kb = kb0 + rot < nkb ? kb0 + rot : kb0 + rot - nkb;
+                mbar_arrive_expect_tx(&full[prefilled], C::STAGE_BYTES);
+                load_b_stage<BN>(sB + prefilled * C::B_BYTES, mb, &full[prefilled], kb, brow);
+                ++prefilled;
+            }
+        }
+    }
+    if (early) pdl_wait();
+    // dependents may launch once every CTA is past the wait: a kernel that
+    // follows this one can rely on the kernel before this one being complete
+    pdl_trigger();
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
@@ -347,38 +405,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;
             bool ok = true;
+            int item = 0;  // (tile, k block) pairs issued so far
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
                 const bool routed = gt.g < p.E;
                 const CUtensorMap* ma = routed ? &tmA0 : &tmA1;
                 const CUtensorMap* mb = routed ? &tmB0 : &tmB1;
                 int brow[C::B_LOADS];
-#pragma unroll
-                for (int h = 0; h < C::B_LOADS; ++h) {
-                    if (EPI == EPI_GLU)
-                        brow[h] = gt.b_row + h * p.N + gt.n_tile * 128;  // gate half, up half
-                    else
-                        brow[h] = gt.b_row + gt.n_tile * BN + h * C::B_BOX_ROWS;
-                }
+                b_tile_rows<BN, EPI>(p, gt, brow);
                 const int rot = MOE_TC_ROT ? tile % nkb : 0;
-                for (int kb0 = 0; kb0 < nkb; ++kb0) {
+                for (int kb0 = 0; kb0 < nkb; ++kb0, ++item) {
                     const int kb = kb0 + rot < nkb ? kb0 + rot : kb0 + rot - nkb;
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, kTimeoutNs)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    // prefilled stages already expect their bytes and hold B
+                    const bool fresh = item >= prefilled;
+                    if (fresh) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
 #pragma unroll
-                    for (int hk = 0; hk < KH; ++hk) {
-                        const int kx = kb * BK + hk * BKH;
-                        tma_load_2d(sA + stage * C::A_BYTES + hk * C::A_HALF, ma, &full[stage], kx,
-                                    gt.a_row);
-#pragma unroll
-                        for (int h = 0; h < C::B_LOADS; ++h)
-                            tma_load_2d(sB + stage * C::B_BYTES + hk * C::B_HALF +
-                                            h * C::B_BOX_ROWS * 128,
-                                        mb, &full[stage], kx, brow[h]);
-                    }
+                    for (int hk = 0; hk < KH; ++hk)
+                        tma_load_2d(sA + stage * C::A_BYTES + hk * C::A_HALF, ma, &full[stage],
+                                    kb * BK + hk * BKH, gt.a_row);
+                    if (fresh) load_b_stage<BN>(sB + stage * C::B_BYTES, mb, &full[stage], kb, brow);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {

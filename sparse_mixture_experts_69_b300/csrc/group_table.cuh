@@ -21,10 +21,15 @@ struct GroupTile {
     int b_row;    // first B row of the group (in B0 or B1)
 };
 
+// L2: read the offsets from L2 (ld.global.cg), for reads made before the wait
+// for the preceding kernel (the offsets are final by then, but an L1 line
+// could predate them); otherwise plain loads.
+template <bool L2 = false>
 __device__ __forceinline__ int group_rows(const GroupedGemm& p, int g, int* a_row, int* out_row,
                                           bool* bad) {
     if (g < p.E) {
-        int lo = p.offsets[g], hi = p.offsets[g + 1];
+        const int lo = L2 ? __ldcg(p.offsets + g) : p.offsets[g];
+        const int hi = L2 ? __ldcg(p.offsets + g + 1) : p.offsets[g + 1];
         if (lo < 0 || hi < lo || hi > p.max_rows0) {
             *bad = true;
             *a_row = 0;
@@ -42,6 +47,7 @@ __device__ __forceinline__ int group_rows(const GroupedGemm& p, int g, int* a_ro
 }
 
 // Warp 0 of the block fills mt_start[0..G] (row-tile prefix). Caller syncs.
+template <bool L2 = false>
 __device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, int* mt_start) {
     if (threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
@@ -53,7 +59,7 @@ __device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, i
         int mt = 0;
         if (g < G) {
             int ar, orow;
-            int M = group_rows(p, g, &ar, &orow, &bad);
+            int M = group_rows<L2>(p, g, &ar, &orow, &bad);
             mt = (M + BM - 1) / BM;
         }
         int incl = mt;
@@ -69,6 +75,7 @@ __device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, i
     if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DEV_BAD_ARG);
 }
 
+template <bool L2 = false>
 __device__ __forceinline__ GroupTile decode_tile(const GroupedGemm& p, const int* mt_start,
                                                  int nt, int BM, int tile) {
     const int G = p.E + p.S;
@@ -87,7 +94,7 @@ __device__ __forceinline__ GroupTile decode_tile(const GroupedGemm& p, const int
     t.m0 = (local % mt) * BM;
     bool bad = false;
     int a_row, out_row;
-    const int M = group_rows(p, lo, &a_row, &out_row, &bad);
+    const int M = group_rows<L2>(p, lo, &a_row, &out_row, &bad);
     t.rows = M - t.m0;
     t.a_row = a_row + t.m0;
     t.out_row = out_row + t.m0;

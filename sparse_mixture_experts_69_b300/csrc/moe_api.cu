@@ -246,7 +246,7 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
                     const int32_t* offsets, const void* W1, const void* W2, const void* x,
                     const void* W1s, const void* W2s, void* yp, void* ys,
                     const int32_t* scatter_rows, const float* scatter_gate, void* y,
-                    float* fin_aux_vecs, float* fin_out3, cudaStream_t st) {
+                    float* fin_aux_vecs, float* fin_out3, bool up_early, cudaStream_t st) {
     int* status = at<int>(ws, L.status);
     void* h = at<void>(ws, L.h);
     void* h_shared = static_cast<char*>(h) + (size_t)s.R_max * s.F * s.esize;
@@ -281,6 +281,7 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
         up.fin_w_imp = s.w_imp;
     }
     up.status = status;
+    up.early = up_early ? 1 : 0;
     MOE_CUDA(launch_grouped_gemm(s, up, st));
     GroupedGemm dn{};
     dn.offsets = offsets;
@@ -307,6 +308,9 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     dn.scatter_scale = scatter_gate;
     dn.scatter_out = y;
     dn.status = status;
+    // the up projection just launched signals only after its wait: when this
+    // launch starts, whatever wrote the offsets before it is complete
+    dn.early = 1;
     MOE_CUDA(launch_grouped_gemm(s, dn, st));
     return MOE_OK;
 }
@@ -413,8 +417,10 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const i
     if (!aligned16(xp) || !aligned16(W1) || !aligned16(W2) || !aligned16(yp)) return MOE_ERR_UNSUPPORTED;
     if (s.S > 0 && (!aligned16(x) || !aligned16(W1s) || !aligned16(W2s) || !aligned16(ys)))
         return MOE_ERR_UNSUPPORTED;
+    // the preceding kernel is the caller's: the up projection waits for it
+    // before it reads the offsets
     return ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, nullptr, nullptr, nullptr,
-                    nullptr, nullptr, (cudaStream_t)stream);
+                    nullptr, nullptr, false, (cudaStream_t)stream);
 }
 
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot,
@@ -496,8 +502,10 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
         MOE_TRY(route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
                            nullptr, nullptr, nullptr, nullptr, nullptr, st));
         MOE_TRY(ec_dispatch_impl(s, L, ws, x, probs, offsets, row_token, row_w, tok_row, xp, st));
+        // the gather signals its dependents after its wait: the offsets the
+        // selection wrote are final when the up projection launches
         MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, nullptr, nullptr,
-                         nullptr, nullptr, nullptr, st));
+                         nullptr, nullptr, nullptr, true, st));
         MOE_CUDA(launch_expert_choice_combine(s, yp, tok_row, probs, s.S ? ys : nullptr, y, st));
         return MOE_OK;
     }
@@ -506,16 +514,18 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
     MOE_TRY(route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
                        nullptr, ids, w, av, o3, st));
     // top-1 without shared experts: each token has at most one expert row, so the
-    // down GEMM writes y itself (dropped tokens are zeroed by the slot kernel).
+    // down GEMM writes y itself (dropped tokens are zeroed by the permute kernel).
     // Not with re-route candidates (a token's gate depends on which candidate
     // is kept) or padding (padding rows belong to no token).
     const bool scatter = s.k == 1 && s.nc == 1 && !s.pad && s.S == 0 && s.dtype == MOE_BF16;
     MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token,
                           !uses_policy(s), scatter ? y : nullptr, st));
+    // the permute signals its dependents after its wait: the offsets the
+    // capacity kernel wrote are final when the up projection launches
     MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys,
                      scatter ? row_token : nullptr, scatter ? w : nullptr,
                      scatter ? y : nullptr, s.dtype == MOE_BF16 ? av : nullptr,
-                     s.dtype == MOE_BF16 ? o3 : nullptr, st));
+                     s.dtype == MOE_BF16 ? o3 : nullptr, true, st));
     if (!scatter)
         MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
     return MOE_OK;

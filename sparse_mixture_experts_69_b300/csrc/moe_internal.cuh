@@ -181,6 +181,13 @@ struct GroupedGemm {
     int fin_k;
     float fin_w_imp;
     int* status;
+    // 1: when the launch is made the offsets are final and B0 / B1 are not
+    // written by any kernel still running, so the tcgen05 kernel builds its tile
+    // table and loads its first B tiles before it waits for the preceding
+    // kernel. Every tcgen05 launch signals its dependents only after that wait,
+    // which makes this hold for the down projection that follows an up
+    // projection.
+    int early;
 };
 cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream_t st);
 
@@ -199,11 +206,21 @@ int num_sms();
 
 // ------------------------------------------------- programmatic dependent launch
 // Every kernel is launched with programmatic stream serialisation: it may be
-// scheduled while the previous kernel on the stream is still finishing. Each
-// kernel therefore does only parameter-only set-up, calls pdl_trigger() (its
-// own dependents may start launching once all of its blocks have started),
-// then pdl_wait(), which returns when the previous kernel has completed and
-// its writes are visible, before it reads or writes any global memory.
+// scheduled while the previous kernel on the stream is still running.
+// pdl_wait() returns when the previous kernel has completed and its writes are
+// visible; pdl_trigger() lets the next kernel start launching once every block
+// of this one has called it (or exited). The rules every kernel here keeps:
+//  - every block calls pdl_wait() before it exits, so a kernel completes only
+//    after the kernel before it has, and completion follows stream order;
+//  - global memory that an earlier kernel may still write, or still read, is
+//    touched only after pdl_wait(). The exceptions read inputs that no kernel
+//    of this library writes, and each argues why at the kernel: the router
+//    weight copy (transpose_router_w_kernel) and the expert GEMMs launched
+//    with GroupedGemm::early;
+//  - the kernels those exceptions rely on call pdl_trigger() only after
+//    pdl_wait(): the selection kernels (the router GEMM before them is then
+//    complete), the permute and gather kernels (the capacity or selection
+//    kernel that wrote the offsets is then complete) and the tcgen05 GEMM.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

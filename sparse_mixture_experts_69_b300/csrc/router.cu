@@ -15,11 +15,15 @@ namespace moe {
 
 // ------------------------------------------------------------------ transpose
 // WgT[n, i] = Wg[i, n] for n < E; WgT[E + n, i] = Wnoise[i, n]. 32x32 tiles.
+// The router weights are inputs no kernel of this library writes, and the only
+// reader of WgT, the router GEMM, is complete whenever a later kernel launches
+// (the selection kernel after it signals its dependents only after its own
+// wait). So the copy runs before the wait for the preceding kernel, under that
+// kernel's tail; the wait at the end keeps the completion order.
 template <typename Tv>
 __global__ void transpose_router_w_kernel(int d, int E, const Tv* __restrict__ Wg,
                                           const Tv* __restrict__ Wn, Tv* __restrict__ wgT) {
     pdl_trigger();
-    pdl_wait();
     __shared__ Tv tile[32][33];
     const Tv* src = blockIdx.z == 0 ? Wg : Wn;
     const int i0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
@@ -33,6 +37,7 @@ __global__ void transpose_router_w_kernel(int d, int E, const Tv* __restrict__ W
         int n = n0 + r, i = i0 + threadIdx.x;
         if (i < d && n < E) dst[(size_t)n * d + i] = tile[threadIdx.x][r];
     }
+    pdl_wait();
 }
 
 cudaError_t launch_transpose_router_w(const Shape& s, const void* Wg, const void* Wnoise,
@@ -126,17 +131,49 @@ struct SelectArgs {
     int* status;
 };
 
+// softplus(u) = log(1 + e^u) = max(u, 0) + log(1 + e^-|u|), with the fast
+// exponential and logarithm (a few ulp: far inside the 1e-4 relative tolerance
+// the probabilities are held to).
 __device__ __forceinline__ float softplus_f(float u) {
-    return fmaxf(u, 0.f) + log1pf(expf(-fabsf(u)));
+    return fmaxf(u, 0.f) + __logf(1.f + __expf(-fabsf(u)));
 }
 
-// One token by one warp; lane l holds experts l, l+32, ... (EPL per lane).
-// On return pr[] holds this lane's probabilities, and lanes j < nc hold the
-// j-th candidate (my_id) and its gate (my_w): p_j over the sum of p of the
-// first k candidates (renorm), else p_j.
+// One token's inputs for the lanes of a warp: lane l holds experts l, l+32, ...
 template <int EPL>
-__device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (&pr)[EPL],
-                                             int& my_id, float& my_w) {
+struct TokenRegs {
+    float z[EPL];    // logits (from_scores: selection scores)
+    float zn[EPL];   // noise logits x.Wnoise (from_scores: probabilities)
+    float eps[EPL];  // standard-normal noise
+};
+
+template <int EPL>
+__device__ __forceinline__ void load_token(const SelectArgs& a, int t, TokenRegs<EPL>& r) {
+    const int lane = threadIdx.x & 31;
+    const size_t row = (size_t)t * a.E;
+    const bool noisy = a.zn && a.noise;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        const bool in = e < a.E;
+        r.eps[i] = 0.f;
+        if (a.from_scores) {
+            r.z[i] = in ? a.sel_in[row + e] : 0.f;
+            r.zn[i] = in ? a.probs_in[row + e] : 0.f;
+        } else {
+            r.z[i] = in ? a.logits[row + e] : 0.f;
+            r.zn[i] = in && noisy ? a.zn[row + e] : 0.f;
+            if (in && noisy) r.eps[i] = a.noise[row + e];
+        }
+    }
+}
+
+// Selection for token t from its loaded inputs. On return pr[] holds this
+// lane's probabilities, and lanes j < nc hold the j-th candidate (my_id) and
+// its gate (my_w): p_j over the sum of p of the first k candidates (renorm),
+// else p_j.
+template <int EPL>
+__device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const TokenRegs<EPL>& r,
+                                            float (&pr)[EPL], int& my_id, float& my_w) {
     const int lane = threadIdx.x & 31;
     const int E = a.E;
     const size_t row = (size_t)t * E;
@@ -145,21 +182,22 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (
     if (a.from_scores) {
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            int e = lane + 32 * i;
-            sc[i] = e < E ? a.sel_in[row + e] : -FLT_MAX;
-            pr[i] = e < E ? a.probs_in[row + e] : 0.f;
+            const int e = lane + 32 * i;
+            sc[i] = e < E ? r.z[i] : -FLT_MAX;
+            pr[i] = e < E ? r.zn[i] : 0.f;
             if (e < E && !isfinite(sc[i])) nonfinite = true;
         }
     } else {
+        const bool noisy = a.zn && a.noise;
         float H[EPL];
         float m = -FLT_MAX;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            int e = lane + 32 * i;
+            const int e = lane + 32 * i;
             float h = -FLT_MAX;
             if (e < E) {
-                h = a.logits[row + e];
-                if (a.zn && a.noise) h = h + a.noise[row + e] * softplus_f(a.zn[row + e]);
+                h = r.z[i];
+                if (noisy) h = h + r.eps[i] * softplus_f(r.zn[i]);
                 if (!isfinite(h)) nonfinite = true;
                 m = fmaxf(m, h);
             }
@@ -169,16 +207,17 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (
         float part = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            int e = lane + 32 * i;
-            pr[i] = e < E ? expf(H[i] - m) : 0.f;
+            const int e = lane + 32 * i;
+            pr[i] = e < E ? __expf(H[i] - m) : 0.f;
             part += pr[i];
         }
-        const float sum = warp_sum(part);
+        // the largest term is e^0 = 1, so the sum is at least 1
+        const float inv = 1.f / warp_sum(part);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            int e = lane + 32 * i;
+            const int e = lane + 32 * i;
             if (e < E) {
-                pr[i] = pr[i] / sum;
+                pr[i] = pr[i] * inv;
                 a.probs[row + e] = pr[i];
                 sc[i] = a.bias ? pr[i] + a.bias[e] : H[i];
                 if (a.sel) a.sel[row + e] = sc[i];
@@ -198,7 +237,7 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (
         int be = INT_MAX;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            int e = lane + 32 * i;
+            const int e = lane + 32 * i;
             if (e < E && !((taken >> i) & 1u) && (be == INT_MAX || sc[i] > bv)) {
                 bv = sc[i];
                 be = e;
@@ -206,8 +245,8 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
             if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
                 bv = ov;
                 be = oe;
@@ -234,18 +273,29 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, float (
     }
 }
 
-// Standalone selection: one warp per token.
+// One token per warp: at the token counts of a layer call nearly the whole
+// grid is resident at once, so the selection takes about one token's latency
+// chain (giving a warp several tokens made that chain several times longer).
+constexpr int kSelWarps = 8;
+
+// Standalone selection.
 template <int EPL>
-__global__ void __launch_bounds__(256) router_select_kernel(SelectArgs a) {
-    pdl_trigger();
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= a.T) return;
+__global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(SelectArgs a) {
+    // dependents launch after this wait: the router GEMM before this kernel is
+    // then complete, so the next router-weight copy may overwrite WgT
     pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    TokenRegs<EPL> r;
+    load_token<EPL>(a, t, r);
     float pr[EPL];
     int id;
     float w;
-    select_token<EPL>(a, t, pr, id, w);
+    select_regs<EPL>(a, t, r, pr, id, w);
 }
+
+static int sel_blocks(int T) { return (T + kSelWarps - 1) / kSelWarps; }
 
 cudaError_t launch_router_select(const Shape& s, const float* logits, const float* zn,
                                  const float* noise, const float* bias, float* probs,
@@ -258,62 +308,59 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
     a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
     a.sel_in = sel_in; a.probs_in = probs_in;
     a.probs = probs; a.sel = sel; a.ids = ids; a.w = w; a.status = status;
-    const int warps = 8;
-    dim3 grid((s.T + warps - 1) / warps), block(32 * warps);
-    if (s.E <= 32) return launch_k(router_select_kernel<1>, grid, block, 0, st, a);
-    if (s.E <= 64) return launch_k(router_select_kernel<2>, grid, block, 0, st, a);
-    if (s.E <= 128) return launch_k(router_select_kernel<4>, grid, block, 0, st, a);
-    if (s.E <= 256) return launch_k(router_select_kernel<8>, grid, block, 0, st, a);
-    if (s.E <= 512) return launch_k(router_select_kernel<16>, grid, block, 0, st, a);
-    return launch_k(router_select_kernel<32>, grid, block, 0, st, a);
+#define MOE_SEL(EPL)                                                                       \
+    return launch_k(router_select_kernel<EPL>, dim3(sel_blocks(s.T)),                \
+                    dim3(32 * kSelWarps), 0, st, a)
+    if (s.E <= 32) MOE_SEL(1);
+    if (s.E <= 64) MOE_SEL(2);
+    if (s.E <= 128) MOE_SEL(4);
+    if (s.E <= 256) MOE_SEL(8);
+    if (s.E <= 512) MOE_SEL(16);
+    MOE_SEL(32);
+#undef MOE_SEL
 }
 
 // Layer path: selection fused with the capacity histogram and the
-// load-balance statistics. One token per warp (the loop also covers grids
-// smaller than T/8); per expert each lane keeps a fixed-point sum of its
-// probabilities, and each chosen
-// (token, expert) adds 1 to blk_hist[e][token / kCapBlockTokens] (the scan
-// kernel zeroes those counters after reading them) and its gate to the
-// block's importance sum.
+// load-balance statistics, one token per warp. Per expert each lane keeps a
+// fixed-point sum of its probabilities, and each chosen (token, expert) adds 1
+// to blk_hist[e][token / kCapBlockTokens] (the scan kernel zeroes those
+// counters after reading them) and its gate to the block's importance sum.
 template <int EPL>
-__global__ void __launch_bounds__(512) router_select_fused_kernel(SelectArgs a, int32_t* blk_hist,
-                                                                  int nblk_cap, AuxAcc acc,
-                                                                  AuxOut out, int defer_final) {
-    pdl_trigger();
+__global__ void __launch_bounds__(32 * kSelWarps) router_select_fused_kernel(
+    SelectArgs a, int32_t* blk_hist, int nblk_cap, AuxAcc acc, AuxOut out, int defer_final) {
     pdl_wait();
+    pdl_trigger();  // after the wait, as in router_select_kernel
     extern __shared__ unsigned long long sm64[];
     const int E = a.E;
     unsigned long long* sP = sm64;
     unsigned long long* sI = sm64 + E;
     unsigned int* sC = reinterpret_cast<unsigned int*>(sm64 + 2 * E);
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
+    TokenRegs<EPL> r;
+    if (t < a.T) load_token<EPL>(a, t, r);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         sP[e] = 0;
         sI[e] = 0;
         sC[e] = 0;
     }
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const int warps = blockDim.x >> 5;
-    unsigned long long regP[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) regP[i] = 0;
-    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < a.T; t += gridDim.x * warps) {
+    if (t < a.T) {
         float pr[EPL];
         int id;
         float w;
-        select_token<EPL>(a, t, pr, id, w);
+        select_regs<EPL>(a, t, r, pr, id, w);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) regP[i] += to_fix(pr[i]);
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            const unsigned long long v = to_fix(pr[i]);
+            if (e < E && v) atomicAdd(&sP[e], v);
+        }
         if (lane < a.k) {
             atomicAdd(&sI[id], to_fix(w));
             atomicAdd(&sC[id], 1u);
             if (blk_hist) atomicAdd(&blk_hist[(size_t)id * nblk_cap + t / kCapBlockTokens], 1);
         }
-    }
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && regP[i]) atomicAdd(&sP[e], regP[i]);
     }
     __syncthreads();
     if (defer_final)  // a later kernel finalises the statistics
@@ -335,14 +382,12 @@ cudaError_t launch_router_select_fused(const Shape& s, const float* logits, cons
     const int nblk_cap = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
     const AuxAcc acc = aux_acc_at(acc_mem, s.E, kAuxGroups);
     const AuxOut out{f, P, I, out3, s.w_imp};
-    // one token per warp, 16 warps per block; blocks spread their statistics
-    // over kAuxGroups copies
-    const int warps = 16;
-    const int grid = (s.T + warps - 1) / warps;
+    // blocks spread their statistics over kAuxGroups copies
     const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int)) + 8;
-#define MOE_SEL_FUSED(EPL)                                                                  \
-    return launch_k(router_select_fused_kernel<EPL>, dim3(grid), dim3(32 * warps), smem, st, a, \
-                    blk_hist, nblk_cap, acc, out, defer_final ? 1 : 0)
+#define MOE_SEL_FUSED(EPL)                                                                 \
+    return launch_k(router_select_fused_kernel<EPL>, dim3(sel_blocks(s.T)),            \
+                    dim3(32 * kSelWarps), smem, st, a, blk_hist, nblk_cap, acc, out,        \
+                    defer_final ? 1 : 0)
     if (s.E <= 32) MOE_SEL_FUSED(1);
     if (s.E <= 64) MOE_SEL_FUSED(2);
     if (s.E <= 128) MOE_SEL_FUSED(4);

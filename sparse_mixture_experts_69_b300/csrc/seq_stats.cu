@@ -8,7 +8,7 @@
 // of aux_q over the non-empty sequences.
 //
 // Two launches after the accumulators are cleared:
-//   1. seq_accumulate_kernel: each warp walks 32 consecutive tokens of the
+//   1. seq_accumulate_kernel: each warp walks 8 consecutive tokens of the
 //      batch (so the whole batch is read once, by many CTAs) and sums the
 //      probabilities of each expert column while the tokens belong to one
 //      sequence, then adds the run to that sequence's accumulator. The sums
