@@ -76,13 +76,14 @@ struct Cfg {
     // M=128, N=BN, D=f32, A=B=bf16, both K-major
     static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-    // the router epilogue stages 32x32 fp32 blocks per epilogue warp (padded rows)
+    // epilogue staging per epilogue warp: the router's 32x32 fp32 block
+    // (padded rows), or 32 rows x 80 bytes of bf16 (store_rows32_bf16)
     static constexpr int STAGING_BYTES = 4 * 32 * 33 * 4;
-    // layout after the stages: barriers (256 B), tile table [G+1], then (router
-    // only) the staging area
-    static constexpr size_t smem_bytes(int G, bool staging) {
-        return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (size_t)(G + 1) +
-               (staging ? 16 + STAGING_BYTES : 0);
+    // layout after the stages: barriers (256 B), tile table [G+1], then the
+    // staging area
+    static constexpr size_t smem_bytes(int G) {
+        return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (size_t)(G + 1) + 16 +
+               STAGING_BYTES;
     }
 };
 
@@ -253,23 +254,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
-// Store NV (multiple of 8) bf16 values of one row; n = how many are in range.
-template <int NV>
-__device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float (&v)[NV], int n) {
-    if (n >= NV) {
+// Stores columns n0 .. n0+31 of the 32 rows of this warp's TMEM lanes; thread
+// `lane` holds its row in v[] and gives its output row index in dst_row (-1:
+// not stored). The values go through shared memory (stg: 32 rows x 80 bytes,
+// the 16 spare bytes spread the rows over the banks) so that each store
+// instruction writes 8 rows x 64 contiguous bytes rather than 32 rows x 16.
+// N is a multiple of 8, so a 16-byte piece lies wholly inside or outside.
+__device__ __forceinline__ void store_rows32_bf16(__nv_bfloat16* out, int N, int n0, int dst_row,
+                                                  const float (&v)[32], uint32_t* stg) {
+    const int lane = threadIdx.x & 31;
+    uint32_t* mine = stg + lane * 20;
 #pragma unroll
-        for (int q = 0; q < NV / 8; ++q) {
-            uint4 pk = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
-                                  pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                  pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                                  pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-            reinterpret_cast<uint4*>(dst)[q] = pk;
-        }
-    } else {
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(mine + 4 * q) =
+            make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                       pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    __syncwarp();
+    const int piece = lane & 3;
+    const int col = n0 + 8 * piece;
 #pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (i < n) dst[i] = __float2bfloat16_rn(v[i]);
+    for (int j = 0; j < 4; ++j) {
+        const int r = (lane >> 2) + 8 * j;
+        const int drow = __shfl_sync(0xffffffffu, dst_row, r);
+        const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 20 + 4 * piece);
+        if (drow >= 0 && col < N)
+            *reinterpret_cast<uint4*>(out + (size_t)drow * N + col) = val;
     }
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -541,16 +553,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(routed ? p.out0 : p.out1);
-                __nv_bfloat16* orow = out + (size_t)(gt.out_row + row) * p.N;
+                uint32_t* stg = reinterpret_cast<uint32_t*>(staging) + q * 32 * 20;
+                int dst_row = rv ? gt.out_row + row : -1;
                 if (EPI == EPI_GLU) {
 #pragma unroll 1
-                    for (int c = 0; c < 128; c += 16) {
-                        float g[16], u[16], v16[16];
+                    for (int c = 0; c < 128; c += 32) {
+                        float g[16], u[16], v[32];
                         tmem_ld16x2(taddr + c, taddr + 128 + c, g, u);
-                        const int n0 = gt.n_tile * 128 + c;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v16[i] = silu(g[i]) * u[i];
-                        if (rv && n0 < p.N) store_bf16_row<16>(orow + n0, v16, p.N - n0);
+                        for (int i = 0; i < 16; ++i) v[i] = silu(g[i]) * u[i];
+                        tmem_ld16x2(taddr + c + 16, taddr + 128 + c + 16, g, u);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[16 + i] = silu(g[i]) * u[i];
+                        const int n0 = gt.n_tile * 128 + c;
+                        if (n0 < p.N) store_rows32_bf16(out, p.N, n0, dst_row, v, stg);
                     }
                 } else {
                     const int act = p.glu ? -1 : p.act;
@@ -558,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (routed && p.scatter_rows) {
                         // top-1 combine: this row is token t's output, times its gate
                         const int t = rv ? p.scatter_rows[gt.out_row + row] : 0;
-                        orow = reinterpret_cast<__nv_bfloat16*>(p.scatter_out) + (size_t)t * p.N;
+                        out = reinterpret_cast<__nv_bfloat16*>(p.scatter_out);
+                        dst_row = rv ? t : -1;
                         scale = rv ? p.scatter_scale[t] : 0.f;
                     }
 #pragma unroll 1
@@ -566,10 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v[32];
                         tmem_ld32(taddr + c, v);
                         const int n0 = gt.n_tile * BN + c;
-                        if (rv && n0 < p.N) {
+                        if (n0 < p.N) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = act_apply(act, v[i]) * scale;
-                            store_bf16_row<32>(orow + n0, v, p.N - n0);
+                            store_rows32_bf16(out, p.N, n0, dst_row, v, stg);
                         }
                     }
                 }
@@ -636,7 +653,7 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     if (!make_map(&mB0, p.B0 ? p.B0 : p.B1, p.B0 ? brows0 : brows1, p.K, C::B_BOX_ROWS) ||
         !make_map(&mB1, p.B1 ? p.B1 : p.B0, p.B1 ? brows1 : brows0, p.K, C::B_BOX_ROWS))
         return cudaErrorInvalidValue;
-    const size_t smem = C::smem_bytes(G, EPI == EPI_ROUTER);
+    const size_t smem = C::smem_bytes(G);
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<BN, EPI>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

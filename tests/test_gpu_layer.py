@@ -165,3 +165,21 @@ def test_skewed_layer_mixes_heavy_and_light_experts(cuda_device, act, k):
     cap = oracle.capacity(ids, c.n_experts, c.T)
     y_ref = _oracle_y(wl, inp, list(range(c.T)), ids, w, cap["slot"])
     assert_maxabs(np32(o["y"]), y_ref, TOL_Y[c.dtype], "y")
+
+
+@pytest.mark.parametrize("T,E,k,cf,d,pad", [
+    (4097, 64, 1, 1.0, 128, 0),   # top-1 (the down GEMM writes y), partial last block
+    (1000, 256, 8, 1.0, 64, 0),   # top-8 over 256 experts, drops in every block
+    (300, 16, 2, 0.5, 64, 0),     # half the assignments dropped
+    (1001, 32, 2, 0.75, 64, 1),   # padded to capacity
+])
+def test_layer_token_order_capacity(cuda_device, T, E, k, cf, d, pad):
+    """Token-order capacity inside the layer (the selection kernel counts the
+    per-256-token histograms, the scan/slot kernel ranks each token), with
+    drops, a partial last block and padding: counts bit-exact and y on every
+    token against the oracle fed the GPU's routing."""
+    from gpu_helpers import layer_vs_oracle
+    wl = WORKLOADS["switch"].with_(T=T, d_model=d, n_experts=E, top_k=k, d_ff=128,
+                                    capacity_factor=cf, pad_to_capacity=pad)
+    o, _ = layer_vs_oracle(wl, cuda_device)
+    assert (o["slot"] < 0).any()
