@@ -119,9 +119,12 @@ static __device__ __forceinline__ void aux_publish(int E, const AuxAcc& acc,
 // aux = E / (T^2 k 2^32) * sum_e count_e * P_e (fixed point) is a sum of
 // positive terms. Each thread keeps its first expert's totals in registers,
 // so there is one round of loads when E <= nthreads.
+// Not inlined: it runs in one block, and inlined it would raise the register
+// count, and so lower the occupancy, of every kernel that calls it.
 template <typename Bar>
-static __device__ void aux_finalize(int T, int E, int k, const AuxAcc& acc, const AuxOut& out,
-                                    int tid, int nthreads, Bar bar) {
+static __device__ __noinline__ void aux_finalize(int T, int E, int k, const AuxAcc& acc,
+                                                 const AuxOut& out, int tid, int nthreads,
+                                                 Bar bar) {
     __shared__ long long s_n[32];
     __shared__ float s_a[32], s_b[32];
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
@@ -194,10 +197,12 @@ struct BlockBar {
 // Publish, then the last of the `participants` blocks (default: the whole
 // grid, counted with the ticket) finalises. Every thread of every
 // participating block calls this once the shared-memory totals are final.
-static __device__ void aux_publish_and_finalize(int T, int E, int k, AuxAcc acc, AuxOut out,
-                                                const unsigned long long* sP,
-                                                const unsigned long long* sI,
-                                                const unsigned int* sC, int participants = -1) {
+static __device__ __noinline__ void aux_publish_and_finalize(int T, int E, int k, AuxAcc acc,
+                                                             AuxOut out,
+                                                             const unsigned long long* sP,
+                                                             const unsigned long long* sI,
+                                                             const unsigned int* sC,
+                                                             int participants = -1) {
     __shared__ int is_last;
     aux_publish(E, acc, sP, sI, sC);
     __threadfence();

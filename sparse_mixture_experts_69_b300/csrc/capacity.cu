@@ -169,21 +169,48 @@ __global__ void __launch_bounds__(kCapBlockTokens) cap_scan_slot_kernel(
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int b = blockIdx.x;
     for (int i = threadIdx.x; i < W * E; i += blockDim.x) mask[i] = 0;
-    // per expert: base (earlier blocks) and total
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int32_t* row = blk_hist + (size_t)e * nblk;
-        int before = 0, total = 0;
-#pragma unroll 8
-        for (int q = 0; q < nblk; ++q) {
-            const int v = __ldcg(row + q);
-            total += v;
-            before += q < b ? v : 0;
+    // per expert: base (earlier blocks) and total. Warp w takes experts w, w+W,
+    // ... kE at a time, lane q block q (32 blocks a round), so the loads of
+    // all its experts are in flight together.
+    constexpr int kE = 8;
+    for (int e0 = warp; e0 < E; e0 += W * kE) {
+        int total[kE], before[kE];
+#pragma unroll
+        for (int i = 0; i < kE; ++i) total[i] = before[i] = 0;
+        for (int q0 = 0; q0 < nblk; q0 += 32) {
+            const int q = q0 + lane;
+            int v[kE];
+#pragma unroll
+            for (int i = 0; i < kE; ++i) {
+                const int e = e0 + i * W;
+                v[i] = (e < E && q < nblk) ? __ldcg(blk_hist + (size_t)e * nblk + q) : 0;
+            }
+#pragma unroll
+            for (int i = 0; i < kE; ++i) {
+                total[i] += v[i];
+                before[i] += q < b ? v[i] : 0;
+            }
         }
-        s_base[e] = before;
-        s_off[e] = total < C ? total : C;  // kept, scanned below
-        if (b == 0) {
-            counts[e] = total;
-            kept[e] = s_off[e];
+#pragma unroll
+        for (int i = 0; i < kE; ++i) {
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                total[i] += __shfl_xor_sync(0xffffffffu, total[i], o);
+                before[i] += __shfl_xor_sync(0xffffffffu, before[i], o);
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < kE; ++i) {
+                const int e = e0 + i * W;
+                if (e >= E) break;
+                s_base[e] = before[i];
+                s_off[e] = total[i] < C ? total[i] : C;  // kept, scanned below
+                if (b == 0) {
+                    counts[e] = total[i];
+                    kept[e] = s_off[e];
+                }
+            }
         }
     }
     __syncthreads();

@@ -40,6 +40,9 @@
 #ifndef MOE_TC_SMEM
 #define MOE_TC_SMEM (192 * 1024)  // shared memory for the pipeline stages
 #endif
+#ifndef MOE_TC_L2_HINTS
+#define MOE_TC_L2_HINTS 1  // L2 eviction policies (b_evict_first, out_l2_keep)
+#endif
 
 namespace moe {
 namespace tc {
@@ -144,6 +147,30 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
+}
+// As tma_load_2d, with an L2 eviction policy (createpolicy) for the lines read.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                 int x, int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_global_hint(void* dst, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -260,8 +287,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // the 16 spare bytes spread the rows over the banks) so that each store
 // instruction writes 8 rows x 64 contiguous bytes rather than 32 rows x 16.
 // N is a multiple of 8, so a 16-byte piece lies wholly inside or outside.
+// keep_l2: store with the evict-last policy `pol` (the output is read back
+// soon, by the next GEMM).
 __device__ __forceinline__ void store_rows32_bf16(__nv_bfloat16* out, int N, int n0, int dst_row,
-                                                  const float (&v)[32], uint32_t* stg) {
+                                                  const float (&v)[32], uint32_t* stg,
+                                                  bool keep_l2, uint64_t pol) {
     const int lane = threadIdx.x & 31;
     uint32_t* mine = stg + lane * 20;
 #pragma unroll
@@ -278,8 +308,13 @@ __device__ __forceinline__ void store_rows32_bf16(__nv_bfloat16* out, int N, int
         const int r = (lane >> 2) + 8 * j;
         const int drow = __shfl_sync(0xffffffffu, dst_row, r);
         const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 20 + 4 * piece);
-        if (drow >= 0 && col < N)
-            *reinterpret_cast<uint4*>(out + (size_t)drow * N + col) = val;
+        if (drow >= 0 && col < N) {
+            uint4* dst = reinterpret_cast<uint4*>(out + (size_t)drow * N + col);
+            if (keep_l2)
+                st_global_hint(dst, val, pol);
+            else
+                *dst = val;
+        }
     }
     __syncwarp();
 }
@@ -299,19 +334,27 @@ __device__ __forceinline__ void b_tile_rows(const GroupedGemm& p, const GroupTil
     }
 }
 // The B tile of k block kb into one ring stage.
-template <int BN>
+// WEF: the weights are read with the evict-first policy pol
+// (GroupedGemm::b_evict_first); otherwise with no cache hint at all.
+template <int BN, bool WEF>
 __device__ __forceinline__ void load_b_stage(uint8_t* sB_stage, const CUtensorMap* mb,
                                              uint64_t* bar, int kb,
-                                             const int (&brow)[Cfg<BN>::B_LOADS]) {
+                                             const int (&brow)[Cfg<BN>::B_LOADS], uint64_t pol) {
 #pragma unroll
     for (int hk = 0; hk < KH; ++hk)
 #pragma unroll
-        for (int h = 0; h < Cfg<BN>::B_LOADS; ++h)
-            tma_load_2d(sB_stage + hk * Cfg<BN>::B_HALF + h * Cfg<BN>::B_BOX_ROWS * 128, mb, bar,
-                        kb * BK + hk * BKH, brow[h]);
+        for (int h = 0; h < Cfg<BN>::B_LOADS; ++h) {
+            uint8_t* dst = sB_stage + hk * Cfg<BN>::B_HALF + h * Cfg<BN>::B_BOX_ROWS * 128;
+            if (WEF)
+                tma_load_2d_hint(dst, mb, bar, kb * BK + hk * BKH, brow[h], pol);
+            else
+                tma_load_2d(dst, mb, bar, kb * BK + hk * BKH, brow[h]);
+        }
 }
 
-template <int BN, int EPI>
+// WEF: weights evict-first in L2 (a separate instantiation: the hinted copy
+// form, even with the normal policy, slowed the launches with weight reuse).
+template <int BN, int EPI, bool WEF>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0,
                            const __grid_constant__ CUtensorMap tmA1,
@@ -381,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     // first ring stages: expected bytes and B tiles (A follows after the wait)
+    const uint64_t pol_w = WEF ? l2_evict_first_policy() : 0ull;
     int prefilled = 0;
     if (early && threadIdx.x == 0) {
         for (int tile = blockIdx.x; tile < total && prefilled < C::STAGES; tile += gridDim.x) {
@@ -392,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rot = MOE_TC_ROT ? tile % nkb : 0;
                 const int kb = kb0 + rot < nkb ? kb0 + rot : kb0 + rot - nkb;
                 mbar_arrive_expect_tx(&full[prefilled], C::STAGE_BYTES);
-                load_b_stage<BN>(sB + prefilled * C::B_BYTES, mb, &full[prefilled], kb, brow);
+                load_b_stage<BN, WEF>(sB + prefilled * C::B_BYTES, mb, &full[prefilled], kb, brow,
+                                 pol_w);
                 ++prefilled;
             }
         }
@@ -439,7 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int hk = 0; hk < KH; ++hk)
                         tma_load_2d(sA + stage * C::A_BYTES + hk * C::A_HALF, ma, &full[stage],
                                     kb * BK + hk * BKH, gt.a_row);
-                    if (fresh) load_b_stage<BN>(sB + stage * C::B_BYTES, mb, &full[stage], kb, brow);
+                    if (fresh)
+                        load_b_stage<BN, WEF>(sB + stage * C::B_BYTES, mb, &full[stage], kb, brow,
+                                         pol_w);
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -516,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int q = warp & 3;
         const int row = 32 * q + lane;
+        const uint64_t pol_o = l2_evict_last_policy();
         int local = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
             const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
@@ -554,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(routed ? p.out0 : p.out1);
                 uint32_t* stg = reinterpret_cast<uint32_t*>(staging) + q * 32 * 20;
+                const bool keep_l2 = MOE_TC_L2_HINTS && p.out_l2_keep;
                 int dst_row = rv ? gt.out_row + row : -1;
                 if (EPI == EPI_GLU) {
 #pragma unroll 1
@@ -566,7 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[16 + i] = silu(g[i]) * u[i];
                         const int n0 = gt.n_tile * 128 + c;
-                        if (n0 < p.N) store_rows32_bf16(out, p.N, n0, dst_row, v, stg);
+                        if (n0 < p.N)
+                            store_rows32_bf16(out, p.N, n0, dst_row, v, stg, keep_l2, pol_o);
                     }
                 } else {
                     const int act = p.glu ? -1 : p.act;
@@ -586,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (n0 < p.N) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = act_apply(act, v[i]) * scale;
-                            store_rows32_bf16(out, p.N, n0, dst_row, v, stg);
+                            store_rows32_bf16(out, p.N, n0, dst_row, v, stg, keep_l2, pol_o);
                         }
                     }
                 }
@@ -640,7 +690,7 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int b
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool WEF>
 static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     using C = Cfg<BN>;
     const GroupedGemm& p = a.p;
@@ -654,7 +704,7 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
         !make_map(&mB1, p.B1 ? p.B1 : p.B0, p.B1 ? brows1 : brows0, p.K, C::B_BOX_ROWS))
         return cudaErrorInvalidValue;
     const size_t smem = C::smem_bytes(G);
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<BN, EPI>,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<BN, EPI, WEF>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     // upper bound of the tile count, from host-known sizes
@@ -664,7 +714,7 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     if (p.E == 0) mt = (long long)p.S * ((p.T + BM - 1) / BM);
     const long long bound = std::max<long long>(1, mt * nt);
     const int grid = (int)std::min<long long>(bound, num_sms());
-    return launch_k(grouped_gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kThreads), smem, st, mA0,
+    return launch_k(grouped_gemm_tc_kernel<BN, EPI, WEF>, dim3(grid), dim3(kThreads), smem, st, mA0,
                     mA1, mB0, mB1, a);
 }
 
@@ -673,8 +723,12 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
 cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStream_t st) {
     tc::TcArgs a{};
     a.p = g;
-    if (g.glu) return tc::launch<256, tc::EPI_GLU>(a, st);
-    return tc::launch<MOE_TC_BN_ACT, tc::EPI_ACT>(a, st);
+    const bool wef = MOE_TC_L2_HINTS && g.b_evict_first;
+    if (g.glu)
+        return wef ? tc::launch<256, tc::EPI_GLU, true>(a, st)
+                   : tc::launch<256, tc::EPI_GLU, false>(a, st);
+    return wef ? tc::launch<MOE_TC_BN_ACT, tc::EPI_ACT, true>(a, st)
+               : tc::launch<MOE_TC_BN_ACT, tc::EPI_ACT, false>(a, st);
 }
 
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
@@ -712,10 +766,10 @@ cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const
     const int mt = (s.T + tc::BM - 1) / tc::BM;
     int bn = Nr <= 32 ? 32 : Nr <= 64 ? 64 : Nr <= 128 ? 128 : 256;
     while (bn > 32 && mt * ((Nr + bn - 1) / bn) < (3 * num_sms()) / 4) bn >>= 1;
-    if (bn == 32) return tc::launch<32, tc::EPI_ROUTER>(a, st);
-    if (bn == 64) return tc::launch<64, tc::EPI_ROUTER>(a, st);
-    if (bn == 128) return tc::launch<128, tc::EPI_ROUTER>(a, st);
-    return tc::launch<256, tc::EPI_ROUTER>(a, st);
+    if (bn == 32) return tc::launch<32, tc::EPI_ROUTER, false>(a, st);
+    if (bn == 64) return tc::launch<64, tc::EPI_ROUTER, false>(a, st);
+    if (bn == 128) return tc::launch<128, tc::EPI_ROUTER, false>(a, st);
+    return tc::launch<256, tc::EPI_ROUTER, false>(a, st);
 }
 
 }  // namespace moe

@@ -188,6 +188,13 @@ struct GroupedGemm {
     // which makes this hold for the down projection that follows an up
     // projection.
     int early;
+    // 1: the output is read back soon and fits in L2 (the up projection's h
+    // of a small layer): store it with an evict-last L2 policy (tcgen05 only)
+    int out_l2_keep;
+    // 1: every group has at most one row tile, so each weight tile is read
+    // once per launch: weights get an evict-first L2 policy and leave L2
+    // before the activations (tcgen05 only; set for T <= 128)
+    int b_evict_first;
 };
 cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream_t st);
 

@@ -325,8 +325,10 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
 // fixed-point sum of its probabilities, and each chosen (token, expert) adds 1
 // to blk_hist[e][token / kCapBlockTokens] (the scan kernel zeroes those
 // counters after reading them) and its gate to the block's importance sum.
+// For E <= 128, 32 registers a thread (eight blocks an SM) keep every warp of a
+// T = 8192 grid resident at once.
 template <int EPL>
-__global__ void __launch_bounds__(32 * kSelWarps) router_select_fused_kernel(
+__global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : 1) router_select_fused_kernel(
     SelectArgs a, int32_t* blk_hist, int nblk_cap, AuxAcc acc, AuxOut out, int defer_final) {
     pdl_wait();
     pdl_trigger();  // after the wait, as in router_select_kernel
