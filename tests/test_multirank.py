@@ -56,3 +56,21 @@ def test_reference_arm_prints_on_rank_zero_only():
                         "--steps", "1", "--warmup", "0"], env=env, capture_output=True,
                        text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_roofline_bound_follows_the_ridge():
+    """The Switch-shaped FFN (111 FLOP per byte) is HBM-bound; the
+    Mixtral-shaped one (thousands) is tensor-bound and, at milliseconds per
+    call, measured against the sustained bf16 rate."""
+    import bench
+    pk = {"hbm_gbs": 6490.5, "bf16_tflops": 1744.3, "bf16_tflops_sustained": 1392.1}
+    sw = bench.roofline_record(137e9, 1.235e9, 0.203, pk, "measured", 605e6)
+    assert sw["bound"] == "hbm" and sw["unit"] == "GB/s" and sw["traffic"] == 605e6
+    assert abs(sw["achieved"] - 1.235e9 / 0.203e-3 / 1e9) < 1e-6
+    assert abs(sw["frac"] - sw["achieved"] / 6490.5) < 1e-12
+    mx = bench.roofline_record(11.54e12, 3.6e9, 9.4, pk, "measured", None)
+    assert mx["bound"] == "tensor" and mx["unit"] == "TFLOP/s"
+    assert mx["peak"] == 1392.1 and mx["peak_kind"] == "measured sustained"
+    assert abs(mx["achieved"] - 11.54e12 / 9.4e-3 / 1e12) < 1e-9
+    short = bench.roofline_record(11.54e12 / 20, 3.6e9 / 20, 0.47, pk, "fallback", None)
+    assert short["peak"] == 1744.3 and short["peak_kind"] == "fallback burst"
