@@ -5,13 +5,16 @@
 // notes, load-balance section (a token beyond capacity is dropped) and the
 // grouped-GEMM section (tokens bucketed by expert, packed contiguously).
 //
-// Token-order priority without any inter-block waiting, in three launches:
-//   1. hist : per block of 256 tokens, assignments per expert
+// Token-order priority without any inter-block waiting, in three steps:
+//   1. hist : per block of 256 tokens, assignments per expert (cap_hist_kernel,
+//             or the layer's fused selection kernel)
 //   2. scan : per expert, exclusive prefix over blocks (block base); totals
 //             give counts, kept = min(counts, C), offsets = scan of kept
 //   3. slot : within a block, the rank of (t, e) among earlier tokens of the
 //             block that chose e, from per-warp lane bitmasks; slot = base + rank
-// then a permute copies each token's row to its kept rows.
+// Steps 2 and 3 are one launch (cap_scan_slot_kernel, every block reading the
+// histograms itself) up to kMaxFusedCapBlocks blocks, two beyond. Then a
+// permute copies each token's row to its kept rows.
 #include "moe_internal.cuh"
 
 namespace moe {
