@@ -81,3 +81,49 @@ def test_layer_in_a_cuda_graph(cuda_device, name):
     for key, got in (("y", y), ("ids", ids), ("w", w), ("counts", counts),
                      ("aux_vecs", aux_vecs), ("out3", out3)):
         assert torch.equal(got, ref[key]), key
+
+
+@pytest.mark.parametrize("name", ["switch", "deepseek"])
+def test_back_to_back_calls_with_different_router_weights(cuda_device, name):
+    """Two layer calls, then two moe_route calls, queued back to back on one
+    stream with one workspace and different router weights: the second
+    call's router-weight copy overwrites the workspace copy the first call's
+    router GEMM reads, so it must not start before that GEMM is done. Each
+    result equals a run of its own."""
+    wl = _small(name)
+    c = wl.cfg
+    dev = cuda_device
+    inp_a = make_inputs(wl, dev)
+    inp_b = dict(inp_a)
+    inp_b["Wg"] = (inp_a["Wg"].float().flip(1) * 1.5).to(inp_a["Wg"].dtype).contiguous()
+    ref_a, _ = run_layer(wl, inp_a, dev)
+    ref_b, _ = run_layer(wl, inp_b, dev)
+    ws = moe.workspace(c, dev)
+    outs = []
+    for inp in (inp_a, inp_b):
+        o = {k: torch.empty_like(v) for k, v in ref_a.items()}
+        moe.moe_layer_fwd(c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"],
+                          inp["logit_offset"], inp["sel_bias"], inp["W1"], inp["W2"], inp["W1s"],
+                          inp["W2s"], o["y"], o["ids"], o["w"], o["counts"], o["aux_vecs"],
+                          o["out3"], ws)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_error(c, ws) == 0
+    for got, ref in zip(outs, (ref_a, ref_b)):
+        for key in ref:
+            assert torch.equal(got[key], ref[key]), key
+    assert not torch.equal(outs[0]["ids"], outs[1]["ids"])
+
+    T, E, k = c.T, c.n_experts, c.top_k
+    routes = []
+    for inp in (inp_a, inp_b):
+        r = dict(logits=torch.empty((T, E), device=dev), probs=torch.empty((T, E), device=dev),
+                 ids=torch.empty((T, k), dtype=torch.int32, device=dev),
+                 w=torch.empty((T, k), device=dev))
+        moe.moe_route(c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"],
+                      inp["sel_bias"], r["logits"], r["probs"], None, r["ids"], r["w"], 0, ws)
+        routes.append(r)
+    torch.cuda.synchronize()
+    for r, ref in zip(routes, (ref_a, ref_b)):
+        assert torch.equal(r["ids"], ref["ids"])
+        assert torch.equal(r["w"], ref["w"])
