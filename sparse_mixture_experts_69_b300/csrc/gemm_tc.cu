@@ -79,14 +79,17 @@ struct Cfg {
     // M=128, N=BN, D=f32, A=B=bf16, both K-major
     static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    // the same with M=64, for tiles of at most 64 rows
+    static constexpr uint32_t IDESC64 = (1u << 4) | (1u << 7) | (1u << 10) |
+                                        ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(64 >> 4) << 24);
     // epilogue staging per epilogue warp: the router's 32x32 fp32 block
     // (padded rows), or 32 rows x 80 bytes of bf16 (store_rows32_bf16)
     static constexpr int STAGING_BYTES = 4 * 32 * 33 * 4;
-    // layout after the stages: barriers (256 B), tile table [G+1], then the
-    // staging area
+    // layout after the stages: barriers (256 B), tile table [G+1], group rows
+    // [G], then the staging area
     static constexpr size_t smem_bytes(int G) {
-        return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (size_t)(G + 1) + 16 +
-               STAGING_BYTES;
+        return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (size_t)(2 * G + 1) +
+               16 + STAGING_BYTES;
     }
 };
 
@@ -375,8 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* mt_start = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+    int* grows = mt_start + p.E + p.S + 1;  // [G] rows of each group
     float* staging = reinterpret_cast<float*>(
-        (reinterpret_cast<uintptr_t>(mt_start + p.E + p.S + 1) + 15) & ~(uintptr_t)15);
+        (reinterpret_cast<uintptr_t>(grows + p.E + p.S) + 15) & ~(uintptr_t)15);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.E + p.S;
     const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
@@ -395,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool early = p.early != 0;
     if (!early) pdl_wait();
     if (early)
-        build_tile_table<true>(p, BM, mt_start);
+        build_tile_table<true>(p, BM, mt_start, grows);
     else
-        build_tile_table<false>(p, BM, mt_start);
+        build_tile_table<false>(p, BM, mt_start, grows);
     __syncthreads();
     const int total = mt_start[G] * nt;
     // no work: leave before any allocation (CTA 0 stays when it owes the
@@ -521,6 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+                // expert tiles of at most 64 rows (few-token experts) run M=64 MMAs
+                const bool m64 =
+                    EPI != EPI_ROUTER && tile_rows(mt_start, grows, G, nt, BM, tile) <= 64;
+                const uint32_t idesc = m64 ? C::IDESC64 : C::IDESC;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kTimeoutNs)) {
                         ok = false;
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sdesc_sw128(smem_u32(sB + stage * C::B_BYTES + hk * C::B_HALF));
 #pragma unroll
                         for (int kk = 0; kk < BKH / 16; ++kk)
-                            umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, C::IDESC,
+                            umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
                                       (kb | hk | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit(&empty[stage]);
@@ -572,7 +580,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&tfull[b], tph, abort_flag, p.status, kTimeoutNs)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(b * BN) + ((uint32_t)(32 * q) << 16);
-            const bool rv = row < gt.rows;
+            // M=64 tiles: accumulator row r is in TMEM lane 32 (r / 16) + r % 16,
+            // so lanes 0..15 of each lane quadrant hold 16 rows and 16..31 none
+            const bool m64 = EPI != EPI_ROUTER && gt.rows <= 64;
+            const int trow = m64 ? (lane < 16 ? 16 * q + lane : BM) : row;
+            const bool rv = trow < gt.rows;
             const bool routed = gt.g < p.E;
             if (EPI == EPI_ROUTER) {
                 // thread = row; stage 32 rows x 32 columns, then each warp writes
@@ -603,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(routed ? p.out0 : p.out1);
                 uint32_t* stg = reinterpret_cast<uint32_t*>(staging) + q * 32 * 20;
                 const bool keep_l2 = MOE_TC_L2_HINTS && p.out_l2_keep;
-                int dst_row = rv ? gt.out_row + row : -1;
+                int dst_row = rv ? gt.out_row + trow : -1;
                 if (EPI == EPI_GLU) {
 #pragma unroll 1
                     for (int c = 0; c < 128; c += 32) {
@@ -623,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float scale = 1.f;
                     if (routed && p.scatter_rows) {
                         // top-1 combine: this row is token t's output, times its gate
-                        const int t = rv ? p.scatter_rows[gt.out_row + row] : 0;
+                        const int t = rv ? p.scatter_rows[gt.out_row + trow] : 0;
                         out = reinterpret_cast<__nv_bfloat16*>(p.scatter_out);
                         dst_row = rv ? t : -1;
                         scale = rv ? p.scatter_scale[t] : 0.f;

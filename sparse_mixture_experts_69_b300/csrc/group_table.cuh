@@ -46,9 +46,11 @@ __device__ __forceinline__ int group_rows(const GroupedGemm& p, int g, int* a_ro
     return p.T;
 }
 
-// Warp 0 of the block fills mt_start[0..G] (row-tile prefix). Caller syncs.
+// Warp 0 of the block fills mt_start[0..G] (row-tile prefix) and, if grows is
+// not NULL, grows[g] = rows of group g. Caller syncs.
 template <bool L2 = false>
-__device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, int* mt_start) {
+__device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, int* mt_start,
+                                                 int* grows = nullptr) {
     if (threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
     const int G = p.E + p.S;
@@ -61,6 +63,7 @@ __device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, i
             int ar, orow;
             int M = group_rows<L2>(p, g, &ar, &orow, &bad);
             mt = (M + BM - 1) / BM;
+            if (grows) grows[g] = M;
         }
         int incl = mt;
 #pragma unroll
@@ -73,6 +76,20 @@ __device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, i
     }
     if (lane == 0) mt_start[G] = running;
     if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DEV_BAD_ARG);
+}
+
+// Valid rows of tile `tile` (at most BM) from the shared-memory tables alone.
+__device__ __forceinline__ int tile_rows(const int* mt_start, const int* grows, int G, int nt,
+                                         int BM, int tile) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (mt_start[mid] * nt <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    const int mt = mt_start[lo + 1] - mt_start[lo];
+    const int m0 = ((tile - mt_start[lo] * nt) % mt) * BM;
+    return min(BM, grows[lo] - m0);
 }
 
 template <bool L2 = false>
