@@ -172,9 +172,15 @@ class ClockSampler:
 
 
 def source_hash():
+    """Hash of the grouped-GEMM kernel code (comments and blank lines left
+    out), which names the kernel version an ncu traffic figure was taken on."""
     h = hashlib.sha256()
     for f in ("gemm_tc.cu", "group_table.cuh"):
-        h.update(open(os.path.join(ROOT, "sparse_mixture_experts_69_b300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "sparse_mixture_experts_69_b300", "csrc", f)).read()
+        for line in text.splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

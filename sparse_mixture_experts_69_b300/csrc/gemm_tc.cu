@@ -11,13 +11,17 @@
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per stage,
 //               128-byte swizzle, completion on a per-stage mbarrier
 //   warp 1      owns the tensor-memory allocation; lane 0 issues tcgen05.mma
-//               (M=128, N=BN, K=16 per instruction) and commits stage releases
-//               and finished accumulators to mbarriers
+//               (M=128, or M=64 for tiles of at most 64 rows; N=BN, K=16 per
+//               instruction) and commits stage releases and finished
+//               accumulators to mbarriers
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//               32*(w%4) .. +31 = tile rows), activation, bf16 pack, global store
+//               32*(w%4) .. +31 = tile rows), activation, bf16 pack, stores
+//               through a shared-memory tile
 // Two accumulator buffers in TMEM let the epilogue of one tile overlap the
-// main loop of the next. Every mbarrier wait is bounded in time; on expiry the
-// CTA records DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+// main loop of the next. Launched early (GroupedGemm::early), a CTA builds its
+// tile table and issues its first B tiles before waiting for the preceding
+// kernel. Every mbarrier wait is bounded in time; on expiry the CTA records
+// DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <algorithm>
 #include <mutex>
 
