@@ -14,9 +14,9 @@ e2e        the same call with the step's inputs copied from pinned host memory
 roofline   the grouped expert GEMM (the dominant kernel): algorithmic bytes
            (weights of touched experts + activations in/out) per launch over its
            CUDA-event duration, against the measured HBM copy bandwidth; or, when
-           its FLOPs per byte are above the ridge of the measured peaks (the
-           Mixtral- and DeepSeek-shaped layers), its TFLOP/s against the
-           measured bf16 rate
+           its FLOPs at the measured bf16 rate take longer than its bytes at the
+           HBM rate (the Mixtral- and DeepSeek-shaped layers), its TFLOP/s
+           against that bf16 rate
 """
 from __future__ import annotations
 
@@ -81,22 +81,22 @@ def peaks():
 
 def roofline_record(flops, ffn_bytes, ffn_ms, pk, pk_kind, traffic):
     """The JSON roofline object of the expert FFN (two grouped-GEMM launches of
-    flops and ffn_bytes in total, ffn_ms per call). The bound is decided by the
-    FFN's FLOPs per algorithmic byte against the ridge of the measured peaks. A
-    tensor-bound FFN of a millisecond or more per call, timed back to back,
-    runs under the power cap: its peak is the sustained bf16 rate, else the
-    burst rate."""
+    flops and ffn_bytes in total, ffn_ms per call). The bound is the larger of
+    the two floors: the algorithmic bytes at the measured HBM rate, or the
+    FLOPs at the measured bf16 rate. An FFN of a millisecond or more per call,
+    timed back to back, runs under the power cap, so its bf16 rate is the
+    sustained one, else the burst one."""
     hbm = pk["hbm_gbs"]
     achieved_gbs = ffn_bytes / (ffn_ms / 1e3) / 1e9
     tflops = flops / (ffn_ms / 1e3) / 1e12
     kernel = "grouped_gemm_tc_kernel (expert FFN: up + down launches)"
-    if flops / ffn_bytes < pk["bf16_tflops"] * 1e12 / (hbm * 1e9):
+    sustained = ffn_ms >= 1.0
+    peak_t = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
+    if ffn_bytes / (hbm * 1e9) >= flops / (peak_t * 1e12):
         return {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": achieved_gbs / hbm, "traffic": traffic, "kernel": kernel,
                 "algorithmic_bytes_per_launch": ffn_bytes / 2, "peak_kind": pk_kind,
                 "tflops": tflops, "tflops_frac_of_bf16_peak": tflops / pk["bf16_tflops"]}
-    sustained = ffn_ms >= 1.0
-    peak_t = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
     return {"bound": "tensor", "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
             "frac": tflops / peak_t, "traffic": traffic, "kernel": kernel,
             "algorithmic_flops_per_launch": flops / 2,

@@ -59,9 +59,9 @@ def test_reference_arm_prints_on_rank_zero_only():
 
 
 def test_roofline_bound_follows_the_ridge():
-    """The Switch-shaped FFN (111 FLOP per byte) is HBM-bound; the
-    Mixtral-shaped one (thousands) is tensor-bound and, at milliseconds per
-    call, measured against the sustained bf16 rate."""
+    """The Switch-shaped FFN (111 FLOP per byte) is HBM-bound; the Mixtral-
+    and DeepSeek-shaped ones are tensor-bound and, at milliseconds per call,
+    measured against the sustained bf16 rate."""
     import bench
     pk = {"hbm_gbs": 6490.5, "bf16_tflops": 1744.3, "bf16_tflops_sustained": 1392.1}
     sw = bench.roofline_record(137e9, 1.235e9, 0.203, pk, "measured", 605e6)
@@ -74,3 +74,7 @@ def test_roofline_bound_follows_the_ridge():
     assert abs(mx["achieved"] - 11.54e12 / 9.4e-3 / 1e12) < 1e-9
     short = bench.roofline_record(11.54e12 / 20, 3.6e9 / 20, 0.47, pk, "fallback", None)
     assert short["peak"] == 1744.3 and short["peak_kind"] == "fallback burst"
+    # DeepSeek-shaped: 256 FLOP per byte, below the burst ridge (269) but above
+    # the sustained one (214); at milliseconds per call the FLOPs bind
+    ds = bench.roofline_record(6.49e12, 25.3e9, 7.37, pk, "measured", None)
+    assert ds["bound"] == "tensor" and ds["peak"] == 1392.1
