@@ -67,6 +67,8 @@ def _load():
             "oracle_expert_choice": (None, [_I, _I, _I, _P, _P, _P, _P]),
             "oracle_combine_expert_choice": (None, [_I, _I, _I, _I, _P, _P, _P, _P, _I, _P]),
             "oracle_seq_aux_stats": (None, [_I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
+            "oracle_philox4x32_10": (None, [_P, _P, _P]),
+            "oracle_draw_noise": (None, [_I, _I, ctypes.c_uint64, ctypes.c_uint64, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -320,3 +322,21 @@ def seq_aux_stats(p, ids, k: int, seq_offsets):
     _load().oracle_seq_aux_stats(E, int(k), stride, _ptr(p), _ptr(ids), n_seq, _ptr(so),
                                  _ptr(f), _ptr(P), _ptr(aux), ctypes.byref(mean))
     return dict(f=f[:n_seq], P=P[:n_seq], aux=aux[:n_seq], mean=mean.value)
+
+
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 block: four 32-bit counter words and two key words in,
+    four 32-bit words out (oracle.c cites the published definition)."""
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def draw_noise(T: int, E: int, seed: int, counter: int = 0) -> np.ndarray:
+    """The router's StandardNormal() draws eps[t, e] for the stream (seed,
+    counter): Philox4x32-10 and the Box-Muller transform (oracle.c)."""
+    eps = np.zeros((T, E), dtype=np.float64)
+    _load().oracle_draw_noise(T, E, seed & (2**64 - 1), counter & (2**64 - 1), _ptr(eps))
+    return eps

@@ -40,6 +40,9 @@
  *               (routing can be reversed: experts select tokens).
  *   sequence    heavensheep.xyz notes, Training: the same balance
  *   statistics  statistics taken inside each sequence instead of the batch.
+ *   noise       the router's StandardNormal() draws, when drawn rather than
+ *               passed in: Philox4x32-10 and the Box-Muller transform (the
+ *               generator is not the pages'; see oracle_philox4x32_10).
  *
  * Inputs arrive as float (bf16 values are widened exactly by the caller).
  * Rounding of intermediates to the storage dtype is optional (round_dtype:
@@ -83,6 +86,63 @@ double oracle_round(double v, int round_dtype) { return round_to(v, round_dtype)
 /* ----------------------------------------------------------------- scalars */
 
 double oracle_softplus(double u) { return fmax(u, 0.0) + log1p(exp(-fabs(u))); }
+
+/* ------------------------------------------------------------ router noise */
+
+/* The StandardNormal() draws of the noisy router ("MoE notes", KeepTopK), when
+ * they are drawn rather than passed in. The pages name no generator; this is
+ * the counter-based Philox4x32-10 of Salmon, Moraes, Dror and Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3" (SC 2011): ten rounds, each two 32x32
+ * -> 64-bit products with the multipliers 0xD2511F53 and 0xCD9E8D57, the high
+ * halves xored with the other counter words and the key, the key bumped by
+ * 0x9E3779B9 and 0xBB67AE85 between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        const uint32_t n0 = hi1 ^ c1 ^ k0;
+        const uint32_t n1 = lo1;
+        const uint32_t n2 = hi0 ^ c3 ^ k1;
+        const uint32_t n3 = lo0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+        if (round < 9) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* eps[t,e] for the stream (seed, counter): the Philox block with counter words
+ * (e, t, counter low, counter high) and key (seed low, seed high) gives r0, r1;
+ * their top 24 bits make u1 = (r0 >> 8) + 1 over 2^24 in (0, 1] and u2 =
+ * (r1 >> 8) over 2^24 in [0, 1); Box and Muller (1958) turn them into the
+ * standard normal sqrt(-2 ln u1) cos(2 pi u2). */
+static const double kPi = 3.14159265358979323846;
+
+void oracle_draw_noise(int T, int E, uint64_t seed, uint64_t counter, double* eps) {
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            const uint32_t ctr[4] = {(uint32_t)e, (uint32_t)t, (uint32_t)counter,
+                                     (uint32_t)(counter >> 32)};
+            uint32_t r[4];
+            oracle_philox4x32_10(ctr, key, r);
+            const double u1 = (double)((r[0] >> 8) + 1u) / 16777216.0;
+            const double u2 = (double)(r[1] >> 8) / 16777216.0;
+            eps[(size_t)t * E + e] = sqrt(-2.0 * log(u1)) * cos(2.0 * kPi * u2);
+        }
+}
 
 static double act_relu(double u) { return u > 0.0 ? u : 0.0; }
 /* GELU, exact form u * Phi(u); Phi written with erfc to avoid cancellation for u << 0 */
