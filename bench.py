@@ -110,7 +110,7 @@ def workload_desc(wl):
     s = (f"{wl.name}: T={c.T} d={c.d_model} E={c.n_experts} k={c.top_k} F={c.d_ff} {act}"
          f" shared={c.n_shared} cf={c.capacity_factor:g}")
     if wl.noisy:
-        s += " noisy-KeepTopK"
+        s += " noisy-KeepTopK" + (" (noise drawn on the device)" if c.noise_draw else "")
     if wl.zipf_s:
         s += f" zipf-offset={wl.zipf_s}"
     if wl.sel_bias:
@@ -219,6 +219,10 @@ class OracleInputs:
             self.inp, self.dev = inp, inp["x"].device
         self.small = {k: (None if v is None or k in ("W1", "W2", "W1s", "W2s") else v.cpu())
                       for k, v in self.inp.items()}
+        if wl.noisy and self.small["noise"] is None:  # the library draws it: the oracle's draws
+            import oracle
+            eps = oracle.draw_noise(c.T, c.n_experts, c.noise_seed, c.noise_counter)
+            self.small["noise"] = torch.from_numpy(eps.astype(np.float32))
         self.cache = {}
 
     def _get(self, key, tid, e, shape):

@@ -108,6 +108,12 @@ typedef struct {
                                 ones zero, and the expert GEMMs run on all
                                 E*C rows (fixed shapes, wasted FLOPs)          */
     int32_t routing;         /* moe_routing                                    */
+    /* Noisy router draws ("MoE notes", KeepTopK: StandardNormal()). 0: the
+     * caller passes them as the noise tensor. 1: the library draws eps[t,e]
+     * itself, as moe_draw_noise does, and the noise pointer must be NULL.   */
+    int32_t noise_draw;
+    uint64_t noise_seed;     /* generator key (noise_draw = 1)                 */
+    uint64_t noise_counter;  /* stream number, e.g. the training step          */
 } moe_config;
 
 /* Terms used below: n_cand = top_k + reroute candidates per token. R_max =
@@ -131,12 +137,25 @@ MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 MOE_API moe_status moe_workspace_reset(const moe_config* cfg, void* ws, size_t ws_bytes,
                                        moe_stream_t stream);
 
+/* The noisy router's standard-normal draws for (noise_seed, noise_counter),
+ * the same values the layer and moe_route use with noise_draw = 1. The pages
+ * name no generator: eps[t,e] comes from the counter-based Philox4x32-10
+ * (Salmon, Moraes, Dror and Shaw, SC 2011) with counter words (e, t,
+ * noise_counter low, high) and key (noise_seed low, high); of its first two
+ * output words r0, r1, u1 = ((r0 >> 8) + 1) / 2^24 and u2 = (r1 >> 8) / 2^24,
+ * and eps = sqrt(-2 ln u1) cos(2 pi u2) (Box and Muller, 1958), in float32.
+ *   noise  out  [T,E] float32
+ * Device-ordered on the stream; no workspace. */
+MOE_API moe_status moe_draw_noise(const moe_config* cfg, float* noise, moe_stream_t stream);
+
 /* Router ("MoE notes", Expert selection + KeepTopK; heavensheep.xyz softmax
  * numerics; ld246.com Q3 selection bias).
  *   x            [T,d] dtype
  *   Wg           [d,E] dtype
  *   Wnoise       [d,E] dtype or NULL   noisy router: H = z + noise*softplus(x.Wnoise)
  *   noise        [T,E] float32 or NULL  standard-normal draws, supplied by the caller
+ *                                       (NULL with noise_draw = 1: drawn in the
+ *                                       selection kernel, see moe_draw_noise)
  *   logit_offset [E] float32 or NULL    added to the logits
  *   sel_bias     [E] float32 or NULL    added to softmax p for the top-k choice only
  *   logits  out  [T,E] float32          z = x.Wg (+ offset), fp32 accumulation

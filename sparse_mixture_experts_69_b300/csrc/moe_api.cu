@@ -141,7 +141,18 @@ moe_status make_shape(const moe_config* c, Shape* s) {
     s->routing = c->routing;
     s->w_imp = c->importance_weight;
     s->esize = c->dtype == MOE_BF16 ? 2 : 4;
+    if (c->noise_draw != 0 && c->noise_draw != 1) return MOE_ERR_INVALID_ARG;
+    s->noise_draw = c->noise_draw;
+    s->noise_seed = c->noise_seed;
+    s->noise_counter = c->noise_counter;
     return MOE_OK;
+}
+
+// Noise arguments of the router: with Wnoise, the draws are either passed in
+// (noise) or drawn (noise_draw = 1, noise NULL); without Wnoise neither.
+bool noise_args_ok(const Shape& s, const void* Wnoise, const float* noise) {
+    if (!Wnoise) return noise == nullptr;
+    return s.noise_draw ? noise == nullptr : noise != nullptr;
 }
 
 moe_status check_ws(const Shape& s, void* ws, size_t ws_bytes, WsLayout* L) {
@@ -391,7 +402,7 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* W
         return MOE_OK;
     }
     if (!x || !Wg || !logits) return MOE_ERR_INVALID_ARG;
-    if ((Wnoise == nullptr) != (noise == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (!noise_args_ok(s, Wnoise, noise)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(Wg) || (Wnoise && !aligned16(Wnoise)))
         return MOE_ERR_UNSUPPORTED;
     return route_impl(s, L, ws, x, Wg, Wnoise, noise, logit_offset, sel_bias, logits, probs,
@@ -486,7 +497,7 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
     MOE_TRY(check_ws(s, ws, ws_bytes, &L));
     cudaStream_t st = (cudaStream_t)stream;
     if (!x || !Wg || !W1 || !W2 || !y) return MOE_ERR_INVALID_ARG;
-    if ((Wnoise == nullptr) != (noise == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (!noise_args_ok(s, Wnoise, noise)) return MOE_ERR_INVALID_ARG;
     if (s.S > 0 && (!W1s || !W2s)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(Wg) || (Wnoise && !aligned16(Wnoise)) || !aligned16(W1) ||
         !aligned16(W2) || !aligned16(y) || (s.S > 0 && (!aligned16(W1s) || !aligned16(W2s))))
@@ -572,6 +583,14 @@ MOE_API moe_status moe_expert_choice_combine(const moe_config* cfg, const void* 
     if (!aligned16(yp) || !aligned16(y) || (ys && !aligned16(ys))) return MOE_ERR_UNSUPPORTED;
     MOE_CUDA(launch_expert_choice_combine(s, yp, tok_row, probs, s.S ? ys : nullptr, y,
                                           (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+MOE_API moe_status moe_draw_noise(const moe_config* cfg, float* noise, moe_stream_t stream) {
+    Shape s;
+    MOE_TRY(make_shape(cfg, &s));
+    if (!noise) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_draw_noise(s, noise, (cudaStream_t)stream));
     return MOE_OK;
 }
 

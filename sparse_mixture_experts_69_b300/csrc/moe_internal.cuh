@@ -41,6 +41,9 @@ struct Shape {
     int renorm;
     float w_imp;
     int esize;    // bytes per element of dtype
+    int noise_draw;                    // 1: the router draws its noise (moe_draw_noise)
+    unsigned long long noise_seed;     // generator key
+    unsigned long long noise_counter;  // stream number
 };
 
 // Workspace layout (byte offsets, each 256-aligned). One layout serves every
@@ -97,6 +100,9 @@ cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
                                     const float* offset, float* logits, float* zn, int* status,
                                     cudaStream_t st);
+// The router's standard-normal draws for (s.noise_seed, s.noise_counter), [T,E]
+cudaError_t launch_draw_noise(const Shape& s, float* noise, cudaStream_t st);
+
 // Noise, softmax, selection bias, top-k, gates
 cudaError_t launch_router_select(const Shape& s, const float* logits, const float* zn,
                                  const float* noise, const float* bias, float* probs,

@@ -121,6 +121,8 @@ struct SelectArgs {
     const float* logits;   // [T,E] z
     const float* zn;       // [T,E] x.Wnoise or NULL
     const float* noise;    // [T,E] or NULL
+    int draw;              // 1: noise drawn from (seed, ctr) instead of read
+    unsigned long long seed, ctr;
     const float* bias;     // [E] or NULL
     const float* sel_in;   // from_scores: [T,E]
     const float* probs_in; // from_scores: [T,E]
@@ -138,6 +140,52 @@ __device__ __forceinline__ float softplus_f(float u) {
     return fmaxf(u, 0.f) + __logf(1.f + __expf(-fabsf(u)));
 }
 
+// ------------------------------------------------------------- drawn noise
+// The noisy router's StandardNormal() draw eps[t,e] for the stream (seed, ctr):
+// the counter-based Philox4x32-10 (Salmon, Moraes, Dror and Shaw, SC 2011;
+// ten rounds of two 32x32 -> 64-bit products by 0xD2511F53 and 0xCD9E8D57,
+// key bumped by 0x9E3779B9 and 0xBB67AE85) with counter words (e, t, ctr low,
+// ctr high) and key (seed low, seed high); the top 24 bits of its first two
+// words give u1 in (0, 1] and u2 in [0, 1), and the Box-Muller transform
+// sqrt(-2 ln u1) cos(2 pi u2) the draw.
+__device__ __forceinline__ float draw_eps(unsigned long long seed, unsigned long long ctr, int t,
+                                          int e) {
+    uint32_t c0 = (uint32_t)e, c1 = (uint32_t)t, c2 = (uint32_t)ctr, c3 = (uint32_t)(ctr >> 32);
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    const float u1 = (float)((c0 >> 8) + 1u) * 0x1p-24f;  // exact: 24-bit integers
+    const float u2 = (float)(c1 >> 8) * 0x1p-24f;
+    return sqrtf(-2.f * logf(u1)) * cospif(2.f * u2);
+}
+
+// One thread per (t, e), row-major [T,E].
+__global__ void __launch_bounds__(256) draw_noise_kernel(int T, int E, unsigned long long seed,
+                                                         unsigned long long ctr,
+                                                         float* __restrict__ noise) {
+    pdl_trigger();
+    pdl_wait();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)T * E) return;
+    noise[i] = draw_eps(seed, ctr, (int)(i / E), (int)(i % E));
+}
+
+cudaError_t launch_draw_noise(const Shape& s, float* noise, cudaStream_t st) {
+    const long long n = (long long)s.T * s.E;
+    return launch_k(draw_noise_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, s.T,
+                    s.E, s.noise_seed, s.noise_counter, noise);
+}
+
 // One token's inputs for the lanes of a warp: lane l holds experts l, l+32, ...
 template <int EPL>
 struct TokenRegs {
@@ -150,7 +198,7 @@ template <int EPL>
 __device__ __forceinline__ void load_token(const SelectArgs& a, int t, TokenRegs<EPL>& r) {
     const int lane = threadIdx.x & 31;
     const size_t row = (size_t)t * a.E;
-    const bool noisy = a.zn && a.noise;
+    const bool noisy = a.zn && (a.noise || a.draw);
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
@@ -162,7 +210,8 @@ __device__ __forceinline__ void load_token(const SelectArgs& a, int t, TokenRegs
         } else {
             r.z[i] = in ? a.logits[row + e] : 0.f;
             r.zn[i] = in && noisy ? a.zn[row + e] : 0.f;
-            if (in && noisy) r.eps[i] = a.noise[row + e];
+            if (in && noisy)
+                r.eps[i] = a.draw ? draw_eps(a.seed, a.ctr, t, e) : a.noise[row + e];
         }
     }
 }
@@ -188,7 +237,7 @@ __device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const To
             if (e < E && !isfinite(sc[i])) nonfinite = true;
         }
     } else {
-        const bool noisy = a.zn && a.noise;
+        const bool noisy = a.zn && (a.noise || a.draw);
         float H[EPL];
         float m = -FLT_MAX;
 #pragma unroll
@@ -306,6 +355,7 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
     a.T = s.T; a.E = s.E; a.k = s.k; a.nc = s.nc; a.renorm = s.renorm;
     a.from_scores = from_scores;
     a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
+    a.draw = zn && !noise && s.noise_draw; a.seed = s.noise_seed; a.ctr = s.noise_counter;
     a.sel_in = sel_in; a.probs_in = probs_in;
     a.probs = probs; a.sel = sel; a.ids = ids; a.w = w; a.status = status;
 #define MOE_SEL(EPL)                                                                       \
@@ -379,6 +429,7 @@ cudaError_t launch_router_select_fused(const Shape& s, const float* logits, cons
     SelectArgs a;
     a.T = s.T; a.E = s.E; a.k = s.k; a.nc = s.nc; a.renorm = s.renorm; a.from_scores = 0;
     a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
+    a.draw = zn && !noise && s.noise_draw; a.seed = s.noise_seed; a.ctr = s.noise_counter;
     a.sel_in = nullptr; a.probs_in = nullptr;
     a.probs = probs; a.sel = nullptr; a.ids = ids; a.w = w; a.status = status;
     const int nblk_cap = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;

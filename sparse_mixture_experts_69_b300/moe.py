@@ -40,7 +40,8 @@ class moe_config(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
                 ("importance_weight", ctypes.c_float), ("reroute", ctypes.c_int32),
                 ("priority", ctypes.c_int32), ("pad_to_capacity", ctypes.c_int32),
-                ("routing", ctypes.c_int32)]
+                ("routing", ctypes.c_int32), ("noise_draw", ctypes.c_int32),
+                ("noise_seed", ctypes.c_uint64), ("noise_counter", ctypes.c_uint64)]
 
 
 @dataclass
@@ -61,12 +62,16 @@ class Config:
     priority: int = MOE_PRIORITY_TOKEN
     pad_to_capacity: int = 0
     routing: int = MOE_TOKEN_CHOICE
+    noise_draw: int = 0
+    noise_seed: int = 0
+    noise_counter: int = 0
 
     def c(self) -> moe_config:
         return moe_config(self.T, self.d_model, self.n_experts, self.top_k, self.d_ff,
                           self.n_shared, self.capacity_factor, self.renorm_topk, self.dtype,
                           self.act, self.importance_weight, self.reroute, self.priority,
-                          self.pad_to_capacity, self.routing)
+                          self.pad_to_capacity, self.routing, self.noise_draw,
+                          self.noise_seed & (2**64 - 1), self.noise_counter & (2**64 - 1))
 
     @property
     def n_cand(self) -> int:
@@ -102,6 +107,7 @@ _SIGS = {
     "moe_aux_stats_noalloc": (ctypes.c_int, [_CFG] + [_P] * 7 + [_P]),
     "moe_expert_choice_dispatch": (ctypes.c_int, [_CFG] + [_P] * 7 + [_P, ctypes.c_size_t, _P]),
     "moe_expert_choice_combine": (ctypes.c_int, [_CFG] + [_P] * 5 + [_P, ctypes.c_size_t, _P]),
+    "moe_draw_noise": (ctypes.c_int, [_CFG, _P, _P]),
     "moe_seq_aux_stats": (ctypes.c_int, [_CFG, _P, _P, _P, ctypes.c_int32] + [_P] * 4 +
                           [_P, ctypes.c_size_t, _P]),
 }
@@ -238,6 +244,12 @@ def moe_expert_choice_combine(cfg: Config, yp, tok_row, probs, ys, y, ws, stream
     _check(lib().moe_expert_choice_combine(ctypes.byref(cfg.c()), _p(yp), _p(tok_row),
                                            _p(probs), _p(ys), _p(y), _p(ws), ws.numel(),
                                            _s(stream)), "moe_expert_choice_combine")
+
+
+def moe_draw_noise(cfg: Config, noise, stream=None):
+    """The router's standard-normal draws for (cfg.noise_seed, cfg.noise_counter)
+    into noise [T,E] float32, as the layer draws them with noise_draw = 1."""
+    _check(lib().moe_draw_noise(ctypes.byref(cfg.c()), _p(noise), _s(stream)), "moe_draw_noise")
 
 
 def moe_seq_aux_stats(cfg: Config, probs, topk_ids, seq_offsets, n_seq: int, f_seq, P_seq,

@@ -6,7 +6,8 @@ DeepSeek-V3 fine-grained + shared, a decode batch); every value comes from
 part of the layer.
 
   tiny     T=256   d=128  E=8   k=2 F=256   GELU,   cf=1.25 (C=40), fp32
-  switch   T=8192  d=1024 E=64  k=1 F=4096  ReLU,   cf=1.0 (C=128), noisy KeepTopK, bf16
+  switch   T=8192  d=1024 E=64  k=1 F=4096  ReLU,   cf=1.0 (C=128), noisy KeepTopK
+           (noise drawn in the selection kernel), bf16
   mixtral  T=16384 d=4096 E=8   k=2 F=14336 SwiGLU, dropless, Zipf(1.2) logit offset, bf16
   deepseek T=8192  d=7168 E=256 k=8 F=2048  SwiGLU, 1 shared, dropless, selection bias
            U(-0.1,0.1), one bias update at rate 1e-3, bf16
@@ -18,8 +19,10 @@ Overflow-policy and routing variants of the Switch layer (same inputs):
   switch_pad      plain dropping, every expert's block padded to C = 128 rows
   switch_ec       expert choice: each expert takes its 128 most probable tokens
 
-Input recipe: x ~ N(0,1); Wg, Wnoise, W1, W2, W1s, W2s ~ N(0, 0.02^2); the
-router noise [T,E] ~ N(0,1) generated on the host side and passed in.
+Input recipe: x ~ N(0,1); Wg, Wnoise, W1, W2, W1s, W2s ~ N(0, 0.02^2). The
+Switch layers draw their router noise [T,E] ~ N(0,1) on the device from
+(noise_seed, noise_counter) (moe_draw_noise); a noisy workload with
+noise_draw = 0 gets it generated here and passed in.
 """
 from __future__ import annotations
 
@@ -38,7 +41,8 @@ W_STD = 0.02
 class Workload:
     name: str
     cfg: Config
-    noisy: bool = False          # KeepTopK noise: Wnoise + host noise tensor
+    noisy: bool = False          # KeepTopK noise: Wnoise, plus a noise tensor unless
+                                 # cfg.noise_draw (then the library draws it)
     zipf_s: float = 0.0          # > 0: logit offset -s ln(e+1)
     sel_bias: bool = False       # selection bias ~ U(-0.1, 0.1)
     bias_rate: float = 0.0       # > 0: one bias update per step
@@ -55,7 +59,8 @@ WORKLOADS = {
     "tiny": Workload("tiny", Config(T=256, d_model=128, n_experts=8, top_k=2, d_ff=256,
                                     capacity_factor=1.25, dtype=MOE_F32, act=MOE_GELU)),
     "switch": Workload("switch", Config(T=8192, d_model=1024, n_experts=64, top_k=1, d_ff=4096,
-                                        capacity_factor=1.0, dtype=MOE_BF16, act=MOE_RELU),
+                                        capacity_factor=1.0, dtype=MOE_BF16, act=MOE_RELU,
+                                        noise_draw=1, noise_seed=0x5EED),
                        noisy=True),
     "mixtral": Workload("mixtral", Config(T=16384, d_model=4096, n_experts=8, top_k=2,
                                           d_ff=14336, capacity_factor=0.0, dtype=MOE_BF16,
@@ -92,7 +97,9 @@ def make_inputs(wl: Workload, device="cuda", experts: bool = True) -> dict:
     }
     if wl.noisy:
         out["Wnoise"] = synth.normal((d, E), s, synth.TID_WNOISE, W_STD, dt, device)
-        out["noise"] = synth.normal((T, E), s, synth.TID_NOISE, 1.0, torch.float32, "cpu").to(device)
+        if not c.noise_draw:
+            out["noise"] = synth.normal((T, E), s, synth.TID_NOISE, 1.0, torch.float32,
+                                        "cpu").to(device)
     if wl.zipf_s > 0:
         out["logit_offset"] = synth.zipf_logit_offset(E, wl.zipf_s).to(device)
     if wl.sel_bias:

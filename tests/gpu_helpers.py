@@ -73,6 +73,20 @@ def check_topk_valid(ids_gpu, s_ref, k, tol_rel=1e-5):
     return diff
 
 
+def oracle_noise(wl, inp):
+    """The router noise of a workload on the host, as the oracle takes it: the
+    passed-in tensor, or, when the library draws it (noise_draw), the oracle's
+    own draws for the same (seed, counter). None for a router without noise."""
+    import oracle
+    c = wl.cfg
+    if inp["noise"] is not None:
+        return inp["noise"].cpu()
+    if not wl.noisy:
+        return None
+    eps = oracle.draw_noise(c.T, c.n_experts, c.noise_seed, c.noise_counter)
+    return torch.from_numpy(eps.astype(np.float32))
+
+
 def layer_outputs(wl, inp, device):
     c = wl.cfg
     T, E, k, d = c.T, c.n_experts, c.top_k, c.d_model

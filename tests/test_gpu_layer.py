@@ -12,7 +12,7 @@ from sparse_mixture_experts_69_b300 import moe, synth
 from sparse_mixture_experts_69_b300.workloads import WORKLOADS, make_inputs
 
 from gpu_helpers import (TOL_AUX, TOL_LOGITS, TOL_Y, assert_maxabs, assert_rowwise,
-                         check_topk_valid, np32, run_layer)
+                         check_topk_valid, np32, oracle_noise, run_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,7 @@ def _oracle_router(wl, inp, tok):
     tok_t = torch.as_tensor(tok)
     g = lambda n: None if inp[n] is None else inp[n].cpu()
     return oracle.router(_cpu_rows(inp["x"], tok_t), g("Wg"), c.top_k, Wnoise=g("Wnoise"),
-                         noise=_cpu_rows(inp["noise"], tok_t), offset=g("logit_offset"),
+                         noise=_cpu_rows(oracle_noise(wl, inp), tok_t), offset=g("logit_offset"),
                          bias=g("sel_bias"), renorm=bool(c.renorm_topk))
 
 

@@ -11,7 +11,8 @@ import oracle
 from sparse_mixture_experts_69_b300 import moe, synth
 from sparse_mixture_experts_69_b300.workloads import WORKLOADS, make_inputs
 
-from gpu_helpers import TOL_AUX, TOL_GATE, TOL_LOGITS, TOL_Y, assert_maxabs, assert_rowwise, np32
+from gpu_helpers import (TOL_AUX, TOL_GATE, TOL_LOGITS, TOL_Y, assert_maxabs, assert_rowwise,
+                         np32, oracle_noise)
 
 pytestmark = pytest.mark.gpu
 
@@ -227,7 +228,7 @@ def test_layer_expert_choice(cuda_device, name, over):
     logits = torch.empty((T, E), device=dev)
     moe.moe_route(cfg, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"],
                   inp["sel_bias"], logits, probs, None, None, None, 0, ws)
-    r = oracle.router(inp["x"], inp["Wg"], 1, Wnoise=inp["Wnoise"], noise=inp["noise"],
+    r = oracle.router(inp["x"], inp["Wg"], 1, Wnoise=inp["Wnoise"], noise=oracle_noise(wl, inp),
                       offset=inp["logit_offset"], bias=inp["sel_bias"])
     assert_rowwise(np32(probs), r["p"], TOL_LOGITS, "probs")
     p_h = np32(probs)

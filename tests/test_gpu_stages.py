@@ -61,6 +61,75 @@ def test_router_f32(cuda_device, T, d, E, k, noisy, offset, bias):
     assert_rowwise(np32(w)[same], r["w"][same], TOL_LOGITS, "gates")
 
 
+@pytest.mark.parametrize("T,E,seed,counter", [(1, 1, 0, 0), (1000, 300, 0x5EED, 7),
+                                               (8192, 64, 2**64 - 1, 2**40 + 3)])
+def test_draw_noise_matches_oracle(cuda_device, T, E, seed, counter):
+    """moe_draw_noise against the oracle's Philox4x32-10 + Box-Muller draws:
+    the 24-bit uniforms are integers on both sides, so only the float32 log,
+    square root and cosine differ from the double ones."""
+    cfg = moe.Config(T=T, d_model=8, n_experts=E, top_k=1, d_ff=8, noise_draw=1,
+                     noise_seed=seed, noise_counter=counter)
+    eps = torch.empty((T, E), device=cuda_device)
+    moe.moe_draw_noise(cfg, eps)
+    ref = oracle.draw_noise(T, E, seed, counter)
+    err = np.abs(np32(eps) - ref) / np.maximum(1.0, np.abs(ref))
+    assert err.max() < 2e-6, err.max()
+
+
+@pytest.mark.parametrize("T,d,E,k,dtype", [(300, 64, 64, 1, moe.MOE_F32),
+                                           (1000, 128, 32, 2, moe.MOE_BF16)])
+def test_router_with_drawn_noise(cuda_device, T, d, E, k, dtype):
+    """noise_draw = 1: the selection kernel draws eps itself; probs, scores and
+    the top-k match the oracle router fed the oracle's draws, and passing
+    moe_draw_noise's output in as the noise tensor routes bit for bit alike."""
+    cfg = moe.Config(T=T, d_model=d, n_experts=E, top_k=k, d_ff=64, dtype=dtype,
+                     act=moe.MOE_GELU, noise_draw=1, noise_seed=99, noise_counter=5)
+    td = cfg.torch_dtype
+    x = synth.normal((T, d), 1, 101, 1.0, td)
+    Wg = synth.normal((d, E), 1, 102, 0.1, td)
+    Wn = synth.normal((d, E), 1, 103, 0.1, td)
+    dev = cuda_device
+    logits = torch.empty((T, E), device=dev)
+    probs = torch.empty((T, E), device=dev)
+    sel = torch.empty((T, E), device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), device=dev)
+    ws = moe.workspace(cfg, dev)
+    moe.moe_route(cfg, x.to(dev), Wg.to(dev), Wn.to(dev), None, None, None, logits, probs, sel,
+                  ids, w, 0, ws)
+    assert moe.moe_read_device_error(cfg, ws) == 0
+    noise = torch.from_numpy(oracle.draw_noise(T, E, 99, 5).astype(np.float32))
+    r = oracle.router(x.float(), Wg.float(), k, Wnoise=Wn.float(), noise=noise)
+    assert_rowwise(np32(probs), r["p"], TOL_LOGITS, "probs")
+    assert_rowwise(np32(sel), r["s"], TOL_LOGITS, "sel_scores")
+    check_topk_valid(ids.cpu().numpy(), r["s"], k)
+    cfg_in = moe.Config(**{**cfg.__dict__, "noise_draw": 0})
+    eps = torch.empty((T, E), device=dev)
+    moe.moe_draw_noise(cfg, eps)
+    ids2 = torch.empty_like(ids)
+    w2 = torch.empty_like(w)
+    moe.moe_route(cfg_in, x.to(dev), Wg.to(dev), Wn.to(dev), eps, None, None, logits, probs, sel,
+                  ids2, w2, 0, ws)
+    assert torch.equal(ids2, ids) and torch.equal(w2, w)
+
+
+def test_noise_arguments_are_checked(cuda_device):
+    """With noise_draw = 1 a noise tensor is refused; without Wnoise the router
+    has no noise term and the call runs."""
+    cfg = moe.Config(T=16, d_model=8, n_experts=4, top_k=1, d_ff=8, noise_draw=1)
+    dev = cuda_device
+    x = torch.zeros((16, 8), dtype=torch.bfloat16, device=dev)
+    Wg = torch.zeros((8, 4), dtype=torch.bfloat16, device=dev)
+    noise = torch.zeros((16, 4), device=dev)
+    out = [torch.empty((16, 4), device=dev) for _ in range(3)]
+    ids = torch.empty((16, 1), dtype=torch.int32, device=dev)
+    w = torch.empty((16, 1), device=dev)
+    ws = moe.workspace(cfg, dev)
+    with pytest.raises(moe.MoeError):
+        moe.moe_route(cfg, x, Wg, Wg, noise, None, None, *out, ids, w, 0, ws)
+    moe.moe_route(cfg, x, Wg, None, None, None, None, *out, ids, w, 0, ws)
+
+
 @pytest.mark.parametrize("T,E,k,renorm", [(1, 5, 2, 1), (513, 8, 2, 1), (200, 64, 1, 1),
                                           (129, 256, 8, 1), (64, 300, 32, 0), (40, 7, 7, 1)])
 def test_select_from_scores_bit_exact(cuda_device, T, E, k, renorm):
