@@ -203,16 +203,27 @@ __device__ __forceinline__ void load_token(const SelectArgs& a, int t, TokenRegs
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         const bool in = e < a.E;
-        r.eps[i] = 0.f;
+        if (!a.draw) r.eps[i] = 0.f;  // drawn noise: already in r (draw_token_eps)
         if (a.from_scores) {
             r.z[i] = in ? a.sel_in[row + e] : 0.f;
             r.zn[i] = in ? a.probs_in[row + e] : 0.f;
         } else {
             r.z[i] = in ? a.logits[row + e] : 0.f;
             r.zn[i] = in && noisy ? a.zn[row + e] : 0.f;
-            if (in && noisy)
-                r.eps[i] = a.draw ? draw_eps(a.seed, a.ctr, t, e) : a.noise[row + e];
+            if (in && noisy && !a.draw) r.eps[i] = a.noise[row + e];
         }
+    }
+}
+
+// Drawn noise of token t (a.draw). It reads no global memory, so the selection
+// kernels make the draws before they wait for the router GEMM, under its run.
+template <int EPL>
+__device__ __forceinline__ void draw_token_eps(const SelectArgs& a, int t, TokenRegs<EPL>& r) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        r.eps[i] = e < a.E ? draw_eps(a.seed, a.ctr, t, e) : 0.f;
     }
 }
 
@@ -330,13 +341,14 @@ constexpr int kSelWarps = 8;
 // Standalone selection.
 template <int EPL>
 __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(SelectArgs a) {
+    const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
+    TokenRegs<EPL> r;
+    if (a.draw && t < a.T) draw_token_eps<EPL>(a, t, r);
     // dependents launch after this wait: the router GEMM before this kernel is
     // then complete, so the next router-weight copy may overwrite WgT
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
     if (t >= a.T) return;
-    TokenRegs<EPL> r;
     load_token<EPL>(a, t, r);
     float pr[EPL];
     int id;
@@ -380,6 +392,9 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
 template <int EPL>
 __global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : 1) router_select_fused_kernel(
     SelectArgs a, int32_t* blk_hist, int nblk_cap, AuxAcc acc, AuxOut out, int defer_final) {
+    const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
+    TokenRegs<EPL> r;
+    if (a.draw && t < a.T) draw_token_eps<EPL>(a, t, r);
     pdl_wait();
     pdl_trigger();  // after the wait, as in router_select_kernel
     extern __shared__ unsigned long long sm64[];
@@ -388,8 +403,6 @@ __global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : 1) router_selec
     unsigned long long* sI = sm64 + E;
     unsigned int* sC = reinterpret_cast<unsigned int*>(sm64 + 2 * E);
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
-    TokenRegs<EPL> r;
     if (t < a.T) load_token<EPL>(a, t, r);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         sP[e] = 0;
