@@ -1,22 +1,32 @@
 """Benchmark of the sparse-MoE layer forward pass on one B300 (or N replicas).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload switch]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral]
+                    [--configs all|none|name,name...] [--only-route]
     python bench.py --impl reference ...     # the CPU oracle, timed on host cores
 
 One step = one moe_layer_fwd (router -> capacity/dispatch -> grouped expert
 GEMMs -> combine -> statistics; plus the loss-free bias update where the
 workload has one) over one batch of T synthetic tokens. Prints one JSON line.
 
+The headline workload (default: the Mixtral-shaped layer, the largest by
+FLOPs and tokens) is timed for exactly K steps; every other workload named by
+--configs (default: all of them) is then measured the same way, with its own
+step count, and reported under the line's "configs" key.
+
 value      tokens/s over all ranks, inputs already resident in HBM
-e2e        the same call with the step's inputs copied from pinned host memory
-           and the result (y, aux) copied back inside the timed region; two
-           buffer sets let the copies of neighbouring steps overlap the compute
+e2e        the same call with the step's inputs (x, and the router noise where
+           the workload passes it in) copied from pinned host memory and the
+           result (y, aux) copied back inside the timed region; two buffer sets
+           let the copies of neighbouring steps overlap the compute; at least
+           200 steps and one second of wall time
 roofline   the grouped expert GEMM (the dominant kernel): algorithmic bytes
            (weights of touched experts + activations in/out) per launch over its
            CUDA-event duration, against the measured HBM copy bandwidth; or, when
            its FLOPs at the measured bf16 rate take longer than its bytes at the
            HBM rate (the Mixtral- and DeepSeek-shaped layers), its TFLOP/s
            against that bf16 rate
+hbm_stages the router, dispatch, combine and statistics entry points alone:
+           their algorithmic bytes over their time, against the HBM peak
 """
 from __future__ import annotations
 
@@ -39,11 +49,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="switch")
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--configs", default="all",
+                    help="other workloads measured after the headline: all, none, or a "
+                         "comma-separated list")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-route", action="store_true",
+                    help="time moe_route alone on the headline workload (no expert weights)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -309,15 +324,20 @@ def cpu_baseline(wl, inp, budget_s=12.0):
 
 
 def run_reference(a):
-    """--impl reference: the CPU oracle, timed on the host cores, same workload."""
+    """--impl reference: the CPU oracle, timed on the host cores, same workload.
+    The synthetic inputs are made on the GPU when one is present (the
+    generator is the same on both devices; generating the Mixtral-shaped
+    layer's 2.8 GB of expert weights on the host would take minutes), then
+    copied to the host; the oracle itself runs on the host only."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from sparse_mixture_experts_69_b300.workloads import WORKLOADS
+    from sparse_mixture_experts_69_b300.workloads import WORKLOADS, make_inputs
     import oracle
     oracle.build()
     wl = WORKLOADS[a.workload]
-    oi = OracleInputs(wl, None)
+    inp = make_inputs(wl, "cuda") if torch.cuda.is_available() else None
+    oi = OracleInputs(wl, inp)
     # per-step sample sized so warm-up + steps take about two minutes of compute
     n, dt = oracle_tokens_per_s(oi, 4)
     per_tok = dt / max(n, 1)
@@ -349,23 +369,67 @@ def run_reference(a):
 
 # ---------------------------------------------------------------- our arm
 
-def main():
-    a = parse()
-    if a.impl == "reference":
-        return run_reference(a)
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
+ALL_CONFIGS = ["tiny", "switch", "mixtral", "deepseek", "decode"]
 
+
+def launches_per_step(wl):
+    """Kernels of this library one step launches. Layer path: [Wg transpose
+    (bf16)], router GEMM, fused selection + histogram + statistics, capacity
+    scan + slots (one launch up to 256 token blocks), permute, up GEMM, down
+    GEMM, [combine: skipped for bf16 top-1 without shared experts, where the
+    down GEMM writes y], [bias update]. Overflow policies: one capacity kernel
+    instead of scan + slots; expert choice: select + gather instead of
+    capacity + permute, its own combine."""
+    c = wl.cfg
+    T, k, nc = c.T, c.top_k, c.n_cand
+    ec = c.routing == 1
+    scatter = (c.dtype == 1 and c.top_k == 1 and nc == 1 and not c.pad_to_capacity
+               and c.n_shared == 0)
+    policy = nc > k or c.priority != 0
+    route_launches = (1 if c.dtype == 1 else 0) + 2
+    if ec:
+        return route_launches + 2 + 2 + 1
+    cap_launches = 1 if policy else (1 if (T + 255) // 256 <= 256 else 2)
+    return (route_launches + cap_launches + 1 + 2 + (0 if scatter else 1)
+            + (1 if wl.bias_rate else 0))
+
+
+def time_graph(fn, n, stream, dev):
+    """Device time of one call of fn: n calls captured in one CUDA graph and
+    replayed between CUDA events (a single small call is host-bound)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+            for _ in range(n):
+                fn()
+    torch.cuda.synchronize()
+    g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def hbm_record(nbytes, ms, hbm):
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"bytes": nbytes, "ms": ms, "gbs": gbs, "frac": gbs / hbm}
+
+
+def measure(wl, steps, warmup, dev, pg, world, local, cpu_budget, want_cpu, auto_steps=False):
+    """Time one workload: the layer with inputs resident (steps x
+    moe_layer_fwd), each entry point alone, and end to end with host buffers.
+    Returns the workload's record (the JSON line's fields)."""
     from sparse_mixture_experts_69_b300 import moe
-    from sparse_mixture_experts_69_b300.workloads import WORKLOADS, make_inputs
+    from sparse_mixture_experts_69_b300.workloads import make_inputs
 
-    wl = WORKLOADS[a.workload].with_(seed=rank)
     c = wl.cfg
     T, E, k, d, nc = c.T, c.n_experts, c.top_k, c.d_model, c.n_cand
     ec = c.routing == moe.MOE_EXPERT_CHOICE
@@ -393,17 +457,22 @@ def main():
             pg.barrier()
 
     # ------------------------------------------------ device-resident timing
-    for _ in range(a.warmup):
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(warmup):
         step(inp["x"], inp["noise"])
+    ev1.record(stream)
     st = moe.moe_read_device_error(c, ws)
     if st != 0:
-        raise RuntimeError("device status after warm-up: " + moe.moe_status_string(st))
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        raise RuntimeError(f"{wl.name}: device status after warm-up: " + moe.moe_status_string(st))
+    if auto_steps:  # about half a second of timed work
+        est = ev0.elapsed_time(ev1) / warmup
+        steps = int(min(4000, max(20, 500.0 / max(est, 1e-3))))
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         ev0.record(stream)
-        for _ in range(a.steps):
+        for _ in range(steps):
             step(inp["x"], inp["noise"])
         ev1.record(stream)
         torch.cuda.synchronize()
@@ -412,10 +481,10 @@ def main():
     ms_max = max_over_ranks(ms, pg, dev)
     st = moe.moe_read_device_error(c, ws)
     if st != 0:
-        raise RuntimeError("device status after timing: " + moe.moe_status_string(st))
-    value = tokens_per_s(world, T, a.steps, ms_max)
+        raise RuntimeError(f"{wl.name}: device status after timing: " + moe.moe_status_string(st))
+    value = tokens_per_s(world, T, steps, ms_max)
 
-    # ------------------------------------------------ per-stage split (same calls, stage APIs)
+    # ------------------------------------------------ each entry point alone
     C, R_max = moe.moe_capacity(c)
     logits = torch.empty((T, E), device=dev)
     probs = torch.empty((T, E), device=dev)
@@ -430,66 +499,46 @@ def main():
     row_w = torch.empty(R_max, device=dev)
     tok_row = torch.empty((T, E), dtype=torch.int32, device=dev) if ec else None
     n_seq = 8
-    seq_offsets = torch.arange(0, T + 1, T // n_seq, dtype=torch.int32, device=dev)[:n_seq + 1]
+    seq_offsets = torch.arange(0, T + 1, max(1, T // n_seq), dtype=torch.int32,
+                               device=dev)[:n_seq + 1].clone()
+    n_seq = seq_offsets.numel() - 1
     seq_offsets[-1] = T
     seq_out = torch.empty((2, n_seq, E), device=dev)
     seq_aux = torch.empty(n_seq + 1, device=dev)
-    # each stage alone: n calls captured in one CUDA graph and replayed, so the
-    # time is the device's (a single call is host-bound for the small stages)
-    def time_calls(fn, n):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
-                for _ in range(n):
-                    fn()
-        torch.cuda.synchronize()
-        g.replay()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / n
-
-    n_split = max(20, min(200, a.steps // 10))
-    # the stage calls take torch's current stream, which is the capture stream in time_calls
+    n_split = 20
+    # the stage calls take torch's current stream, which is the capture stream in time_graph
     route = lambda: moe.moe_route(
         c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"], inp["logit_offset"], bias, logits,
         probs, None, None if ec else ids, None if ec else w, 0, ws)
     ffn = lambda: moe.moe_expert_ffn(c, xp, offsets, inp["W1"], inp["W2"], inp["x"], inp["W1s"],
                                      inp["W2s"], yp, ys, ws)
+    tg = lambda fn: time_graph(fn, n_split, stream, dev)
     if ec:
         stage_ms = {
-            "route": time_calls(route, n_split),
-            "dispatch": time_calls(lambda: moe.moe_expert_choice_dispatch(
-                c, inp["x"], probs, offsets, row_token, row_w, tok_row, xp, ws), n_split),
-            "expert_ffn": time_calls(ffn, n_split),
-            "combine": time_calls(lambda: moe.moe_expert_choice_combine(
-                c, yp, tok_row, probs, ys, y, ws), n_split),
+            "route": tg(route),
+            "dispatch": tg(lambda: moe.moe_expert_choice_dispatch(
+                c, inp["x"], probs, offsets, row_token, row_w, tok_row, xp, ws)),
+            "expert_ffn": tg(ffn),
+            "combine": tg(lambda: moe.moe_expert_choice_combine(
+                c, yp, tok_row, probs, ys, y, ws)),
         }
     else:
         stage_ms = {
-            "route": time_calls(route, n_split),
-            "dispatch": time_calls(lambda: moe.moe_dispatch(
-                c, inp["x"], ids, counts, kept, offsets, slot, xp, row_token, ws), n_split),
-            "expert_ffn": time_calls(ffn, n_split),
-            "combine": time_calls(lambda: moe.moe_combine(c, yp, slot, w, ys, y, ws),
-                                  n_split),
-            "aux": time_calls(lambda: moe.moe_aux_stats(c, probs, ids, w, fP[0], fP[1], fP[2],
-                                                        out3, ws), n_split),
-            "seq_aux_8_sequences": time_calls(lambda: moe.moe_seq_aux_stats(
+            "route": tg(route),
+            "dispatch": tg(lambda: moe.moe_dispatch(
+                c, inp["x"], ids, counts, kept, offsets, slot, xp, row_token, ws)),
+            "expert_ffn": tg(ffn),
+            "combine": tg(lambda: moe.moe_combine(c, yp, slot, w, ys, y, ws)),
+            "aux": tg(lambda: moe.moe_aux_stats(c, probs, ids, w, fP[0], fP[1], fP[2], out3,
+                                                ws)),
+            f"seq_aux_{n_seq}_sequences": tg(lambda: moe.moe_seq_aux_stats(
                 c, probs, ids, seq_offsets, n_seq, seq_out[0], seq_out[1], seq_aux[:n_seq],
-                seq_aux[n_seq:], ws), n_split),
+                seq_aux[n_seq:], ws)),
         }
     st = moe.moe_read_device_error(c, ws)
     if st != 0:
-        raise RuntimeError("device status after the stage timing: " + moe.moe_status_string(st))
+        raise RuntimeError(f"{wl.name}: device status after the stage timing: "
+                           + moe.moe_status_string(st))
 
     # algorithmic work of the expert FFN (two grouped-GEMM launches): rows the
     # GEMMs run on (padding rows included where the blocks are padded), and the
@@ -504,14 +553,27 @@ def main():
     flops = 2 * (R + S * T) * d * (F1 + F)
     ffn_ms = stage_ms["expert_ffn"]
     pk, pk_kind = peaks()
-    roofline = roofline_record(flops, ffn_bytes, ffn_ms, pk, pk_kind, ncu_traffic(a.workload))
+    roofline = roofline_record(flops, ffn_bytes, ffn_ms, pk, pk_kind, ncu_traffic(wl.name))
+    # the memory-bound entry points: algorithmic bytes (inputs read once,
+    # outputs written once) over their time
+    noisy_b = (d * E * es + (T * E * 4 if inp["noise"] is not None else 0)) if wl.noisy else 0
+    route_b = (T * d * es + d * E * es + noisy_b + 2 * T * E * 4
+               + (0 if ec else T * nc * 8))
+    hbm = pk["hbm_gbs"]
+    hbm_stages = {"route": hbm_record(route_b, stage_ms["route"], hbm)}
+    if not ec:
+        hbm_stages["dispatch"] = hbm_record(T * d * es + 2 * T * nc * 4 + R * (d * es + 4),
+                                            stage_ms["dispatch"], hbm)
+        hbm_stages["combine"] = hbm_record(R * d * es + T * nc * 8 + S * T * d * es + T * d * es,
+                                           stage_ms["combine"], hbm)
+        hbm_stages["aux"] = hbm_record(T * E * 4 + T * k * 8, stage_ms["aux"], hbm)
 
     # ------------------------------------------------ end to end (host buffers)
-    # Every step uploads its inputs (x and the router noise) from pinned host
-    # memory and downloads its result (y, and the aux scalars) to pinned host
-    # memory. Two buffer sets and separate upload / download streams let step
-    # i+1's upload and step i-1's download run under step i's compute, as a
-    # caller streaming batches through the layer would arrange it.
+    # Every step uploads its inputs (x, and the router noise where it is passed
+    # in) from pinned host memory and downloads its result (y, and the aux
+    # scalars) to pinned host memory. Two buffer sets and separate upload /
+    # download streams let step i+1's upload and step i-1's download run under
+    # step i's compute, as a caller streaming batches through the layer would.
     x_host = inp["x"].cpu().pin_memory()
     noise_host = inp["noise"].cpu().pin_memory() if inp["noise"] is not None else None
     nbuf = 2
@@ -528,7 +590,6 @@ def main():
     downloaded = [torch.cuda.Event() for _ in range(nbuf)]
     for e_ in computed + downloaded:
         e_.record(stream)  # every buffer starts free
-    K2 = max(10, a.steps // 4)
 
     def e2e_step(i):
         bi = i % nbuf
@@ -554,8 +615,16 @@ def main():
                 o3_host[bi].copy_(o3_dev[bi], non_blocking=True)
         downloaded[bi].record(down_st)
 
+    # an estimate first, then at least 200 steps and one second of wall time
     for i in range(3):
         e2e_step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(10):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / 10
+    K2 = int(max(200, 1.2 / max(est, 1e-6)))
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -569,51 +638,130 @@ def main():
         noise_host.numel() * 4 if noise_host is not None else 0)
     d2h = y_host[0].numel() * y_host[0].element_size() + (0 if ec else 12)
     e2e_value = tokens_per_s(world, T, K2, e2e_s * 1e3)
+    st = moe.moe_read_device_error(c, ws)
+    if st != 0:
+        raise RuntimeError(f"{wl.name}: device status after e2e: " + moe.moe_status_string(st))
 
-    # layer path: [Wg transpose (bf16)], router GEMM, fused selection + histogram +
-    # statistics, capacity scan + slots (one launch up to 256 token blocks),
-    # permute, up GEMM, down GEMM, [combine: skipped for bf16 top-1 without
-    # shared experts, where the down GEMM writes y], [bias update]
-    # overflow policies: one capacity kernel instead of scan + slots; expert
-    # choice: select + gather instead of capacity + permute, its own combine
-    scatter = (c.dtype == 1 and c.top_k == 1 and nc == 1 and not c.pad_to_capacity
-               and c.n_shared == 0)
-    policy = nc > k or c.priority != 0
-    route_launches = (1 if c.dtype == 1 else 0) + 2
-    if ec:
-        launches_per_step = route_launches + 2 + 2 + 1
-    else:
-        cap_launches = 1 if policy else (1 if (T + 255) // 256 <= 256 else 2)
-        launches_per_step = (route_launches + cap_launches + 1 + 2 + (0 if scatter else 1)
-                             + (1 if wl.bias_rate else 0))
-
-    if rank != 0:
-        return 0
     cb = None
     # the oracle's per-token sample has no expert-choice counterpart (an expert's
     # choice depends on the whole batch); that variant reports none
-    if not a.no_cpu_baseline and world == 1 and not ec:
-        cb = cpu_baseline(wl, inp)
-    clocks = clk.summary()
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_max / a.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if c.dtype == 1 else "f32", "data": "synthetic",
-        "config": {"workload": workload_desc(wl), "global_batch": world * T,
-                   "seq_len": None, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: each step streams "
-                         f"{w_bytes / 1e9:.2f} GB of expert weights through the 126 MB L2"},
-        "roofline": roofline,
-        "cpu_baseline": cb,
+    if want_cpu and world == 1 and not ec:
+        cb = cpu_baseline(wl, inp, cpu_budget)
+    rec = {
+        "workload": workload_desc(wl), "value": value, "unit": "tokens/s",
+        "ms_per_step": ms_max / steps, "steps": steps,
+        "dtype": "bf16" if c.dtype == 1 else "f32",
+        "roofline": roofline, "hbm_stages": hbm_stages, "cpu_baseline": cb,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": K2,
+                "d2h_bytes_per_step": d2h, "steps": K2, "wall_s": e2e_s,
                 "copies": "pinned host buffers, double-buffered, upload / download streams "
                           "overlapping the compute stream"},
-        "gpu_launches": launches_per_step * a.steps,
-        "clocks": clocks,
-        "stage_ms": stage_ms,
-        "rows_kept": R, "experts_touched": touched,
+        "clocks": clk.summary(), "stage_ms": stage_ms, "rows_kept": R,
+        "experts_touched": touched, "weights_gb": w_bytes / 1e9,
+        "gpu_launches": launches_per_step(wl) * steps,
+    }
+    return rec
+
+
+def run_only_route(a, dev):
+    """Time moe_route alone on the headline workload (router inputs only, no
+    expert weights): its HBM rate against the measured peak."""
+    from sparse_mixture_experts_69_b300 import moe
+    from sparse_mixture_experts_69_b300.workloads import WORKLOADS, make_inputs
+    wl = WORKLOADS[a.workload]
+    c = wl.cfg
+    T, E, d, nc = c.T, c.n_experts, c.d_model, c.n_cand
+    inp = make_inputs(wl, dev, experts=False)
+    ws = moe.workspace(c, dev)
+    logits = torch.empty((T, E), device=dev)
+    probs = torch.empty((T, E), device=dev)
+    ids = torch.empty((T, nc), dtype=torch.int32, device=dev)
+    w = torch.empty((T, nc), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fn = lambda: moe.moe_route(c, inp["x"], inp["Wg"], inp["Wnoise"], inp["noise"],
+                               inp["logit_offset"], inp["sel_bias"], logits, probs, None, ids,
+                               w, 0, ws)
+    for _ in range(a.warmup):
+        fn()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(a.steps):
+        fn()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    st = moe.moe_read_device_error(c, ws)
+    if st != 0:
+        raise RuntimeError("device status: " + moe.moe_status_string(st))
+    ms = ev0.elapsed_time(ev1) / a.steps
+    es = 2 if c.dtype == 1 else 4
+    noisy_b = (d * E * es + (T * E * 4 if inp["noise"] is not None else 0)) if wl.noisy else 0
+    nbytes = T * d * es + d * E * es + noisy_b + 2 * T * E * 4 + T * nc * 8
+    pk, pk_kind = peaks()
+    line = {"mode": "only-route", "workload": workload_desc(wl), "steps": a.steps,
+            "route_ms": ms, "graph_route_ms": time_graph(fn, 20, stream, dev),
+            "route": hbm_record(nbytes, ms, pk["hbm_gbs"]), "peak_kind": pk_kind,
+            "router_gflop": 2.0 * T * d * (2 * E if wl.noisy else E) / 1e9}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        return run_reference(a)
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if a.only_route:
+        return run_only_route(a, dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from sparse_mixture_experts_69_b300.workloads import WORKLOADS
+
+    wl = WORKLOADS[a.workload].with_(seed=rank)
+    head = measure(wl, a.steps, a.warmup, dev, pg, world, local, 12.0,
+                   not a.no_cpu_baseline and rank == 0)
+    torch.cuda.empty_cache()
+    # the other workloads, one after another (each one's tensors are freed
+    # before the next is made); replicas under torchrun time the headline only
+    others = {}
+    names = ALL_CONFIGS if a.configs == "all" else (
+        [] if a.configs == "none" else [n for n in a.configs.split(",") if n])
+    if world == 1:
+        for name in names:
+            if name == a.workload:
+                continue
+            others[name] = measure(WORKLOADS[name], 0, max(3, min(a.warmup, 10)), dev, None, 1,
+                                   local, 6.0, not a.no_cpu_baseline, auto_steps=True)
+            torch.cuda.empty_cache()
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    c = wl.cfg
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": head["dtype"], "data": "synthetic",
+        "config": {"workload": head["workload"], "global_batch": world * c.T,
+                   "seq_len": None, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: each step streams "
+                         f"{head['weights_gb']:.2f} GB of expert weights through the 126 MB L2"},
+        "roofline": head["roofline"],
+        "cpu_baseline": head["cpu_baseline"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "stage_ms": head["stage_ms"],
+        "hbm_stages": head["hbm_stages"],
+        "rows_kept": head["rows_kept"], "experts_touched": head["experts_touched"],
+        "configs": others,
     }
     print(json.dumps(line), flush=True)
     if pg:

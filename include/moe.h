@@ -334,8 +334,11 @@ MOE_API moe_status moe_seq_aux_stats(const moe_config* cfg, const float* probs,
  * that loads the library holds one copy until the process exits. n_experts
  * above 512 returns MOE_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on a device looks up that array's device address (with
- *     the device current) and caches it; make that first call before any
- *     stream capture.
+ *     the device current) and caches it together with the current CUDA
+ *     context; make that first call before any stream capture. A call made
+ *     in another context of that device (after cudaDeviceReset destroyed the
+ *     primary context and the runtime made a new one) looks it up again, so
+ *     the first call after a reset should also come before any capture.
  *   - All calls share the one array and it keeps the last call's contents;
  *     each call clears it on its stream before use. Calls whose work overlaps
  *     on the GPU (other streams, other threads) race on it: serialise them. */
@@ -343,6 +346,26 @@ MOE_API moe_status moe_aux_stats_noalloc(const moe_config* cfg, const float* pro
                                          const int32_t* topk_ids, const float* topk_w,
                                          float* f, float* P, float* importance, float* out3,
                                          moe_stream_t stream);
+
+/* Limits of the library's bounded device waits. Settings of the process,
+ * read when a kernel is enqueued, so they apply to every call made after
+ * this one, on every thread and device.
+ *   wait_ns        time limit of each pipeline wait of the tensor-core GEMM
+ *                  kernels (the router and expert GEMMs); 0 restores the
+ *                  default of 2 s. A wait that runs out records
+ *                  MOE_ERR_TIMEOUT; the kernel then lets its own copies and
+ *                  matrix operations in flight finish (with a fixed limit of
+ *                  0.25 s), frees its tensor memory and returns, leaving its
+ *                  outputs incomplete.
+ *   policy_passes  pass limit of the fixed-point loop of capacity with
+ *                  re-routing or rank priority (moe_dispatch); 0 restores the
+ *                  default of 4096; if the loop has not settled by then it
+ *                  records MOE_ERR_TIMEOUT and writes the slots of its last
+ *                  pass (every row index still in range). Negative values
+ *                  return MOE_ERR_INVALID_ARG.
+ * No device work: the defaults never run out on a working GPU, and lowering
+ * them exists to exercise the failure path. Host only. */
+MOE_API moe_status moe_set_wait_limits(uint64_t wait_ns, int32_t policy_passes);
 
 /* Synchronise `stream`, read and clear the workspace status word, and map it
  * to MOE_OK, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_ARG (the

@@ -21,7 +21,8 @@
 // main loop of the next. Launched early (GroupedGemm::early), a CTA builds its
 // tile table and issues its first B tiles before waiting for the preceding
 // kernel. Every mbarrier wait is bounded in time; on expiry the CTA records
-// DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+// DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits. The
+// limit is 2 s unless moe_set_wait_limits changed it.
 #include <algorithm>
 #include <mutex>
 
@@ -56,7 +57,11 @@ constexpr int KH = MOE_TC_KH;
 constexpr int BKH = 64;      // 64 bf16 = 128 bytes = one swizzle atom row
 constexpr int BK = BKH * KH; // K per pipeline stage
 constexpr int kThreads = 192;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
+// Waits of a CTA that is aborting, for its own copies and MMAs already in
+// flight, keep this fixed limit whatever the limit of the pipeline waits is
+// (moe_set_wait_limits): those operations finish in microseconds, and shared
+// memory and TMEM must not be released under them.
+constexpr unsigned long long kDrainNs = 250000000ull;
 
 enum Epi : int { EPI_ACT = 0, EPI_GLU = 1, EPI_ROUTER = 2 };
 
@@ -66,6 +71,7 @@ struct TcArgs {
     float* logits;        // router: [T,E]
     float* zn;            // router: [T,E] or NULL
     int E_router;         // router: columns < E_router are logits
+    unsigned long long wait_ns;  // limit of each pipeline mbarrier wait
 };
 
 template <int BN>
@@ -130,7 +136,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 // Wait for the phase with the given parity to complete. Returns false if the
-// CTA is aborting or the wait exceeded kTimeoutNs (which starts the abort).
+// CTA is aborting or the wait exceeded limit_ns (which starts the abort).
 __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                        int* status, unsigned long long limit_ns) {
     const uint32_t a = smem_u32(bar);
@@ -481,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rot = MOE_TC_ROT ? tile % nkb : 0;
                 for (int kb0 = 0; kb0 < nkb; ++kb0, ++item) {
                     const int kb = kb0 + rot < nkb ? kb0 + rot : kb0 + rot - nkb;
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, kTimeoutNs)) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, args.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -508,8 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int s = 0; s < C::STAGES; ++s)
                     if ((filled >> s) & 1u) {
                         volatile int never = 0;
-                        mbar_wait(&full[s], (fill_parity >> s) & 1u, &never, p.status,
-                                  kTimeoutNs / 8);
+                        mbar_wait(&full[s], (fill_parity >> s) & 1u, &never, p.status, kDrainNs);
                     }
             }
         }
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
                 const int b = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
-                if (!mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.status, kTimeoutNs)) {
+                if (!mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.status, args.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     EPI != EPI_ROUTER && tile_rows(mt_start, grows, G, nt, BM, tile) <= 64;
                 const uint32_t idesc = m64 ? C::IDESC64 : C::IDESC;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kTimeoutNs)) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status, args.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -561,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) {
                 umma_commit(drain);
                 volatile int never = 0;
-                mbar_wait(drain, 0, &never, p.status, kTimeoutNs / 8);
+                mbar_wait(drain, 0, &never, p.status, kDrainNs);
             }
         }
     } else {
@@ -581,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
             const int b = local & 1;
             const uint32_t tph = (local >> 1) & 1;
-            if (!mbar_wait(&tfull[b], tph, abort_flag, p.status, kTimeoutNs)) break;
+            if (!mbar_wait(&tfull[b], tph, abort_flag, p.status, args.wait_ns)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(b * BN) + ((uint32_t)(32 * q) << 16);
             // M=64 tiles: accumulator row r is in TMEM lane 32 (r / 16) + r % 16,
@@ -739,6 +744,7 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
 cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStream_t st) {
     tc::TcArgs a{};
     a.p = g;
+    a.wait_ns = wait_limit_ns();
     const bool wef = MOE_TC_L2_HINTS && g.b_evict_first;
     if (g.glu)
         return wef ? tc::launch<256, tc::EPI_GLU, true>(a, st)
@@ -777,6 +783,7 @@ cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const
     a.logits = logits;
     a.zn = zn;
     a.E_router = s.E;
+    a.wait_ns = wait_limit_ns();
     // Narrowest tile that covers Nr, halved while that leaves too few tiles to
     // keep most SMs streaming x (the router reads T d b bytes of x and little else).
     const int mt = (s.T + tc::BM - 1) / tc::BM;

@@ -3,6 +3,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "aux_common.cuh"
@@ -29,6 +30,14 @@ int num_sms() {
     }
     return cache[dev];
 }
+
+namespace {
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_policy_passes{kDefaultPolicyPasses};
+}  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int policy_max_passes() { return g_policy_passes.load(std::memory_order_relaxed); }
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -612,6 +621,13 @@ MOE_API moe_status moe_seq_aux_stats(const moe_config* cfg, const float* probs,
     return MOE_OK;
 }
 
+MOE_API moe_status moe_set_wait_limits(uint64_t wait_ns, int32_t policy_passes) {
+    if (policy_passes < 0) return MOE_ERR_INVALID_ARG;
+    g_wait_ns.store(wait_ns ? (unsigned long long)wait_ns : kDefaultWaitNs);
+    g_policy_passes.store(policy_passes ? policy_passes : kDefaultPolicyPasses);
+    return MOE_OK;
+}
+
 MOE_API moe_status moe_read_device_error(const moe_config* cfg, void* ws, size_t ws_bytes,
                                          moe_stream_t stream) {
     Shape s;
@@ -644,21 +660,52 @@ namespace {
 
 // Host code may not hand g_aux_noalloc_scratch itself to a kernel: on the host
 // that name is a stand-in, not a device address. Its device address is
-// looked up once per device, with that device current, and cached.
+// looked up once per device, with that device current, and cached together
+// with the CUDA context it belongs to. A call from another context on that
+// device (the primary context was destroyed by cudaDeviceReset and made
+// again, which loads the library's device code again) looks the address up
+// afresh.
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
+CUcontext g_noalloc_ctx[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    });
+    return fn;
+}
+
+CUcontext current_context() {
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn fn = ctx_get_current_fn();
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
 
 moe_status noalloc_scratch_current_device(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
+    const CUcontext ctx = current_context();
+    if (!g_noalloc_ptr[dev] || !ctx || ctx != g_noalloc_ctx[dev]) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_aux_noalloc_scratch) != cudaSuccess || !ptr)
             return MOE_ERR_CUDA;
         g_noalloc_ptr[dev] = ptr;
+        // the lookup makes the device's primary context current if no context was
+        g_noalloc_ctx[dev] = current_context();
     }
     *out = g_noalloc_ptr[dev];
     return MOE_OK;

@@ -217,6 +217,14 @@ cudaError_t launch_bias_update(const Shape& s, const int32_t* counts, float* bia
 
 int num_sms();
 
+// Limits of the bounded device waits (moe_set_wait_limits): the time limit of
+// each tcgen05 pipeline mbarrier wait, and the pass limit of the capacity
+// policy's fixed-point loop. Read at launch time.
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+constexpr int kDefaultPolicyPasses = 4096;
+unsigned long long wait_limit_ns();
+int policy_max_passes();
+
 // ------------------------------------------------- programmatic dependent launch
 // Every kernel is launched with programmatic stream serialisation: it may be
 // scheduled while the previous kernel on the stream is still running.

@@ -47,7 +47,6 @@ namespace {
 constexpr int kPolCtas = 8;
 constexpr int kPolThreads = 1024;
 constexpr int kPolWarps = kPolThreads / 32;
-constexpr int kPolMaxPasses = 4096;
 
 struct PolArgs {
     int T, k, nc, E, C, priority, pad, rows;  // rows: R_max
@@ -58,6 +57,7 @@ struct PolArgs {
     int32_t* slot;       // [T,nc]; holds ranks between passes
     int32_t* row_token;  // [R_max]
     int* status;
+    int max_passes;      // bound of the fixed-point loop (DEV_TIMEOUT when it is reached)
 };
 
 __device__ __forceinline__ unsigned lanemask_lt_pol() {
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kPolThreads, 1) cap_policy_kernel(PolArgs a) {
 
     const int rounds = a.priority == MOE_PRIORITY_TOKEN ? 1 : nc;
     bool settled = false;
-    for (int pass = 0; pass < kPolMaxPasses; ++pass) {
+    for (int pass = 0; pass < a.max_passes; ++pass) {
         // each owned token's tries under the current fill positions
         for (int tl = tid; tl < nown; tl += kPolThreads) {
             const int t = t_lo + tl;
@@ -342,6 +342,7 @@ cudaError_t launch_capacity_policy(const Shape& s, const int32_t* ids, int32_t* 
     a.slot = slot;
     a.row_token = row_token;
     a.status = status;
+    a.max_passes = policy_max_passes();
     const size_t smem = sizeof(int) * policy_smem_words(s.E, s.T);
     cudaError_t err = cudaFuncSetAttribute(cap_policy_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -7,22 +7,24 @@ part of the layer.
 
   tiny     T=256   d=128  E=8   k=2 F=256   GELU,   cf=1.25 (C=40), fp32
   switch   T=8192  d=1024 E=64  k=1 F=4096  ReLU,   cf=1.0 (C=128), noisy KeepTopK
-           (noise drawn in the selection kernel), bf16
+           with the noise tensor [T,E] generated on the host and passed in, bf16
   mixtral  T=16384 d=4096 E=8   k=2 F=14336 SwiGLU, dropless, Zipf(1.2) logit offset, bf16
   deepseek T=8192  d=7168 E=256 k=8 F=2048  SwiGLU, 1 shared, dropless, selection bias
            U(-0.1,0.1), one bias update at rate 1e-3, bf16
   decode   T=64    d=4096 E=64  k=6 F=1408  SwiGLU, 2 shared, dropless, bf16
 
-Overflow-policy and routing variants of the Switch layer (same inputs):
+Variants of the Switch layer (same inputs):
+  switch_drawn    the router noise drawn by the library in the selection kernel
+                  (noise_draw = 1) instead of passed in
   switch_reroute  a full expert sends the token to its next candidate (1 extra)
   switch_rank     the same, every token's first choice served before any second
   switch_pad      plain dropping, every expert's block padded to C = 128 rows
   switch_ec       expert choice: each expert takes its 128 most probable tokens
 
 Input recipe: x ~ N(0,1); Wg, Wnoise, W1, W2, W1s, W2s ~ N(0, 0.02^2). The
-Switch layers draw their router noise [T,E] ~ N(0,1) on the device from
-(noise_seed, noise_counter) (moe_draw_noise); a noisy workload with
-noise_draw = 0 gets it generated here and passed in.
+router noise [T,E] ~ N(0,1) of the Switch layers is generated here and passed
+in; switch_drawn has the library draw it from (noise_seed, noise_counter)
+(moe_draw_noise) instead.
 """
 from __future__ import annotations
 
@@ -59,8 +61,7 @@ WORKLOADS = {
     "tiny": Workload("tiny", Config(T=256, d_model=128, n_experts=8, top_k=2, d_ff=256,
                                     capacity_factor=1.25, dtype=MOE_F32, act=MOE_GELU)),
     "switch": Workload("switch", Config(T=8192, d_model=1024, n_experts=64, top_k=1, d_ff=4096,
-                                        capacity_factor=1.0, dtype=MOE_BF16, act=MOE_RELU,
-                                        noise_draw=1, noise_seed=0x5EED),
+                                        capacity_factor=1.0, dtype=MOE_BF16, act=MOE_RELU),
                        noisy=True),
     "mixtral": Workload("mixtral", Config(T=16384, d_model=4096, n_experts=8, top_k=2,
                                           d_ff=14336, capacity_factor=0.0, dtype=MOE_BF16,
@@ -73,6 +74,8 @@ WORKLOADS = {
                                         n_shared=2, capacity_factor=0.0, dtype=MOE_BF16,
                                         act=MOE_SWIGLU)),
 }
+WORKLOADS["switch_drawn"] = WORKLOADS["switch"].with_(name="switch_drawn", noise_draw=1,
+                                                      noise_seed=0x5EED)
 WORKLOADS["switch_reroute"] = WORKLOADS["switch"].with_(name="switch_reroute", reroute=1)
 WORKLOADS["switch_rank"] = WORKLOADS["switch"].with_(name="switch_rank", reroute=1,
                                                      priority=MOE_PRIORITY_RANK)

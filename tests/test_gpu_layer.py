@@ -1,8 +1,11 @@
 """The whole layer at the workloads' full sizes, in the launch configuration the
-benchmark times (moe_layer_fwd on one stream). Routing, logits and outputs are
-compared with the oracle's own evaluation: on every token where the oracle
-finishes in seconds, else on seeded samples of tokens (the expert FFN of a
-token depends only on its own routing when nothing is dropped)."""
+benchmark times (moe_layer_fwd on one stream). Router logits and
+probabilities of every token are compared with the oracle's router; ids,
+gates, counts and slots of every token are compared bit for bit with the
+oracle's selection and capacity fed the GPU's own scores; y is compared with
+the oracle fed the GPU's routing on every token of the small cases and, at
+full size, on at least 256 tokens chosen to cover the grouped GEMM's tile
+boundaries (a token's output depends only on its own routing and rows)."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +14,7 @@ import oracle
 from sparse_mixture_experts_69_b300 import moe, synth
 from sparse_mixture_experts_69_b300.workloads import WORKLOADS, make_inputs
 
-from gpu_helpers import (TOL_AUX, TOL_LOGITS, TOL_Y, assert_maxabs, assert_rowwise,
+from gpu_helpers import (TOL_AUX, TOL_GATE, TOL_LOGITS, TOL_Y, assert_maxabs, assert_rowwise,
                          check_topk_valid, np32, oracle_noise, run_layer)
 
 pytestmark = pytest.mark.gpu
@@ -60,9 +63,78 @@ def _sample(T, n, seed):
     return sorted(set(synth.randint((n,), seed, 300, T).tolist()))
 
 
-def test_switch_full(cuda_device):
-    """Noisy top-1, capacity 128 with drops: every token routed by the oracle."""
-    wl = WORKLOADS["switch"]
+def _identical_scores(c, sel, probs):
+    """The oracle's top-k choice and gates taken on the GPU's own selection
+    scores and probabilities (the "identical router logits" comparison)."""
+    return oracle.select(np32(sel), np32(probs), c.top_k, bool(c.renorm_topk))
+
+
+def _boundary_tokens(cap, row_cap=128):
+    """Tokens whose rows sit where the grouped GEMM's tiles change: the first,
+    middle and last row tile of the heaviest expert, rows 128n-1 and 128n of
+    every expert that has them, every row of up to 16 experts small enough
+    for the 64-row tiles, and the first and last row of every expert."""
+    offsets, row_token = cap["offsets"], cap["row_token"]
+    kept = np.diff(offsets)
+    rows = set()
+    heavy = int(np.argmax(kept))
+    lo, n = int(offsets[heavy]), int(kept[heavy])
+    mid = (n // 2) // row_cap * row_cap
+    for r in list(range(0, min(n, 8))) + list(range(mid, min(n, mid + 8))) + \
+            list(range(max(0, n - 8), n)) + [n // row_cap * row_cap - 1]:
+        if 0 <= r < n:
+            rows.add(lo + r)
+    light = [e for e in range(len(kept)) if 0 < kept[e] <= 64][:16]
+    for e in light:
+        rows.update(range(int(offsets[e]), int(offsets[e + 1])))
+    for e in range(len(kept)):
+        a, m = int(offsets[e]), int(kept[e])
+        if m == 0:
+            continue
+        rows.update((a, a + m - 1))
+        for b in range(row_cap, m, row_cap):
+            rows.update((a + b - 1, a + b))
+    return sorted({int(row_token[r]) for r in rows}), heavy, light
+
+
+def _dispatch_full(c, x, ids, dev):
+    """moe_dispatch on the layer's ids: counts, kept, offsets, slot, xp, row_token."""
+    T, E, k, d = c.T, c.n_experts, c.top_k, c.d_model
+    C, R = moe.moe_capacity(c)
+    o = dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+             kept=torch.empty(E, dtype=torch.int32, device=dev),
+             offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+             slot=torch.empty((T, k), dtype=torch.int32, device=dev),
+             xp=torch.empty((R, d), dtype=c.torch_dtype, device=dev),
+             row_token=torch.empty(R, dtype=torch.int32, device=dev))
+    ws = moe.workspace(c, dev)
+    moe.moe_dispatch(c, x, ids, o["counts"], o["kept"], o["offsets"], o["slot"], o["xp"],
+                     o["row_token"], ws)
+    assert moe.moe_read_device_error(c, ws) == 0
+    return o, ws
+
+
+def _check_stats(c, o, probs):
+    """Layer statistics against the oracle's, computed from the GPU's own
+    probabilities, ids and gates."""
+    st = oracle.aux_stats(np32(probs), o["ids"].cpu().numpy(), np32(o["w"]), c.n_experts,
+                          c.importance_weight)
+    o3 = np32(o["out3"])
+    assert o3[0] == pytest.approx(st["aux"], rel=TOL_AUX)
+    assert o3[1] == pytest.approx(st["cv2"], rel=TOL_AUX)
+    assert o3[2] == pytest.approx(st["L_imp"], rel=TOL_AUX)
+    av = np32(o["aux_vecs"])
+    np.testing.assert_allclose(av[0], st["f"], rtol=1e-6)
+    np.testing.assert_allclose(av[1], st["P"], rtol=TOL_AUX)
+    np.testing.assert_allclose(av[2], st["I"], rtol=TOL_AUX)
+    return st
+
+
+@pytest.mark.parametrize("name", ["switch", "switch_drawn"])
+def test_switch_full(cuda_device, name):
+    """Noisy top-1, capacity 128 with drops (router noise passed in from the
+    host, or drawn by the library): every token routed by the oracle."""
+    wl = WORKLOADS[name]
     c = wl.cfg
     inp = make_inputs(wl, cuda_device)
     o, _ = run_layer(wl, inp, cuda_device)
@@ -71,70 +143,116 @@ def test_switch_full(cuda_device):
     assert_rowwise(np32(logits), r["z"], TOL_LOGITS, "logits")
     assert_rowwise(np32(probs), r["p"], TOL_LOGITS, "probs")
     ids = o["ids"].cpu().numpy()
+    # bit-exact on identical scores, valid against the oracle's own scores
+    ids_ref, w_ref = _identical_scores(c, sel, probs)
+    np.testing.assert_array_equal(ids, ids_ref)
     diff = check_topk_valid(ids, r["s"], c.top_k)
     assert len(diff) <= 2, diff
     assert np.all(np32(o["w"]) == 1.0)  # Softmax(KeepTopK(H, 1)) = 1
     C, _ = moe.moe_capacity(c)
-    cap = oracle.capacity(r["ids"], c.n_experts, C)
+    cap = oracle.capacity(ids_ref, c.n_experts, C)
+    np.testing.assert_array_equal(o["counts"].cpu().numpy(), cap["counts"])
     dropped = int((cap["slot"] < 0).sum())
     assert 200 < dropped < 600, dropped
-    touched = {int(ids[t, 0]) for t in diff} | {int(r["ids"][t, 0]) for t in diff}
-    if not diff:
-        np.testing.assert_array_equal(o["counts"].cpu().numpy(), cap["counts"])
-    tok = [t for t in _sample(c.T, 256, 1) if int(r["ids"][t, 0]) not in touched]
-    slot = cap["slot"][tok]
-    y_ref = _oracle_y(wl, inp, tok, r["ids"][tok], r["w"][tok], slot)
+    tok = sorted(set(_sample(c.T, 256, 1)) | set(_boundary_tokens(cap)[0]))
+    y_ref = _oracle_y(wl, inp, tok, ids[tok], w_ref[tok], cap["slot"][tok])
     assert_maxabs(np32(o["y"][torch.as_tensor(tok)]), y_ref, TOL_Y[c.dtype], "y")
     # dropped tokens of top-1 routing output exactly zero
-    dropped_tok = [t for t in range(c.T) if cap["slot"][t, 0] < 0 and int(r["ids"][t, 0]) not in touched]
-    assert dropped_tok and float(o["y"][torch.as_tensor(dropped_tok)].abs().max()) == 0.0
+    dropped_tok = np.nonzero(cap["slot"][:, 0] < 0)[0]
+    assert float(o["y"][torch.as_tensor(dropped_tok)].abs().max()) == 0.0
+    _check_stats(c, o, probs)
+    # the oracle's own statistics (its own probabilities and routing)
     st = oracle.aux_stats(r["p"].astype(np.float32), r["ids"], r["w"].astype(np.float32),
                           c.n_experts, c.importance_weight)
-    o3 = np32(o["out3"])
-    assert o3[0] == pytest.approx(st["aux"], rel=TOL_AUX)
-    assert o3[1] == pytest.approx(st["cv2"], rel=TOL_AUX)
-    av = np32(o["aux_vecs"])
-    if not diff:
-        np.testing.assert_allclose(av[0], st["f"], rtol=1e-6)
-        np.testing.assert_allclose(av[2], st["I"], rtol=TOL_AUX)
-    np.testing.assert_allclose(av[1], st["P"], rtol=TOL_AUX)
+    assert np32(o["out3"])[0] == pytest.approx(st["aux"], rel=1e-4)
 
 
-@pytest.mark.parametrize("name,n_tok", [("mixtral", 12), ("deepseek", 8), ("decode", 16)])
-def test_large_config_sampled(cuda_device, name, n_tok):
+@pytest.mark.parametrize("name", ["mixtral", "deepseek", "decode"])
+def test_large_config_full(cuda_device, name):
+    """The Mixtral-, DeepSeek- and decode-shaped layers at full size:
+    logits and probabilities of every token against the oracle's router;
+    ids, gates, counts, offsets, slots and rows of every token bit-exact
+    against the oracle's selection and capacity on the GPU's own scores; y
+    against the oracle on at least 256 tokens that include every tile
+    boundary kind; statistics and the bias update against the oracle."""
+    dev = cuda_device
     wl = WORKLOADS[name]
     c = wl.cfg
-    inp = make_inputs(wl, cuda_device)
-    o, ws = run_layer(wl, inp, cuda_device)
-    counts = o["counts"].cpu().numpy()
-    ids_all = o["ids"].cpu().numpy()
-    assert counts.sum() == c.T * c.top_k
-    np.testing.assert_array_equal(counts, np.bincount(ids_all.ravel(), minlength=c.n_experts))
-    logits, probs, sel, ids2, _ = _route(wl, inp, cuda_device)
-    np.testing.assert_array_equal(ids2.cpu().numpy(), ids_all)  # same routing, same bits
-    tok = _sample(c.T, n_tok, 2) if c.T > n_tok else list(range(c.T))
-    r = _oracle_router(wl, inp, tok)
-    tt = torch.as_tensor(tok)
-    assert_rowwise(np32(logits[tt]), r["z"], TOL_LOGITS, "logits")
-    assert_rowwise(np32(probs[tt]), r["p"], TOL_LOGITS, "probs")
-    diff = check_topk_valid(ids_all[tok], r["s"], c.top_k)
-    keep = [i for i in range(len(tok)) if i not in diff]
-    assert_rowwise(np32(o["w"][tt])[keep], r["w"][keep], TOL_LOGITS, "gates")
-    tok_k = [tok[i] for i in keep]
-    slot = np.zeros((len(tok_k), c.top_k), np.int32)  # dropless: every assignment kept
-    y_ref = _oracle_y(wl, inp, tok_k, r["ids"][keep], r["w"][keep], slot)
-    assert_maxabs(np32(o["y"][torch.as_tensor(tok_k)]), y_ref, TOL_Y[c.dtype], "y")
+    T, E, k = c.T, c.n_experts, c.top_k
+    inp = make_inputs(wl, dev)
+    o, ws = run_layer(wl, inp, dev)
+    logits, probs, sel, _, _ = _route(wl, inp, dev)
+    r = _oracle_router(wl, inp, list(range(T)))
+    assert_rowwise(np32(logits), r["z"], TOL_LOGITS, "logits")
+    assert_rowwise(np32(probs), r["p"], TOL_LOGITS, "probs")
+    ids = o["ids"].cpu().numpy()
+    ids_ref, w_ref = _identical_scores(c, sel, probs)
+    np.testing.assert_array_equal(ids, ids_ref)
+    assert_rowwise(np32(o["w"]), w_ref, TOL_GATE, "gates")
+    # the oracle's own routing differs only where its scores tie within 1e-5
+    diff = check_topk_valid(ids, r["s"], k)
+    srt = -np.sort(-r["s"], axis=1)[:, :k + 1]
+    gaps = (srt[:, :-1] - srt[:, 1:]).min(axis=1) / np.abs(r["s"]).max(axis=1)
+    assert set(diff) <= set(np.nonzero(gaps < 1e-5)[0].tolist())
+    C, R = moe.moe_capacity(c)
+    cap = oracle.capacity(ids_ref, E, C)
+    np.testing.assert_array_equal(o["counts"].cpu().numpy(), cap["counts"])
+    dp, _ = _dispatch_full(c, inp["x"], o["ids"], dev)
+    for key in ("counts", "kept", "offsets", "slot"):
+        np.testing.assert_array_equal(dp[key].cpu().numpy(), cap[key], err_msg=key)
+    n = int(cap["offsets"][-1])
+    np.testing.assert_array_equal(dp["row_token"][:n].cpu().numpy(), cap["row_token"])
+    # xp[row] is x[row_token[row]], byte for byte
+    assert torch.equal(dp["xp"][:n], inp["x"][dp["row_token"][:n].long()])
+    # y on boundary tokens plus a seeded sample, at least 256 tokens
+    btok, heavy, light = _boundary_tokens(cap)
+    tok = sorted(set(btok) | set(_sample(T, 256, 2)))
+    if len(tok) < min(256, T):
+        tok = sorted(set(tok) | set(range(min(256, T))))
+    assert len(tok) >= min(256, T)
+    if E > 64:
+        assert len(light) >= 8  # the 64-row MMA path is covered
+    y_ref = _oracle_y(wl, inp, tok, ids[tok], np.asarray(np32(o["w"]), np.float64)[tok],
+                      cap["slot"][tok])
+    assert_maxabs(np32(o["y"][torch.as_tensor(tok)]), y_ref, TOL_Y[c.dtype], "y")
+    _check_stats(c, o, probs)
     if wl.bias_rate:
-        # one loss-free bias update: experts above the mean load move down by the
-        # rate, below it up, at it not at all (bit-exact parity is a stage test)
         bias = inp["sel_bias"].clone()
         moe.moe_bias_update(c, o["counts"], bias, wl.bias_rate)
-        delta = (bias.cpu().double() - inp["sel_bias"].cpu().double()).numpy()
-        over = counts * c.n_experts > c.T * c.top_k
-        under = counts * c.n_experts < c.T * c.top_k
-        assert np.all(delta[over] < 0) and np.all(delta[under] > 0)
-        assert np.all(delta[~over & ~under] == 0)
-        assert np.allclose(np.abs(delta[over | under]), wl.bias_rate, rtol=1e-3)
+        want = oracle.bias_update(o["counts"].cpu(), inp["sel_bias"].cpu(), T, k, wl.bias_rate)
+        np.testing.assert_array_equal(bias.cpu().numpy(), want)
+
+
+def test_deepseek_whole_experts(cuda_device):
+    """moe_expert_ffn at the DeepSeek shape: every row of the heaviest routed
+    expert (dozens of 128-row tiles and a partial last one), every row of the
+    four lightest non-empty experts (64-row tiles) and every row of the
+    shared expert's first tile, against the oracle's expert FFN."""
+    dev = cuda_device
+    wl = WORKLOADS["deepseek"]
+    c = wl.cfg
+    inp = make_inputs(wl, dev)
+    _, _, _, ids, _ = _route(wl, inp, dev)
+    dp, ws = _dispatch_full(c, inp["x"], ids, dev)
+    C, R = moe.moe_capacity(c)
+    yp = torch.empty((R, c.d_model), dtype=c.torch_dtype, device=dev)
+    ys = torch.empty((c.n_shared, c.T, c.d_model), dtype=c.torch_dtype, device=dev)
+    moe.moe_expert_ffn(c, dp["xp"], dp["offsets"], inp["W1"], inp["W2"], inp["x"], inp["W1s"],
+                       inp["W2s"], yp, ys, ws)
+    assert moe.moe_read_device_error(c, ws) == 0
+    offsets = dp["offsets"].cpu().numpy()
+    kept = np.diff(offsets)
+    heavy = int(np.argmax(kept))
+    lightest = [int(e) for e in np.argsort(kept, kind="stable") if kept[e] > 0][:4]
+    assert kept[heavy] > 20 * 128 and all(kept[e] <= 64 for e in lightest)
+    for e in [heavy] + lightest:
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        ref = oracle.expert_ffn(dp["xp"][lo:hi].cpu(), inp["W1"][e].cpu(), inp["W2"][e].cpu(),
+                                c.act, oracle.ROUND_BF16)
+        assert_maxabs(np32(yp[lo:hi]), ref, TOL_Y[c.dtype], f"expert {e} ({hi - lo} rows)")
+    ref = oracle.expert_ffn(inp["x"][:128].cpu(), inp["W1s"][0].cpu(), inp["W2s"][0].cpu(),
+                            c.act, oracle.ROUND_BF16)
+    assert_maxabs(np32(ys[0, :128]), ref, TOL_Y[c.dtype], "shared expert")
 
 
 def test_layer_is_deterministic(cuda_device):

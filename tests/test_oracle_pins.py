@@ -440,11 +440,65 @@ def test_synth_deterministic_and_sliceable():
     torch.testing.assert_close(a, b, rtol=0, atol=0)
     tail = synth.normal((10, 33), seed=0, tid=100, offset=54 * 33)
     torch.testing.assert_close(a[54:], tail, rtol=0, atol=0)
+    # slices that start inside a Philox block and inside a Box-Muller pair
+    flat = a.view(-1)
+    for off in (1, 2, 3, 5, 7, 1001):
+        part = synth.normal((37,), seed=0, tid=100, offset=off)
+        torch.testing.assert_close(flat[off:off + 37], part, rtol=0, atol=0)
+    u = synth.uniform((50,), seed=4, tid=103, lo=0.0, hi=1.0)
+    torch.testing.assert_close(u[3:], synth.uniform((47,), seed=4, tid=103, lo=0.0, hi=1.0,
+                                                    offset=3), rtol=0, atol=0)
     assert not torch.equal(a, synth.normal((64, 33), seed=1, tid=100))
+    assert not torch.equal(a, synth.normal((64, 33), seed=0, tid=101))
     v = synth.normal((200000,), seed=3, tid=101, std=0.02).double()
     assert abs(v.mean().item()) < 3e-4 and abs(v.std().item() / 0.02 - 1) < 0.01
     u = synth.uniform((100000,), seed=3, tid=102, lo=-0.1, hi=0.1).double()
     assert u.min() >= -0.1 and u.max() < 0.1 and abs(u.mean().item()) < 2e-3
+    r = synth.randint((100000,), seed=3, tid=104, high=7)
+    assert r.min() == 0 and r.max() == 6
+    assert np.abs(np.bincount(r.numpy(), minlength=7) / 1e5 - 1 / 7).max() < 5e-3
+
+
+# Known-answer vectors published with Philox4x32-10 (counter, key -> output)
+PHILOX_KAT = [
+    ((0x00000000, 0x00000000, 0x00000000, 0x00000000), (0x00000000, 0x00000000),
+     (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((0xFFFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF), (0xFFFFFFFF, 0xFFFFFFFF),
+     (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
+
+
+@pytest.mark.parametrize("ctr,key,want", PHILOX_KAT)
+def test_synth_philox_known_answers(ctr, key, want):
+    c = [torch.tensor([v], dtype=torch.int64) for v in ctr]
+    out = synth.philox(*c, key[0], key[1])
+    assert [int(o) for o in out] == list(want)
+
+
+def test_synth_normal_is_standard_normal():
+    """The inputs the workloads state as N(0,1): mean, variance, the
+    Kolmogorov-Smirnov distance to the normal CDF over two million draws,
+    symmetry, the tail masses beyond 3 and 4 sigma, and no correlation
+    between the cos and sin halves of a Box-Muller pair."""
+    from scipy import stats
+    z = synth.normal((1 << 21,), seed=11, tid=105, dtype=torch.float64).numpy()
+    n = z.size
+    assert abs(z.mean()) < 5 / np.sqrt(n)
+    assert abs(z.var() - 1.0) < 5 * np.sqrt(2.0 / n)
+    assert stats.kstest(z, "norm").statistic < 2.0 / np.sqrt(n)
+    assert abs((z > 0).mean() - 0.5) < 5 * 0.5 / np.sqrt(n)
+    for c in (3.0, 4.0):
+        tail = (np.abs(z) > c).mean()
+        want = 2 * stats.norm.sf(c)
+        assert abs(tail - want) < 5 * np.sqrt(want / n) + 1e-7, (c, tail, want)
+    assert np.abs(z).max() < 6.7  # 32-bit uniforms bound |z| by sqrt(64 ln 2)
+    pair = z.reshape(-1, 2)
+    assert abs(np.corrcoef(pair[:, 0], pair[:, 1])[0, 1]) < 5 / np.sqrt(n / 2)
+    # bf16 / fp32 values are the float64 draws rounded once more
+    zb = synth.normal((4096,), seed=11, tid=105, dtype=torch.bfloat16)
+    torch.testing.assert_close(zb, torch.from_numpy(z[:4096]).float().bfloat16(), rtol=0, atol=0)
 
 
 def test_importance_sums_the_gates():

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from sparse_mixture_experts_69_b300 import moe, synth
 
 from gpu_helpers import TOL_AUX, np32
@@ -44,8 +45,12 @@ def test_noalloc_matches_workspace_version_on_consecutive_calls(cuda_device):
         f1, P1, I1, o1 = _outs(E, dev)
         moe.moe_aux_stats_noalloc(cfg, probs, ids, w, f1, P1, I1, o1)
         torch.cuda.synchronize()
-        for a, b, name in [(f1, f0, "f"), (P1, P0, "P"), (I1, I0, "importance"),
-                           (o1, o0, "aux/cv2/L")]:
+        ref = oracle.aux_stats(probs.cpu(), ids.cpu(), w.cpu(), E, cfg.importance_weight)
+        ref3 = [ref["aux"], ref["cv2"], ref["L_imp"]]
+        for a, b, r, name in [(f1, f0, ref["f"], "f"), (P1, P0, ref["P"], "P"),
+                              (I1, I0, ref["I"], "importance"), (o1, o0, ref3, "aux/cv2/L")]:
+            np.testing.assert_allclose(np32(a), r, rtol=TOL_AUX, atol=0,
+                                       err_msg=f"call {call} {name} vs the oracle")
             np.testing.assert_allclose(np32(a), np32(b), rtol=TOL_AUX, err_msg=f"call {call} {name}")
         assert np32(o1)[0] > 0.0  # outputs were written
 
