@@ -59,6 +59,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-route", action="store_true",
                     help="time moe_route alone on the headline workload (no expert weights)")
+    ap.add_argument("--override", default="",
+                    help="comma-separated field=value changes to the headline workload "
+                         "(e.g. d_ff=64 keeps the router, dispatch and combine shapes of a "
+                         "layer with small expert weights, for profiling)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -663,12 +667,25 @@ def measure(wl, steps, warmup, dev, pg, world, local, cpu_budget, want_cpu, auto
     return rec
 
 
+def headline_workload(a):
+    """The --workload entry of WORKLOADS with the --override changes."""
+    from sparse_mixture_experts_69_b300.workloads import WORKLOADS
+    wl = WORKLOADS[a.workload]
+    kw = {}
+    for item in filter(None, a.override.split(",")):
+        key, val = item.split("=", 1)
+        kw[key.strip()] = float(val) if "." in val else int(val, 0)
+    if kw:
+        wl = wl.with_(name=wl.name + "[" + a.override + "]", **kw)
+    return wl
+
+
 def run_only_route(a, dev):
     """Time moe_route alone on the headline workload (router inputs only, no
     expert weights): its HBM rate against the measured peak."""
     from sparse_mixture_experts_69_b300 import moe
-    from sparse_mixture_experts_69_b300.workloads import WORKLOADS, make_inputs
-    wl = WORKLOADS[a.workload]
+    from sparse_mixture_experts_69_b300.workloads import make_inputs
+    wl = headline_workload(a)
     c = wl.cfg
     T, E, d, nc = c.T, c.n_experts, c.d_model, c.n_cand
     inp = make_inputs(wl, dev, experts=False)
@@ -723,7 +740,7 @@ def main():
 
     from sparse_mixture_experts_69_b300.workloads import WORKLOADS
 
-    wl = WORKLOADS[a.workload].with_(seed=rank)
+    wl = headline_workload(a).with_(seed=rank)
     head = measure(wl, a.steps, a.warmup, dev, pg, world, local, 12.0,
                    not a.no_cpu_baseline and rank == 0)
     torch.cuda.empty_cache()

@@ -347,9 +347,10 @@ MOE_API moe_status moe_aux_stats_noalloc(const moe_config* cfg, const float* pro
                                          float* f, float* P, float* importance, float* out3,
                                          moe_stream_t stream);
 
-/* Limits of the library's bounded device waits. Settings of the process,
- * read when a kernel is enqueued, so they apply to every call made after
- * this one, on every thread and device.
+/* Limits of the library's bounded device waits, and a switch that makes one
+ * of them run out on purpose. Settings of the process, read when a kernel is
+ * enqueued, so they apply to every call made after this one, on every thread
+ * and device.
  *   wait_ns        time limit of each pipeline wait of the tensor-core GEMM
  *                  kernels (the router and expert GEMMs); 0 restores the
  *                  default of 2 s. A wait that runs out records
@@ -361,11 +362,18 @@ MOE_API moe_status moe_aux_stats_noalloc(const moe_config* cfg, const float* pro
  *                  re-routing or rank priority (moe_dispatch); 0 restores the
  *                  default of 4096; if the loop has not settled by then it
  *                  records MOE_ERR_TIMEOUT and writes the slots of its last
- *                  pass (every row index still in range). Negative values
- *                  return MOE_ERR_INVALID_ARG.
- * No device work: the defaults never run out on a working GPU, and lowering
- * them exists to exercise the failure path. Host only. */
-MOE_API moe_status moe_set_wait_limits(uint64_t wait_ns, int32_t policy_passes);
+ *                  pass (every row index still in range).
+ *   hold_first_accumulator
+ *                  1: in every CTA of the tensor-core GEMM kernels the thread
+ *                  issuing the matrix operations withholds the signal that
+ *                  the first tile's accumulator is ready, so the epilogue's
+ *                  wait for it can only end by running out after wait_ns:
+ *                  a way to exercise the failure path without a fault. 0 for
+ *                  normal operation.
+ * Negative or out-of-range values return MOE_ERR_INVALID_ARG. No device work:
+ * the defaults never run out on a working GPU. Host only. */
+MOE_API moe_status moe_set_wait_limits(uint64_t wait_ns, int32_t policy_passes,
+                                       int32_t hold_first_accumulator);
 
 /* Synchronise `stream`, read and clear the workspace status word, and map it
  * to MOE_OK, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_ARG (the

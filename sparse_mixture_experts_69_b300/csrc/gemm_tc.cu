@@ -36,9 +36,6 @@
 #ifndef MOE_TC_PROMO
 #define MOE_TC_PROMO 2  // L2 promotion of TMA loads: 0 none, 1 128 B, 2 256 B
 #endif
-#ifndef MOE_TC_ROT
-#define MOE_TC_ROT 0  // 1: each tile starts its k loop at a tile-dependent block
-#endif
 #ifndef MOE_TC_BN_ACT
 #define MOE_TC_BN_ACT 256  // output tile width of the ReLU/GELU/plain expert GEMMs
 #endif
@@ -71,7 +68,16 @@ struct TcArgs {
     float* logits;        // router: [T,E]
     float* zn;            // router: [T,E] or NULL
     int E_router;         // router: columns < E_router are logits
+    // router with its K range split over ksplit CTAs per output tile: CTA part
+    // s writes its raw fp32 sums to part[s][T][N] (logits, zn, offset unused);
+    // the selection kernel adds the parts in order s = 0, 1, ...
+    int ksplit;
+    float* part;
     unsigned long long wait_ns;  // limit of each pipeline mbarrier wait
+    // 1: the MMA warp withholds the "accumulator ready" signal of its CTA's
+    // first tile, so the epilogue's first wait can only end by running out
+    // (moe_set_wait_limits; tests of the failure path)
+    int hold_first_acc;
 };
 
 template <int BN>
@@ -413,7 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
         build_tile_table<false>(p, BM, mt_start, grows);
     __syncthreads();
-    const int total = mt_start[G] * nt;
+    // work items: output tiles, times the K parts of a split router GEMM
+    const int ks = EPI == EPI_ROUTER ? args.ksplit : 1;
+    const int total = mt_start[G] * nt * ks;
     // no work: leave before any allocation (CTA 0 stays when it owes the
     // statistics finalisation); every CTA passes the wait before it exits, so
     // this kernel completes only after the preceding one has
@@ -441,17 +449,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_w = WEF ? l2_evict_first_policy() : 0ull;
     int prefilled = 0;
     if (early && threadIdx.x == 0) {
-        for (int tile = blockIdx.x; tile < total && prefilled < C::STAGES; tile += gridDim.x) {
+        for (int w = blockIdx.x; w < total && prefilled < C::STAGES; w += gridDim.x) {
+            const int tile = w / ks, sp = w - tile * ks;
             const GroupTile gt = decode_tile<true>(p, mt_start, nt, BM, tile);
             const CUtensorMap* mb = gt.g < p.E ? &tmB0 : &tmB1;
             int brow[C::B_LOADS];
             b_tile_rows<BN, EPI>(p, gt, brow);
-            for (int kb0 = 0; kb0 < nkb && prefilled < C::STAGES; ++kb0) {
-                const int rot = MOE_TC_ROT ? tile % nkb : 0;
-                const int kb = kb0 + rot < nkb ? kb0 + rot : kb0 + rot - nkb;
+            const int kb_hi = (sp + 1) * nkb / ks;
+            for (int kb = sp * nkb / ks; kb < kb_hi && prefilled < C::STAGES; ++kb) {
                 mbar_arrive_expect_tx(&full[prefilled], C::STAGE_BYTES);
                 load_b_stage<BN, WEF>(sB + prefilled * C::B_BYTES, mb, &full[prefilled], kb, brow,
-                                 pol_w);
+                                      pol_w);
                 ++prefilled;
             }
         }
@@ -477,16 +485,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t filled = 0, fill_parity = 0;
             bool ok = true;
             int item = 0;  // (tile, k block) pairs issued so far
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const int tile = w / ks, sp = w - tile * ks;
                 const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
                 const bool routed = gt.g < p.E;
                 const CUtensorMap* ma = routed ? &tmA0 : &tmA1;
                 const CUtensorMap* mb = routed ? &tmB0 : &tmB1;
                 int brow[C::B_LOADS];
                 b_tile_rows<BN, EPI>(p, gt, brow);
-                const int rot = MOE_TC_ROT ? tile % nkb : 0;
-                for (int kb0 = 0; kb0 < nkb; ++kb0, ++item) {
-                    const int kb = kb0 + rot < nkb ? kb0 + rot : kb0 + rot - nkb;
+                const int kb_hi = (sp + 1) * nkb / ks;
+                for (int kb = sp * nkb / ks; kb < kb_hi; ++kb, ++item) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, args.wait_ns)) {
                         ok = false;
                         break;
@@ -525,7 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int local = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++local) {
+                const int tile = w / ks, sp = w - tile * ks;
                 const int b = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
                 if (!mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.status, args.wait_ns)) {
@@ -538,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool m64 =
                     EPI != EPI_ROUTER && tile_rows(mt_start, grows, G, nt, BM, tile) <= 64;
                 const uint32_t idesc = m64 ? C::IDESC64 : C::IDESC;
-                for (int kb = 0; kb < nkb; ++kb) {
+                const int kb_lo = sp * nkb / ks, kb_hi = (sp + 1) * nkb / ks;
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, p.status, args.wait_ns)) {
                         ok = false;
                         break;
@@ -553,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < BKH / 16; ++kk)
                             umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
-                                      (kb | hk | kk) != 0 ? 1u : 0u);
+                                      (kb != kb_lo || hk | kk) ? 1u : 0u);
                     }
                     umma_commit(&empty[stage]);
                     if (++stage == C::STAGES) {
@@ -561,9 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phase ^= 1;
                     }
                 }
-                if (ok) umma_commit(&tfull[b]);
+                if (ok && !(args.hold_first_acc && local == 0)) umma_commit(&tfull[b]);
             }
-            if (!ok) {
+            if (!ok || args.hold_first_acc) {
+                // every MMA this thread issued completes before TMEM is freed
                 umma_commit(drain);
                 volatile int never = 0;
                 mbar_wait(drain, 0, &never, p.status, kDrainNs);
@@ -582,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * q + lane;
         const uint64_t pol_o = l2_evict_last_policy();
         int local = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+        for (int w = blockIdx.x; w < total; w += gridDim.x, ++local) {
+            const int tile = w / ks, sp = w - tile * ks;
             const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
             const int b = local & 1;
             const uint32_t tph = (local >> 1) & 1;
@@ -609,7 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = v[i];
                     __syncwarp();
                     const int n = gt.n_tile * BN + c + lane;
-                    if (n < p.N) {
+                    if (n < p.N && args.part) {
+                        float* dst = args.part + (size_t)sp * p.T * p.N + n;
+                        for (int r = 0; r < rows_here; ++r)
+                            dst[(size_t)(gt.out_row + 32 * q + r) * p.N] = stg[r * 33 + lane];
+                    } else if (n < p.N) {
                         const bool is_logit = n < E_r;
                         const float off = (is_logit && args.offset) ? args.offset[n] : 0.f;
                         float* dst = is_logit ? args.logits + n : args.zn + (n - E_r);
@@ -733,7 +749,7 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     const long long nt = (p.N + ncol_tile - 1) / ncol_tile;
     long long mt = (long long)p.max_rows0 / BM + p.E + (long long)p.S * ((p.T + BM - 1) / BM);
     if (p.E == 0) mt = (long long)p.S * ((p.T + BM - 1) / BM);
-    const long long bound = std::max<long long>(1, mt * nt);
+    const long long bound = std::max<long long>(1, mt * nt * (EPI == EPI_ROUTER ? a.ksplit : 1));
     const int grid = (int)std::min<long long>(bound, num_sms());
     return launch_k(grouped_gemm_tc_kernel<BN, EPI, WEF>, dim3(grid), dim3(kThreads), smem, st, mA0,
                     mA1, mB0, mB1, a);
@@ -744,7 +760,9 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
 cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStream_t st) {
     tc::TcArgs a{};
     a.p = g;
+    a.ksplit = 1;
     a.wait_ns = wait_limit_ns();
+    a.hold_first_acc = hold_first_accumulator();
     const bool wef = MOE_TC_L2_HINTS && g.b_evict_first;
     if (g.glu)
         return wef ? tc::launch<256, tc::EPI_GLU, true>(a, st)
@@ -753,9 +771,27 @@ cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStr
                : tc::launch<MOE_TC_BN_ACT, tc::EPI_ACT, false>(a, st);
 }
 
+// Plan of the router GEMM (T x Nr outputs, K = d). The column tile is the
+// narrowest of 32/64/128/256 that covers Nr, so x is read once per row tile.
+// When the output tiles would leave SMs idle, the K range of each tile is
+// split over 2, 4, ... CTAs (each keeping at least 4 blocks of K) while the
+// work items fit one wave. The plan assumes a 148-SM part whatever the
+// device, so the split, and with it every rounding of the logits, is the
+// same on any GPU.
+void router_plan(int T, int d, int Nr, int* bn, int* ksplit) {
+    constexpr int kPlanSms = 148;
+    const int b = Nr <= 32 ? 32 : Nr <= 64 ? 64 : Nr <= 128 ? 128 : 256;
+    const long long tiles = (long long)((T + tc::BM - 1) / tc::BM) * ((Nr + b - 1) / b);
+    const int nkb = (d + tc::BK - 1) / tc::BK;
+    int s = 1;
+    while (tiles * s * 2 <= kPlanSms && nkb / (s * 2) >= 4) s *= 2;
+    *bn = b;
+    *ksplit = s;
+}
+
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
-                                    const float* offset, float* logits, float* zn, int* status,
-                                    cudaStream_t st) {
+                                    const float* offset, float* logits, float* zn, float* part,
+                                    int* status, cudaStream_t st) {
     tc::TcArgs a{};
     GroupedGemm& p = a.p;
     p.offsets = nullptr;
@@ -784,11 +820,12 @@ cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const
     a.zn = zn;
     a.E_router = s.E;
     a.wait_ns = wait_limit_ns();
-    // Narrowest tile that covers Nr, halved while that leaves too few tiles to
-    // keep most SMs streaming x (the router reads T d b bytes of x and little else).
-    const int mt = (s.T + tc::BM - 1) / tc::BM;
-    int bn = Nr <= 32 ? 32 : Nr <= 64 ? 64 : Nr <= 128 ? 128 : 256;
-    while (bn > 32 && mt * ((Nr + bn - 1) / bn) < (3 * num_sms()) / 4) bn >>= 1;
+    a.hold_first_acc = hold_first_accumulator();
+    int bn, ks;
+    router_plan(s.T, s.d, Nr, &bn, &ks);
+    a.ksplit = ks;
+    a.part = ks > 1 ? part : nullptr;
+    if (ks > 1 && !part) return cudaErrorInvalidValue;
     if (bn == 32) return tc::launch<32, tc::EPI_ROUTER, false>(a, st);
     if (bn == 64) return tc::launch<64, tc::EPI_ROUTER, false>(a, st);
     if (bn == 128) return tc::launch<128, tc::EPI_ROUTER, false>(a, st);

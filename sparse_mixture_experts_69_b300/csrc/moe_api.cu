@@ -34,10 +34,12 @@ int num_sms() {
 namespace {
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 std::atomic<int> g_policy_passes{kDefaultPolicyPasses};
+std::atomic<int> g_hold_first_acc{0};
 }  // namespace
 
 unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 int policy_max_passes() { return g_policy_passes.load(std::memory_order_relaxed); }
+int hold_first_accumulator() { return g_hold_first_acc.load(std::memory_order_relaxed); }
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -59,6 +61,14 @@ WsLayout ws_layout(const Shape& s) {
     L.seq_ticket = take(16);
     L.zero_end = off;
     L.zn = take(T * E * 4);
+    size_t part = 0;  // K parts of the router GEMM, for Nr = E or 2E (noisy)
+    if (s.dtype == MOE_BF16)
+        for (int nr = (int)E; nr <= 2 * (int)E; nr += (int)E) {
+            int bn, ks;
+            router_plan(s.T, s.d, nr, &bn, &ks);
+            if (ks > 1) part = std::max(part, (size_t)ks * T * nr * 4);
+        }
+    L.rpart = take(part);
     L.wgT = take(2 * E * d * es);
     L.logits = take(T * E * 4);
     L.probs = take(T * E * 4);
@@ -202,10 +212,18 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x
     const bool noisy = Wnoise != nullptr;
     const int Nr = noisy ? 2 * s.E : s.E;
     float* zn = noisy ? at<float>(ws, L.zn) : nullptr;
+    RouterLogits rl{logits, zn, nullptr, 1, Nr, offset};
     if (s.dtype == MOE_BF16) {
         void* wgT = at<void>(ws, L.wgT);
+        int bn, ks;
+        router_plan(s.T, s.d, Nr, &bn, &ks);
+        if (ks > 1) {
+            rl.part = at<float>(ws, L.rpart);
+            rl.nsplit = ks;
+        }
         MOE_CUDA(launch_transpose_router_w(s, Wg, Wnoise, wgT, st));
-        MOE_CUDA(launch_router_gemm_bf16(s, Nr, x, wgT, offset, logits, zn, status, st));
+        MOE_CUDA(launch_router_gemm_bf16(s, Nr, x, wgT, offset, logits, zn,
+                                         at<float>(ws, L.rpart), status, st));
     } else {
         MOE_CUDA(launch_router_gemm_f32(s, Nr, static_cast<const float*>(x),
                                         static_cast<const float*>(Wg),
@@ -214,15 +232,17 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x
     }
     if (aux_out3) {
         // bf16: the up GEMM (tcgen05) finalises the statistics later in the layer
-        MOE_CUDA(launch_router_select_fused(s, logits, zn, noisy ? noise : nullptr, bias, probs,
-                                            ids, w, status,
+        MOE_CUDA(launch_router_select_fused(s, rl, noisy ? noise : nullptr, bias, probs, ids, w,
+                                            status,
                                             uses_policy(s) ? nullptr : at<int32_t>(ws, L.blk_hist),
                                             at<void>(ws, L.aux_acc), aux_vecs, aux_vecs + s.E,
                                             aux_vecs + 2 * s.E, aux_out3,
                                             s.dtype == MOE_BF16, st));
     } else {
-        MOE_CUDA(launch_router_select(s, logits, zn, noisy ? noise : nullptr, bias, probs, sel,
-                                      ids, w, 0, nullptr, nullptr, status, st));
+        // moe_route's logits are an output: formed here when the GEMM was split
+        MOE_CUDA(launch_router_select(s, rl, rl.nsplit > 1 ? logits : nullptr,
+                                      noisy ? noise : nullptr, bias, probs, sel, ids, w, 0,
+                                      nullptr, nullptr, status, st));
     }
     return MOE_OK;
 }
@@ -405,7 +425,8 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const void* W
         return MOE_ERR_INVALID_ARG;
     if (from_scores) {
         if (!sel_scores) return MOE_ERR_INVALID_ARG;
-        MOE_CUDA(launch_router_select(s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+        const RouterLogits none{nullptr, nullptr, nullptr, 1, s.E, nullptr};
+        MOE_CUDA(launch_router_select(s, none, nullptr, nullptr, nullptr, nullptr, nullptr,
                                       topk_ids, topk_w, 1, sel_scores, probs,
                                       at<int>(ws, L.status), st));
         return MOE_OK;
@@ -621,10 +642,13 @@ MOE_API moe_status moe_seq_aux_stats(const moe_config* cfg, const float* probs,
     return MOE_OK;
 }
 
-MOE_API moe_status moe_set_wait_limits(uint64_t wait_ns, int32_t policy_passes) {
-    if (policy_passes < 0) return MOE_ERR_INVALID_ARG;
+MOE_API moe_status moe_set_wait_limits(uint64_t wait_ns, int32_t policy_passes,
+                                       int32_t hold_first_accumulator) {
+    if (policy_passes < 0 || (hold_first_accumulator != 0 && hold_first_accumulator != 1))
+        return MOE_ERR_INVALID_ARG;
     g_wait_ns.store(wait_ns ? (unsigned long long)wait_ns : kDefaultWaitNs);
     g_policy_passes.store(policy_passes ? policy_passes : kDefaultPolicyPasses);
+    g_hold_first_acc.store(hold_first_accumulator);
     return MOE_OK;
 }
 

@@ -57,6 +57,7 @@ struct WsLayout {
     size_t seq_ticket; // u32 ticket of the sequence-statistics kernel
     size_t zero_end;   // end of the zero-between-calls prefix
     size_t zn;         // [T,E] f32 noise logits x.Wnoise
+    size_t rpart;      // K parts of a split router GEMM (router_plan), bf16 only
     size_t wgT;        // [Nr,d] dtype: Wg^T (rows 0..E-1) and Wnoise^T (E..2E-1)
     size_t logits;     // [T,E] f32 (layer only)
     size_t probs;      // [T,E] f32 (layer only)
@@ -96,15 +97,32 @@ cudaError_t launch_transpose_router_w(const Shape& s, const void* Wg, const void
 cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const float* Wg,
                                    const float* Wnoise, const float* offset, float* logits,
                                    float* zn, cudaStream_t st);
-// Router GEMM for bf16 inputs (tcgen05)
+// Router GEMM for bf16 inputs (tcgen05). router_plan gives its column tile
+// width and K split; with a split (ksplit > 1) the kernel writes the raw parts
+// to part [ksplit][T][Nr] and logits, zn and offset are left to the selection
+// kernel, otherwise it writes logits (+ offset) and zn itself.
+void router_plan(int T, int d, int Nr, int* bn, int* ksplit);
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
-                                    const float* offset, float* logits, float* zn, int* status,
-                                    cudaStream_t st);
+                                    const float* offset, float* logits, float* zn, float* part,
+                                    int* status, cudaStream_t st);
 // The router's standard-normal draws for (s.noise_seed, s.noise_counter), [T,E]
 cudaError_t launch_draw_noise(const Shape& s, float* noise, cudaStream_t st);
 
-// Noise, softmax, selection bias, top-k, gates
-cudaError_t launch_router_select(const Shape& s, const float* logits, const float* zn,
+// The router GEMM's output as the selection kernels read it: logits and zn,
+// or (nsplit > 1) the K parts part [nsplit][T][Nr] of [logits | zn] without
+// the offset, which the selection kernel adds up in order and then adds the
+// offset to.
+struct RouterLogits {
+    const float* logits;  // [T,E] (nsplit <= 1)
+    const float* zn;      // [T,E] or NULL (nsplit <= 1)
+    const float* part;    // [nsplit][T][Nr] (nsplit > 1)
+    int nsplit, Nr;
+    const float* offset;  // [E] or NULL (added when nsplit > 1)
+};
+
+// Noise, softmax, selection bias, top-k, gates. logits_out (or NULL) receives
+// the logits when the selection kernel forms them from K parts.
+cudaError_t launch_router_select(const Shape& s, const RouterLogits& rl, float* logits_out,
                                  const float* noise, const float* bias, float* probs,
                                  float* sel, int32_t* ids, float* w, int from_scores,
                                  const float* sel_in, const float* probs_in, int* status,
@@ -113,7 +131,7 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
 // Layer path: selection + capacity histogram + statistics in one kernel
 // defer_final: only add the statistics sums; a later kernel of the layer (the
 // up GEMM) turns them into f, P, importance, aux and CV^2.
-cudaError_t launch_router_select_fused(const Shape& s, const float* logits, const float* zn,
+cudaError_t launch_router_select_fused(const Shape& s, const RouterLogits& rl,
                                        const float* noise, const float* bias, float* probs,
                                        int32_t* ids, float* w, int* status, int32_t* blk_hist,
                                        void* acc_mem, float* f, float* P, float* I, float* out3,
@@ -218,12 +236,14 @@ cudaError_t launch_bias_update(const Shape& s, const int32_t* counts, float* bia
 int num_sms();
 
 // Limits of the bounded device waits (moe_set_wait_limits): the time limit of
-// each tcgen05 pipeline mbarrier wait, and the pass limit of the capacity
-// policy's fixed-point loop. Read at launch time.
+// each tcgen05 pipeline mbarrier wait, the pass limit of the capacity
+// policy's fixed-point loop, and the test switch that makes the tcgen05
+// kernels withhold their first "accumulator ready" signal. Read at launch time.
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 constexpr int kDefaultPolicyPasses = 4096;
 unsigned long long wait_limit_ns();
 int policy_max_passes();
+int hold_first_accumulator();
 
 // ------------------------------------------------- programmatic dependent launch
 // Every kernel is launched with programmatic stream serialisation: it may be

@@ -118,8 +118,8 @@ cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const
 // ------------------------------------------------------------------ selection
 struct SelectArgs {
     int T, E, k, nc, renorm, from_scores;  // nc >= k candidates are written
-    const float* logits;   // [T,E] z
-    const float* zn;       // [T,E] x.Wnoise or NULL
+    RouterLogits rl;       // z = x.Wg (+ offset) and zn = x.Wnoise, or their K parts
+    float* logits_out;     // [T,E] or NULL: z, written when formed from K parts
     const float* noise;    // [T,E] or NULL
     int draw;              // 1: noise drawn from (seed, ctr) instead of read
     unsigned long long seed, ctr;
@@ -194,11 +194,44 @@ struct TokenRegs {
     float eps[EPL];  // standard-normal noise
 };
 
-template <int EPL>
+// PARTS: the logits come as K parts of the router GEMM (a.rl.nsplit > 1).
+template <int EPL, bool PARTS>
 __device__ __forceinline__ void load_token(const SelectArgs& a, int t, TokenRegs<EPL>& r) {
     const int lane = threadIdx.x & 31;
     const size_t row = (size_t)t * a.E;
-    const bool noisy = a.zn && (a.noise || a.draw);
+    const bool noisy = a.rl.zn && (a.noise || a.draw);
+    const RouterLogits& rl = a.rl;
+    if (PARTS) {
+        // the K parts of [z | zn], added in part order, then the offset
+        const size_t plane = (size_t)a.T * rl.Nr;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            r.z[i] = 0.f;
+            r.zn[i] = 0.f;
+        }
+        for (int q = 0; q < rl.nsplit; ++q) {
+            const float* pr = rl.part + q * plane + (size_t)t * rl.Nr;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < a.E) {
+                    r.z[i] += pr[e];
+                    if (noisy) r.zn[i] += pr[a.E + e];
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (!a.draw) r.eps[i] = 0.f;
+            if (e < a.E) {
+                if (rl.offset) r.z[i] += rl.offset[e];
+                if (a.logits_out) a.logits_out[row + e] = r.z[i];
+                if (noisy && !a.draw) r.eps[i] = a.noise[row + e];
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
@@ -208,8 +241,8 @@ __device__ __forceinline__ void load_token(const SelectArgs& a, int t, TokenRegs
             r.z[i] = in ? a.sel_in[row + e] : 0.f;
             r.zn[i] = in ? a.probs_in[row + e] : 0.f;
         } else {
-            r.z[i] = in ? a.logits[row + e] : 0.f;
-            r.zn[i] = in && noisy ? a.zn[row + e] : 0.f;
+            r.z[i] = in ? rl.logits[row + e] : 0.f;
+            r.zn[i] = in && noisy ? rl.zn[row + e] : 0.f;
             if (in && noisy && !a.draw) r.eps[i] = a.noise[row + e];
         }
     }
@@ -227,6 +260,38 @@ __device__ __forceinline__ void draw_token_eps(const SelectArgs& a, int t, Token
     }
 }
 
+// Sorts n = EPL (a power of two, at most 8) (key, expert, probability)
+// triples into descending key order, equal keys by ascending expert, with a
+// bitonic network of compile-time compare-exchanges (registers only).
+template <int N>
+__device__ __forceinline__ void sort_desc(unsigned (&k)[N], int (&e)[N], float (&p)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    // within each bitonic block of `size`, the first half of
+                    // the blocks sorts descending, the second ascending
+                    const bool desc = ((i & size) == 0) || size == N;
+                    const bool j_first = k[j] > k[i] || (k[j] == k[i] && e[j] < e[i]);
+                    if (j_first == desc) {
+                        const unsigned tk = k[i];
+                        k[i] = k[j];
+                        k[j] = tk;
+                        const int te = e[i];
+                        e[i] = e[j];
+                        e[j] = te;
+                        const float tp = p[i];
+                        p[i] = p[j];
+                        p[j] = tp;
+                    }
+                }
+            }
+}
+
 // Selection for token t from its loaded inputs. On return pr[] holds this
 // lane's probabilities, and lanes j < nc hold the j-th candidate (my_id) and
 // its gate (my_w): p_j over the sum of p of the first k candidates (renorm),
@@ -237,18 +302,24 @@ __device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const To
     const int lane = threadIdx.x & 31;
     const int E = a.E;
     const size_t row = (size_t)t * E;
-    float sc[EPL];
+    // Scores become unsigned keys in the same order (sign flip of the float's
+    // bits; -0 is first made +0 so the two compare equal, as floats do).
+    unsigned key[EPL];
     bool nonfinite = false;
+    auto to_key = [](float v) {
+        const unsigned b = __float_as_uint(__fadd_rn(v, 0.f));
+        return b ^ ((b >> 31) ? 0xFFFFFFFFu : 0x80000000u);
+    };
     if (a.from_scores) {
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
-            sc[i] = e < E ? r.z[i] : -FLT_MAX;
+            key[i] = e < E ? to_key(r.z[i]) : 0u;
             pr[i] = e < E ? r.zn[i] : 0.f;
-            if (e < E && !isfinite(sc[i])) nonfinite = true;
+            if (e < E && !isfinite(r.z[i])) nonfinite = true;
         }
     } else {
-        const bool noisy = a.zn && (a.noise || a.draw);
+        const bool noisy = a.rl.zn && (a.noise || a.draw);
         float H[EPL];
         float m = -FLT_MAX;
 #pragma unroll
@@ -276,54 +347,85 @@ __device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const To
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
+            key[i] = 0u;
             if (e < E) {
                 pr[i] = pr[i] * inv;
                 a.probs[row + e] = pr[i];
-                sc[i] = a.bias ? pr[i] + a.bias[e] : H[i];
-                if (a.sel) a.sel[row + e] = sc[i];
-            } else {
-                sc[i] = -FLT_MAX;
+                const float sc = a.bias ? pr[i] + a.bias[e] : H[i];
+                if (a.sel) a.sel[row + e] = sc;
+                key[i] = to_key(sc);
             }
         }
     }
     if (__any_sync(0xffffffffu, nonfinite) && lane == 0) flag_status(a.status, DEV_NONFINITE);
 
-    // top-nc: nc rounds of a warp arg-max ordered by (score desc, index asc)
-    unsigned taken = 0;
+    // top-nc: nc rounds of a warp arg-max ordered by (score desc, index asc).
     float my_p = 0.f, psum = 0.f;
     my_id = 0;
-    for (int j = 0; j < a.nc; ++j) {
-        float bv = 0.f;
-        int be = INT_MAX;
+    if (EPL <= 8) {
+        // Each lane sorts its candidates once (a sorting network on (key desc,
+        // expert asc)); a round is then the warp maximum of the lanes' first
+        // keys, the warp minimum of the expert index among the lanes holding
+        // it, and a shift of the winning lane's list.
+        int ex[EPL];
+        float pv[EPL];
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && (be == INT_MAX || sc[i] > bv)) {
-                bv = sc[i];
-                be = e;
+            ex[i] = lane + 32 * i < E ? lane + 32 * i : 0x7FFFFFFF;
+            pv[i] = pr[i];
+        }
+        sort_desc<EPL>(key, ex, pv);
+        for (int j = 0; j < a.nc; ++j) {
+            const bool has = ex[0] != 0x7FFFFFFF;
+            const unsigned top = __reduce_max_sync(0xffffffffu, has ? key[0] : 0u);
+            const int win = (int)__reduce_min_sync(
+                0xffffffffu, (has && key[0] == top) ? (unsigned)ex[0] : 0x7FFFFFFFu);
+            const int owner = win & 31;
+            const float pj = __shfl_sync(0xffffffffu, pv[0], owner);
+            if (lane == owner) {
+#pragma unroll
+                for (int i = 0; i + 1 < EPL; ++i) {
+                    key[i] = key[i + 1];
+                    ex[i] = ex[i + 1];
+                    pv[i] = pv[i + 1];
+                }
+                ex[EPL - 1] = 0x7FFFFFFF;
+            }
+            if (j < a.k) psum += pj;
+            if (lane == j) {
+                my_id = win;
+                my_p = pj;
             }
         }
+    } else {
+        // a lane-local scan per round over the candidates not yet taken
+        unsigned taken = 0;
+        for (int j = 0; j < a.nc; ++j) {
+            unsigned bk = 0;
+            int be = -1;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                bv = ov;
-                be = oe;
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((taken >> i) & 1u) && (be < 0 || key[i] > bk)) {
+                    bk = key[i];
+                    be = e;
+                }
             }
-        }
-        be = __shfl_sync(0xffffffffu, be, 0);
-        const int owner = be & 31, slot_i = be >> 5;
-        float mine = 0.f;
+            const unsigned top = __reduce_max_sync(0xffffffffu, be >= 0 ? bk : 0u);
+            const int win = (int)__reduce_min_sync(
+                0xffffffffu, (be >= 0 && bk == top) ? (unsigned)be : 0x7FFFFFFFu);
+            const int owner = win & 31, slot_i = win >> 5;
+            float mine = 0.f;
 #pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (i == slot_i) mine = pr[i];
-        if (lane == owner) taken |= 1u << slot_i;
-        const float pj = __shfl_sync(0xffffffffu, mine, owner);
-        if (j < a.k) psum += pj;
-        if (lane == j) {
-            my_id = be;
-            my_p = pj;
+            for (int i = 0; i < EPL; ++i)
+                if (i == slot_i) mine = pr[i];
+            if (lane == owner) taken |= 1u << slot_i;
+            const float pj = __shfl_sync(0xffffffffu, mine, owner);
+            if (j < a.k) psum += pj;
+            if (lane == j) {
+                my_id = win;
+                my_p = pj;
+            }
         }
     }
     my_w = a.renorm ? my_p / psum : my_p;
@@ -339,8 +441,8 @@ __device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const To
 constexpr int kSelWarps = 8;
 
 // Standalone selection.
-template <int EPL>
-__global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(SelectArgs a) {
+template <int EPL, bool PARTS>
+__global__ void __launch_bounds__(32 * kSelWarps, EPL <= 8 ? 4 : 1) router_select_kernel(SelectArgs a) {
     const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
     TokenRegs<EPL> r;
     if (a.draw && t < a.T) draw_token_eps<EPL>(a, t, r);
@@ -349,7 +451,7 @@ __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(SelectArg
     pdl_wait();
     pdl_trigger();
     if (t >= a.T) return;
-    load_token<EPL>(a, t, r);
+    load_token<EPL, PARTS>(a, t, r);
     float pr[EPL];
     int id;
     float w;
@@ -358,7 +460,7 @@ __global__ void __launch_bounds__(32 * kSelWarps) router_select_kernel(SelectArg
 
 static int sel_blocks(int T) { return (T + kSelWarps - 1) / kSelWarps; }
 
-cudaError_t launch_router_select(const Shape& s, const float* logits, const float* zn,
+cudaError_t launch_router_select(const Shape& s, const RouterLogits& rl, float* logits_out,
                                  const float* noise, const float* bias, float* probs,
                                  float* sel, int32_t* ids, float* w, int from_scores,
                                  const float* sel_in, const float* probs_in, int* status,
@@ -366,13 +468,16 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
     SelectArgs a;
     a.T = s.T; a.E = s.E; a.k = s.k; a.nc = s.nc; a.renorm = s.renorm;
     a.from_scores = from_scores;
-    a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
-    a.draw = zn && !noise && s.noise_draw; a.seed = s.noise_seed; a.ctr = s.noise_counter;
+    a.rl = rl; a.logits_out = logits_out; a.noise = noise; a.bias = bias;
+    a.draw = rl.zn && !noise && s.noise_draw; a.seed = s.noise_seed; a.ctr = s.noise_counter;
     a.sel_in = sel_in; a.probs_in = probs_in;
     a.probs = probs; a.sel = sel; a.ids = ids; a.w = w; a.status = status;
 #define MOE_SEL(EPL)                                                                       \
-    return launch_k(router_select_kernel<EPL>, dim3(sel_blocks(s.T)),                \
-                    dim3(32 * kSelWarps), 0, st, a)
+    return a.rl.nsplit > 1 && !from_scores                                                 \
+               ? launch_k(router_select_kernel<EPL, true>, dim3(sel_blocks(s.T)),          \
+                          dim3(32 * kSelWarps), 0, st, a)                                   \
+               : launch_k(router_select_kernel<EPL, false>, dim3(sel_blocks(s.T)),         \
+                          dim3(32 * kSelWarps), 0, st, a)
     if (s.E <= 32) MOE_SEL(1);
     if (s.E <= 64) MOE_SEL(2);
     if (s.E <= 128) MOE_SEL(4);
@@ -383,14 +488,16 @@ cudaError_t launch_router_select(const Shape& s, const float* logits, const floa
 }
 
 // Layer path: selection fused with the capacity histogram and the
-// load-balance statistics, one token per warp. Per expert each lane keeps a
-// fixed-point sum of its probabilities, and each chosen (token, expert) adds 1
-// to blk_hist[e][token / kCapBlockTokens] (the scan kernel zeroes those
-// counters after reading them) and its gate to the block's importance sum.
+// load-balance statistics, one token per warp. Each warp leaves its token's
+// probabilities in shared memory and thread e of the block adds expert e's
+// column (fp32, in warp order) and turns the sum into 32.32 fixed point for
+// the order-free global total; each chosen (token, expert) adds 1 to
+// blk_hist[e][token / kCapBlockTokens] (the scan kernel zeroes those counters
+// after reading them) and its gate to the block's importance sum.
 // For E <= 128, 32 registers a thread (eight blocks an SM) keep every warp of a
 // T = 8192 grid resident at once.
-template <int EPL>
-__global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : 1) router_select_fused_kernel(
+template <int EPL, bool PARTS>
+__global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : EPL == 8 ? 4 : 1) router_select_fused_kernel(
     SelectArgs a, int32_t* blk_hist, int nblk_cap, AuxAcc acc, AuxOut out, int defer_final) {
     const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
     TokenRegs<EPL> r;
@@ -402,14 +509,15 @@ __global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : 1) router_selec
     unsigned long long* sP = sm64;
     unsigned long long* sI = sm64 + E;
     unsigned int* sC = reinterpret_cast<unsigned int*>(sm64 + 2 * E);
-    const int lane = threadIdx.x & 31;
-    if (t < a.T) load_token<EPL>(a, t, r);
+    float* sProb = reinterpret_cast<float*>(sC + E);  // [kSelWarps][E]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (t < a.T) load_token<EPL, PARTS>(a, t, r);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        sP[e] = 0;
         sI[e] = 0;
         sC[e] = 0;
     }
     __syncthreads();
+    float* mine = sProb + warp * E;
     if (t < a.T) {
         float pr[EPL];
         int id;
@@ -418,14 +526,24 @@ __global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : 1) router_selec
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
-            const unsigned long long v = to_fix(pr[i]);
-            if (e < E && v) atomicAdd(&sP[e], v);
+            if (e < E) mine[e] = pr[i];
         }
         if (lane < a.k) {
             atomicAdd(&sI[id], to_fix(w));
             atomicAdd(&sC[id], 1u);
             if (blk_hist) atomicAdd(&blk_hist[(size_t)id * nblk_cap + t / kCapBlockTokens], 1);
         }
+    } else {
+        for (int e = lane; e < E; e += 32) mine[e] = 0.f;
+    }
+    __syncthreads();
+    // the block's probability sum of expert e: fp32 in warp order (fixed),
+    // then one fixed-point conversion, so the total over blocks is exact
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < kSelWarps; ++q) v += sProb[q * E + e];
+        sP[e] = to_fix(v);
     }
     __syncthreads();
     if (defer_final)  // a later kernel finalises the statistics
@@ -434,26 +552,38 @@ __global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : 1) router_selec
         aux_publish_and_finalize(a.T, E, a.k, acc, out, sP, sI, sC);
 }
 
-cudaError_t launch_router_select_fused(const Shape& s, const float* logits, const float* zn,
+cudaError_t launch_router_select_fused(const Shape& s, const RouterLogits& rl,
                                        const float* noise, const float* bias, float* probs,
                                        int32_t* ids, float* w, int* status, int32_t* blk_hist,
                                        void* acc_mem, float* f, float* P, float* I, float* out3,
                                        bool defer_final, cudaStream_t st) {
     SelectArgs a;
     a.T = s.T; a.E = s.E; a.k = s.k; a.nc = s.nc; a.renorm = s.renorm; a.from_scores = 0;
-    a.logits = logits; a.zn = zn; a.noise = noise; a.bias = bias;
-    a.draw = zn && !noise && s.noise_draw; a.seed = s.noise_seed; a.ctr = s.noise_counter;
+    a.rl = rl; a.logits_out = nullptr; a.noise = noise; a.bias = bias;
+    a.draw = rl.zn && !noise && s.noise_draw; a.seed = s.noise_seed; a.ctr = s.noise_counter;
     a.sel_in = nullptr; a.probs_in = nullptr;
     a.probs = probs; a.sel = nullptr; a.ids = ids; a.w = w; a.status = status;
     const int nblk_cap = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
     const AuxAcc acc = aux_acc_at(acc_mem, s.E, kAuxGroups);
     const AuxOut out{f, P, I, out3, s.w_imp};
-    // blocks spread their statistics over kAuxGroups copies
-    const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int)) + 8;
+    // sP, sI (u64), sC (u32) and the warps' probabilities (f32) per expert
+    const size_t smem = (size_t)s.E * (2 * sizeof(unsigned long long) + sizeof(unsigned int) +
+                                       kSelWarps * sizeof(float)) + 8;
+    if (smem > 48 * 1024) {
+        for (auto fn : {router_select_fused_kernel<32, false>, router_select_fused_kernel<32, true>}) {
+            cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+            if (err != cudaSuccess) return err;
+        }
+    }
 #define MOE_SEL_FUSED(EPL)                                                                 \
-    return launch_k(router_select_fused_kernel<EPL>, dim3(sel_blocks(s.T)),            \
-                    dim3(32 * kSelWarps), smem, st, a, blk_hist, nblk_cap, acc, out,        \
-                    defer_final ? 1 : 0)
+    return a.rl.nsplit > 1                                                                 \
+               ? launch_k(router_select_fused_kernel<EPL, true>, dim3(sel_blocks(s.T)),    \
+                          dim3(32 * kSelWarps), smem, st, a, blk_hist, nblk_cap, acc, out,  \
+                          defer_final ? 1 : 0)                                              \
+               : launch_k(router_select_fused_kernel<EPL, false>, dim3(sel_blocks(s.T)),   \
+                          dim3(32 * kSelWarps), smem, st, a, blk_hist, nblk_cap, acc, out,  \
+                          defer_final ? 1 : 0)
     if (s.E <= 32) MOE_SEL_FUSED(1);
     if (s.E <= 64) MOE_SEL_FUSED(2);
     if (s.E <= 128) MOE_SEL_FUSED(4);

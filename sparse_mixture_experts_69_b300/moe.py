@@ -104,7 +104,7 @@ _SIGS = {
     "moe_bias_update": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, _P]),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_P] * 16 + [_P, ctypes.c_size_t, _P]),
     "moe_read_device_error": (ctypes.c_int, [_CFG, _P, ctypes.c_size_t, _P]),
-    "moe_set_wait_limits": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_int32]),
+    "moe_set_wait_limits": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32]),
     "moe_aux_stats_noalloc": (ctypes.c_int, [_CFG] + [_P] * 7 + [_P]),
     "moe_expert_choice_dispatch": (ctypes.c_int, [_CFG] + [_P] * 7 + [_P, ctypes.c_size_t, _P]),
     "moe_expert_choice_combine": (ctypes.c_int, [_CFG] + [_P] * 5 + [_P, ctypes.c_size_t, _P]),
@@ -266,6 +266,9 @@ def moe_read_device_error(cfg: Config, ws, stream=None) -> int:
     return lib().moe_read_device_error(ctypes.byref(cfg.c()), _p(ws), ws.numel(), _s(stream))
 
 
-def moe_set_wait_limits(wait_ns: int = 0, policy_passes: int = 0):
-    """Limits of the bounded device waits (0 restores each default); host only."""
-    _check(lib().moe_set_wait_limits(int(wait_ns), int(policy_passes)), "moe_set_wait_limits")
+def moe_set_wait_limits(wait_ns: int = 0, policy_passes: int = 0,
+                        hold_first_accumulator: int = 0):
+    """Limits of the bounded device waits (0 restores each default) and the
+    switch that makes the GEMMs' first accumulator wait run out; host only."""
+    _check(lib().moe_set_wait_limits(int(wait_ns), int(policy_passes),
+                                     int(hold_first_accumulator)), "moe_set_wait_limits")

@@ -47,9 +47,19 @@ def assert_maxabs(gpu, ref, rel, what):
     return err / scale if scale else 0.0
 
 
-def check_topk_valid(ids_gpu, s_ref, k, tol_rel=1e-5):
+def score_tolerance(s_ref, p_ref=None, biased=False):
+    """Per-token tolerance of the selection scores that the router tolerance
+    allows: scores H (no selection bias) within 1e-5 of max |H|; scores p +
+    bias within the probabilities' rule, TOL_LOGITS * max p of the token."""
+    if biased:
+        return TOL_LOGITS * np.abs(np.asarray(p_ref)).max(axis=1)
+    return 1e-5 * np.maximum(np.abs(np.asarray(s_ref)).max(axis=1), 1e-30)
+
+
+def check_topk_valid(ids_gpu, s_ref, k, tol_rel=1e-5, tol=None):
     """GPU ids against reference scores: equal except where the scores tie
-    within tol_rel; returns the indices of tokens whose ids differ."""
+    within the tolerance (tol: per-token absolute values; default tol_rel *
+    max |s| of the token); returns the indices of tokens whose ids differ."""
     ids_gpu = np.asarray(ids_gpu)
     T = ids_gpu.shape[0]
     diff = []
@@ -58,16 +68,16 @@ def check_topk_valid(ids_gpu, s_ref, k, tol_rel=1e-5):
         order = sorted(range(len(s)), key=lambda e: (-s[e], e))[:k]
         if list(ids_gpu[t]) == order:
             continue
-        tol = tol_rel * max(np.abs(s).max(), 1e-30)
+        tol_t = tol_rel * max(np.abs(s).max(), 1e-30) if tol is None else float(tol[t])
         chosen = list(ids_gpu[t])
         assert len(set(chosen)) == k, f"token {t}: repeated ids {chosen}"
         # the GPU order must be non-increasing in the reference scores up to tol,
         # and nothing left out may beat the last chosen score by more than tol
         for a, b in zip(chosen, chosen[1:]):
-            assert s[a] >= s[b] - tol, f"token {t}: order {chosen} vs scores"
+            assert s[a] >= s[b] - tol_t, f"token {t}: order {chosen} vs scores"
         rest = [e for e in range(len(s)) if e not in chosen]
         if rest:
-            assert max(s[e] for e in rest) <= min(s[e] for e in chosen) + tol, \
+            assert max(s[e] for e in rest) <= min(s[e] for e in chosen) + tol_t, \
                 f"token {t}: ids {chosen} are not a top-{k} (ref {order})"
         diff.append(t)
     return diff

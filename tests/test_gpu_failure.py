@@ -4,10 +4,12 @@ kernel reports MOE_ERR_TIMEOUT through the workspace status word and
 returns, and the same CUDA context then runs the path again, within the
 default limits, with results that match the oracle.
 
-- The tensor-core GEMM kernels bound every pipeline wait in time. With a
-  1 ns limit the epilogue's wait for its first accumulator cannot be met, so
-  at least one CTA aborts; aborting CTAs let their own copies and matrix
-  operations finish before they free tensor memory and exit.
+- The tensor-core GEMM kernels bound every pipeline wait in time. With the
+  hold switch on, each CTA's first "accumulator ready" signal is withheld
+  (a signal nothing else gives), so the epilogue's wait for it runs out
+  after the limit (1 ms here) in every CTA; aborting CTAs let their own
+  copies and matrix operations finish before they free tensor memory and
+  exit.
 - The capacity kernel with re-routing bounds its fixed-point loop in
   passes. One pass cannot settle when an expert overflows (the first pass
   starts from "no expert is full"); its slots then stay in range."""
@@ -66,12 +68,12 @@ def test_gemm_wait_limit_runs_out_and_the_context_stays_usable(cuda_device):
         moe.moe_expert_ffn(c, o["xp"], o["offsets"], inp["W1"], inp["W2"], inp["x"], inp["W1s"],
                            inp["W2s"], yp, ys, ws)
 
-    moe.moe_set_wait_limits(1, 0)
+    moe.moe_set_wait_limits(1_000_000, 0, 1)
     try:
         ffn()
         st = moe.moe_read_device_error(c, ws)
     finally:
-        moe.moe_set_wait_limits(0, 0)
+        moe.moe_set_wait_limits(0, 0, 0)
     assert st == MOE_ERR_TIMEOUT, moe.moe_status_string(st)
     # the status word was cleared by the read; the same context runs the FFN again
     ffn()
@@ -99,12 +101,12 @@ def test_policy_pass_limit_runs_out_and_the_context_stays_usable(cuda_device):
     o = _routed(wl, inp, dev, ws)
     assert moe.moe_read_device_error(c, ws) == 0
     C, R = moe.moe_capacity(c)
-    moe.moe_set_wait_limits(0, 1)
+    moe.moe_set_wait_limits(0, 1, 0)
     try:
         _dispatch(c, inp, o, ws)
         st = moe.moe_read_device_error(c, ws)
     finally:
-        moe.moe_set_wait_limits(0, 0)
+        moe.moe_set_wait_limits(0, 0, 0)
     assert st == MOE_ERR_TIMEOUT, moe.moe_status_string(st)
     slot = o["slot"].cpu().numpy()
     assert slot.min() >= -1 and slot.max() < R  # the unsettled slots stay in range
