@@ -380,21 +380,23 @@ def launches_per_step(wl):
     """Kernels of this library one step launches. Layer path: [Wg transpose
     (bf16)], router GEMM, fused selection + histogram + statistics, capacity
     scan + slots (one launch up to 256 token blocks), permute, up GEMM, down
-    GEMM, [combine: skipped for bf16 top-1 without shared experts, where the
-    down GEMM writes y], [bias update]. Overflow policies: one capacity kernel
-    instead of scan + slots; expert choice: select + gather instead of
-    capacity + permute, its own combine."""
+    GEMM, [combine: skipped where the down GEMM writes y itself, by its
+    folded combine (bf16, packed rows, combine_mode = 1) or, for top-1
+    without shared experts, by scattering gate * output], [bias update]. Overflow policies:
+    one capacity kernel instead of scan + slots; expert choice: select +
+    gather instead of capacity + permute, its own combine."""
     c = wl.cfg
     T, k, nc = c.T, c.top_k, c.n_cand
     ec = c.routing == 1
-    scatter = (c.dtype == 1 and c.top_k == 1 and nc == 1 and not c.pad_to_capacity
-               and c.n_shared == 0)
+    scatter = c.top_k == 1 and nc == 1 and c.n_shared == 0
+    combine_in_gemm = c.dtype == 1 and not c.pad_to_capacity and (
+        scatter or c.combine_mode == 1)
     policy = nc > k or c.priority != 0
     route_launches = (1 if c.dtype == 1 else 0) + 2
     if ec:
         return route_launches + 2 + 2 + 1
     cap_launches = 1 if policy else (1 if (T + 255) // 256 <= 256 else 2)
-    return (route_launches + cap_launches + 1 + 2 + (0 if scatter else 1)
+    return (route_launches + cap_launches + 1 + 2 + (0 if combine_in_gemm else 1)
             + (1 if wl.bias_rate else 0))
 
 

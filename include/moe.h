@@ -82,6 +82,12 @@ typedef enum { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_routing;
  * token (each token's candidates in rank order), or rank by rank (every
  * token's first choice before any second choice). */
 typedef enum { MOE_PRIORITY_TOKEN = 0, MOE_PRIORITY_RANK = 1 } moe_priority;
+/* MOE_COMBINE_IN_GEMM: the down GEMM's epilogue adds each token's rows once
+ * the last of them is stored (no combine launch; each row is still read back
+ * once, to keep the fixed order of the sum). MOE_COMBINE_KERNEL: the separate
+ * combine kernel after the down GEMM. MOE_COMBINE_AUTO: the separate kernel,
+ * which measured as fast or faster on every workload of this library. */
+typedef enum { MOE_COMBINE_AUTO = 0, MOE_COMBINE_IN_GEMM = 1, MOE_COMBINE_KERNEL = 2 } moe_combine_mode;
 
 /* Problem statement of one MoE layer call. */
 typedef struct {
@@ -114,6 +120,11 @@ typedef struct {
     int32_t noise_draw;
     uint64_t noise_seed;     /* generator key (noise_draw = 1)                 */
     uint64_t noise_counter;  /* stream number, e.g. the training step          */
+    /* Where moe_layer_fwd combines the expert outputs (bf16 layers with packed
+     * rows; fp32 and padded layers always use the separate combine kernel,
+     * top-1 layers without shared experts always scatter gate * output from
+     * the down GEMM). The result is the same bit for bit either way.        */
+    int32_t combine_mode;    /* moe_combine_mode                               */
 } moe_config;
 
 /* Terms used below: n_cand = top_k + reroute candidates per token. R_max =

@@ -313,7 +313,9 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec, in
                                                       const uint4* __restrict__ x,
                                                       const int32_t* __restrict__ slot,
                                                       uint4* __restrict__ xp,
-                                                      uint4* __restrict__ y_zero, int* status) {
+                                                      uint4* __restrict__ y_zero,
+                                                      int32_t* __restrict__ tok_need,
+                                                      int* status) {
     // the expert GEMM that follows reads the offsets before its own wait, so
     // dependents launch only after this kernel's wait (the capacity kernel
     // that wrote them is then complete)
@@ -328,6 +330,7 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec, in
         my_slot = -1;
     }
     unsigned live = __ballot_sync(0xffffffffu, my_slot >= 0);
+    if (tok_need && lane == 0) tok_need[t] = __popc(live);
     if (y_zero && !live) {  // dropped everywhere: its output row is zero
         for (int v = lane; v < nvec; v += 32) y_zero[(size_t)t * nvec + v] = make_uint4(0, 0, 0, 0);
         return;
@@ -357,10 +360,11 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec, in
 }
 
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
-                           void* y_zero, int* status, cudaStream_t st) {
+                           void* y_zero, int32_t* tok_need, int* status, cudaStream_t st) {
     const int nvec = s.d * s.esize / 16;
     return launch_k(permute_kernel, dim3((s.T + 7) / 8), dim3(256), 0, st, s.T, s.nc, nvec,
-                    s.R_max, (const uint4*)x, slot, (uint4*)xp, (uint4*)y_zero, status);
+                    s.R_max, (const uint4*)x, slot, (uint4*)xp, (uint4*)y_zero, tok_need,
+                    status);
 }
 
 }  // namespace moe

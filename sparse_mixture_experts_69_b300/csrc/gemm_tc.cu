@@ -338,6 +338,134 @@ __device__ __forceinline__ void store_rows32_bf16(__nv_bfloat16* out, int N, int
     __syncwarp();
 }
 
+// --------------------------------------------------------- folded combine
+static_assert(MOE_TC_BN_ACT == kDownTileN, "the folded combine counts 256-column tiles");
+
+// Combine folded into the down projection (GroupedGemm::fold_cnt), run by an
+// epilogue warp once its rows of the tile are stored. Every valid row counts
+// itself for its token and this column tile. For each token whose count the
+// warp completed, the warp then adds up the token's rows over the tile's 256
+// columns (lane = 8 consecutive columns) exactly as the combine kernel does:
+// acc = fmaf(gate_j, row_j, acc) over the kept choices j = 0, 1, ..., then
+// acc += shared row s for s = 0, 1, ..., all on the bf16 values as stored,
+// and the sum rounded to bf16 into y. The result does not depend on which
+// row arrived last.
+__device__ __noinline__ void fold_tile(const GroupedGemm& p, const GroupTile& gt, bool routed,
+                                       int trow, bool rv) {
+    const int lane = threadIdx.x & 31;
+    const int nt = (p.N + kDownTileN - 1) / kDownTileN;
+    bool bad = false, nonfinite = false;
+    int t = -1;
+    if (rv) {
+        t = routed ? __ldcg(p.fold_rows + gt.out_row + trow) : gt.m0 + trow;
+        if (t < 0 || t >= p.T) {
+            bad = true;
+            t = -1;
+        }
+    }
+    __threadfence();  // this lane's stores of the tile's rows ...
+    __syncwarp();     // ... come before any row of the warp is counted
+    bool last = false;
+    if (t >= 0) {
+        int* cnt = p.fold_cnt + (size_t)t * nt + gt.n_tile;
+        const int need = __ldcg(p.fold_need + t) + p.S;
+        last = atomicAdd(cnt, 1) == need - 1;
+        if (last) *cnt = 0;  // every row of (t, tile) is in: ready for the next call
+    }
+    unsigned todo = __ballot_sync(0xffffffffu, last);
+    if (todo) __threadfence();  // the other rows' stores are visible to the loads below
+    const __nv_bfloat16* yp = reinterpret_cast<const __nv_bfloat16*>(p.out0);
+    const __nv_bfloat16* ys = reinterpret_cast<const __nv_bfloat16*>(p.out1);
+    __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(p.fold_y);
+    const int n0 = gt.n_tile * kDownTileN + 8 * lane;
+    const bool cv = n0 < p.N;  // N is a multiple of 8
+    // lane j holds choice j's row and gate of token tt (-1: dropped or none)
+    auto load_choices = [&](int tt, int& r, float& g) {
+        r = -1;
+        g = 0.f;
+        if (tt >= 0 && lane < p.fold_nc) {
+            r = __ldcg(p.fold_slot + (size_t)tt * p.fold_nc + lane);
+            g = __ldcg(p.fold_w + (size_t)tt * p.fold_nc + lane);
+            if (r >= p.max_rows0) {
+                bad = true;
+                r = -1;
+            }
+        }
+    };
+    int tt = todo ? __shfl_sync(0xffffffffu, t, __ffs(todo) - 1) : -1;
+    int my_r, nx_r;
+    float my_g, nx_g;
+    load_choices(tt, my_r, my_g);
+    while (todo) {
+        todo &= todo - 1;
+        // the next token's choices load while this one's rows are summed
+        const int nx = todo ? __shfl_sync(0xffffffffu, t, __ffs(todo) - 1) : -1;
+        load_choices(nx, nx_r, nx_g);
+        // the token's rows in the combine's order: kept choices, then shared
+        // experts; loaded kChunk at a time, added in order
+        constexpr int kChunk = 12;
+        unsigned live = __ballot_sync(0xffffffffu, my_r >= 0);
+        const int nlive = __popc(live);
+        const int nrow = nlive + p.S;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        unsigned rem = live;  // kept choices not yet loaded, in order
+        for (int c0 = 0; c0 < nrow; c0 += kChunk) {
+            uint4 raw[kChunk];
+            float g[kChunk];
+#pragma unroll
+            for (int q = 0; q < kChunk; ++q) {
+                const int i = c0 + q;
+                g[q] = 0.f;
+                if (i < nlive) {  // warp-uniform
+                    const int j = __ffs(rem) - 1;  // the i-th kept choice
+                    rem &= rem - 1;
+                    const int r = __shfl_sync(0xffffffffu, my_r, j);
+                    g[q] = __shfl_sync(0xffffffffu, my_g, j);
+                    if (cv) raw[q] = __ldcg(reinterpret_cast<const uint4*>(yp + (size_t)r * p.N + n0));
+                } else if (i < nrow && cv) {
+                    raw[q] = __ldcg(reinterpret_cast<const uint4*>(
+                        ys + ((size_t)(i - nlive) * p.T + tt) * p.N + n0));
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kChunk; ++q) {
+                const int i = c0 + q;
+                if (i < nrow && cv) {
+                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[q]);
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2) {
+                        const float2 v = __bfloat1622float2(h[k2]);
+                        if (i < nlive) {
+                            acc[2 * k2] = fmaf(g[q], v.x, acc[2 * k2]);
+                            acc[2 * k2 + 1] = fmaf(g[q], v.y, acc[2 * k2 + 1]);
+                        } else {
+                            acc[2 * k2] += v.x;
+                            acc[2 * k2 + 1] += v.y;
+                        }
+                    }
+                }
+            }
+        }
+        if (cv) {
+            uint4 out;
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                nonfinite |= !isfinite(acc[2 * i]) || !isfinite(acc[2 * i + 1]);
+                h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+            }
+            *reinterpret_cast<uint4*>(y + (size_t)tt * p.N + n0) = out;
+        }
+        tt = nx;
+        my_r = nx_r;
+        my_g = nx_g;
+    }
+    if (bad) flag_status(p.status, DEV_BAD_ARG);
+    if (__any_sync(0xffffffffu, nonfinite) && lane == 0) flag_status(p.status, DEV_NONFINITE);
+}
+
 // ------------------------------------------------------------------ kernel
 // First B row of each B box of tile gt: SwiGLU tiles take 128 gate rows and
 // the matching 128 up rows; other tiles take BN consecutive rows.
@@ -676,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             store_rows32_bf16(out, p.N, n0, dst_row, v, stg, keep_l2, pol_o);
                         }
                     }
+                    if (EPI == EPI_ACT && p.fold_cnt) fold_tile(p, gt, routed, trow, rv);
                 }
             }
             tc_fence_before();

@@ -59,6 +59,7 @@ WsLayout ws_layout(const Shape& s) {
     L.blk_hist = take(nblk * E * 4);
     L.cap_ticket = take(16);
     L.seq_ticket = take(16);
+    L.fold_cnt = take(s.dtype == MOE_BF16 ? T * ((d + kDownTileN - 1) / kDownTileN) * 4 : 0);
     L.zero_end = off;
     L.zn = take(T * E * 4);
     size_t part = 0;  // K parts of the router GEMM, for Nr = E or 2E (noisy)
@@ -84,6 +85,7 @@ WsLayout ws_layout(const Shape& s) {
     L.kept = take(E * 4);
     L.offsets = take((E + 1) * 4);
     L.row_token = take(R * 4);
+    L.tok_need = take(T * 4);
     L.blk_base = take(nblk * E * 4);
     L.xp = take(R * d * es);
     L.h = take((R + S * T) * F * es);
@@ -164,6 +166,9 @@ moe_status make_shape(const moe_config* c, Shape* s) {
     s->noise_draw = c->noise_draw;
     s->noise_seed = c->noise_seed;
     s->noise_counter = c->noise_counter;
+    if (c->combine_mode < MOE_COMBINE_AUTO || c->combine_mode > MOE_COMBINE_KERNEL)
+        return MOE_ERR_INVALID_ARG;
+    s->combine_mode = c->combine_mode;
     return MOE_OK;
 }
 
@@ -250,7 +255,7 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x
 moe_status dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const void* x,
                          const int32_t* ids, int32_t* counts, int32_t* kept, int32_t* offsets,
                          int32_t* slot, void* xp, int32_t* row_token, bool hist_ready,
-                         void* y_zero, cudaStream_t st) {
+                         void* y_zero, int32_t* tok_need, cudaStream_t st) {
     int* status = at<int>(ws, L.status);
     // padded blocks: rows no token takes must read zero, so clear the block
     // buffer first (the permute then fills the taken rows)
@@ -264,7 +269,7 @@ moe_status dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const void
                                  at<unsigned int>(ws, L.cap_ticket), at<int32_t>(ws, L.blk_base),
                                  counts, kept, offsets, slot, row_token, status, hist_ready, st));
     }
-    MOE_CUDA(launch_permute(s, x, slot, xp, y_zero, status, st));
+    MOE_CUDA(launch_permute(s, x, slot, xp, y_zero, tok_need, status, st));
     return MOE_OK;
 }
 
@@ -280,13 +285,24 @@ moe_status ec_dispatch_impl(const Shape& s, const WsLayout& L, void* ws, const v
 
 // scatter (top-1, no shared experts, bf16): the down GEMM writes y[token] =
 // gate * output directly through row_token instead of yp (no combine pass).
+// fold (bf16, otherwise): the down GEMM writes yp and ys and also sums each
+// token's rows into y once the last of them is stored (no combine launch).
 // fin_aux_vecs / fin_out3 (layer path, bf16): the up GEMM finalises the
 // statistics the selection kernel accumulated.
+// The combine of the layer path, done by the down projection (ffn_impl).
+struct Fold {
+    const int32_t* row_token;  // [R_max]
+    const int32_t* slot;       // [T,nc]
+    const float* w;            // [T,nc]
+    void* y;                   // [T,d]
+};
+
 moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
                     const int32_t* offsets, const void* W1, const void* W2, const void* x,
                     const void* W1s, const void* W2s, void* yp, void* ys,
                     const int32_t* scatter_rows, const float* scatter_gate, void* y,
-                    float* fin_aux_vecs, float* fin_out3, bool up_early, cudaStream_t st) {
+                    float* fin_aux_vecs, float* fin_out3, bool up_early, const Fold* fold,
+                    cudaStream_t st) {
     int* status = at<int>(ws, L.status);
     void* h = at<void>(ws, L.h);
     void* h_shared = static_cast<char*>(h) + (size_t)s.R_max * s.F * s.esize;
@@ -356,6 +372,15 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     dn.scatter_rows = scatter_rows;
     dn.scatter_scale = scatter_gate;
     dn.scatter_out = y;
+    if (fold) {
+        dn.fold_cnt = at<int32_t>(ws, L.fold_cnt);
+        dn.fold_need = at<int32_t>(ws, L.tok_need);
+        dn.fold_rows = fold->row_token;
+        dn.fold_slot = fold->slot;
+        dn.fold_w = fold->w;
+        dn.fold_nc = s.nc;
+        dn.fold_y = fold->y;
+    }
     dn.status = status;
     dn.b_evict_first = one_tile;
     // the up projection just launched signals only after its wait: when this
@@ -452,7 +477,7 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* x, const int3
     if (s.routing == MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_UNSUPPORTED;
     return dispatch_impl(s, L, ws, x, topk_ids, counts, kept, offsets, slot, xp, row_token,
-                         false, nullptr, (cudaStream_t)stream);
+                         false, nullptr, nullptr, (cudaStream_t)stream);
 }
 
 MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* offsets,
@@ -471,7 +496,7 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const i
     // the preceding kernel is the caller's: the up projection waits for it
     // before it reads the offsets
     return ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, nullptr, nullptr, nullptr,
-                    nullptr, nullptr, false, (cudaStream_t)stream);
+                    nullptr, nullptr, false, nullptr, (cudaStream_t)stream);
 }
 
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* slot,
@@ -556,7 +581,7 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
         // the gather signals its dependents after its wait: the offsets the
         // selection wrote are final when the up projection launches
         MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys, nullptr, nullptr,
-                         nullptr, nullptr, nullptr, true, st));
+                         nullptr, nullptr, nullptr, true, nullptr, st));
         MOE_CUDA(launch_expert_choice_combine(s, yp, tok_row, probs, s.S ? ys : nullptr, y, st));
         return MOE_OK;
     }
@@ -569,15 +594,25 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const void* x, const voi
     // Not with re-route candidates (a token's gate depends on which candidate
     // is kept) or padding (padding rows belong to no token).
     const bool scatter = s.k == 1 && s.nc == 1 && !s.pad && s.S == 0 && s.dtype == MOE_BF16;
+    // otherwise (bf16, packed rows) the down GEMM can also combine, on request:
+    // each token's rows are summed in the fixed combine order once the last
+    // one is stored. It re-reads every row it adds, like the combine kernel,
+    // and on the workloads measured it was no faster (the Mixtral-shaped layer
+    // within noise, the DeepSeek-shaped one slower), so the automatic choice
+    // is the separate kernel.
+    const bool fold = !scatter && !s.pad && s.dtype == MOE_BF16 &&
+                      s.combine_mode == MOE_COMBINE_IN_GEMM;
+    const Fold fold_args{row_token, slot, w, y};
     MOE_TRY(dispatch_impl(s, L, ws, x, ids, cnt, kept, offsets, slot, xp, row_token,
-                          !uses_policy(s), scatter ? y : nullptr, st));
+                          !uses_policy(s), (scatter || (fold && s.S == 0)) ? y : nullptr,
+                          fold ? at<int32_t>(ws, L.tok_need) : nullptr, st));
     // the permute signals its dependents after its wait: the offsets the
     // capacity kernel wrote are final when the up projection launches
     MOE_TRY(ffn_impl(s, L, ws, xp, offsets, W1, W2, x, W1s, W2s, yp, ys,
                      scatter ? row_token : nullptr, scatter ? w : nullptr,
                      scatter ? y : nullptr, s.dtype == MOE_BF16 ? av : nullptr,
-                     s.dtype == MOE_BF16 ? o3 : nullptr, true, st));
-    if (!scatter)
+                     s.dtype == MOE_BF16 ? o3 : nullptr, true, fold ? &fold_args : nullptr, st));
+    if (!scatter && !fold)
         MOE_CUDA(launch_combine(s, yp, slot, w, s.S ? ys : nullptr, y, at<int>(ws, L.status), st));
     return MOE_OK;
 }

@@ -44,6 +44,7 @@ struct Shape {
     int noise_draw;                    // 1: the router draws its noise (moe_draw_noise)
     unsigned long long noise_seed;     // generator key
     unsigned long long noise_counter;  // stream number
+    int combine_mode;                  // moe_combine_mode
 };
 
 // Workspace layout (byte offsets, each 256-aligned). One layout serves every
@@ -54,6 +55,7 @@ struct WsLayout {
     size_t aux_acc;    // statistics accumulators (aux_acc_bytes(E, kAuxGroups))
     size_t blk_hist;   // [E][nblk] i32 capacity histogram counters
     size_t cap_ticket; // u32 ticket of the fused scan + slot kernel
+    size_t fold_cnt;   // [T][down-GEMM column tiles] i32 arrivals of the folded combine
     size_t seq_ticket; // u32 ticket of the sequence-statistics kernel
     size_t zero_end;   // end of the zero-between-calls prefix
     size_t zn;         // [T,E] f32 noise logits x.Wnoise
@@ -71,6 +73,7 @@ struct WsLayout {
     size_t kept;       // [E] i32 (layer only)
     size_t offsets;    // [E+1] i32 (layer only)
     size_t row_token;  // [R_max] i32 (layer only)
+    size_t tok_need;   // [T] i32 kept choices per token (layer, folded combine)
     size_t blk_base;   // [E][nblk] i32
     size_t xp;         // [R_max,d] dtype (layer only)
     size_t h;          // [R_max + S T, F] dtype
@@ -144,8 +147,9 @@ cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_his
                             unsigned int* cap_ticket, int32_t* blk_base, int32_t* counts,
                             int32_t* kept, int32_t* offsets, int32_t* slot, int32_t* row_token,
                             int* status, bool hist_ready, cudaStream_t st);
-// y_zero (top-1 layers whose combine is done by the down GEMM): the output row
-// of a token whose only assignment was dropped is zeroed here.
+// y_zero (layers whose combine is done by the down GEMM and that have no
+// shared experts): the output row of a token whose every assignment was
+// dropped is zeroed here. tok_need (or NULL): each token's kept choices.
 // Capacity with re-routing and/or rank priority: one thread-block cluster
 // (see policy.cu). ids [T,nc]; slot [T,nc]; offsets e*C when s.pad.
 cudaError_t launch_capacity_policy(const Shape& s, const int32_t* ids, int32_t* counts,
@@ -168,7 +172,10 @@ cudaError_t launch_seq_aux(const Shape& s, const float* probs, const int32_t* id
                            float* aux_seq, float* aux_mean, void* scratch, unsigned int* ticket,
                            int* status, cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* slot, void* xp,
-                           void* y_zero, int* status, cudaStream_t st);
+                           void* y_zero, int32_t* tok_need, int* status, cudaStream_t st);
+// Column tile width of the down projection's output (d), which the folded
+// combine counts arrivals per.
+constexpr int kDownTileN = 256;
 
 // Grouped expert GEMMs. Up: h = act(A W1^T); down: out = h W2^T.
 struct GroupedGemm {
@@ -194,6 +201,19 @@ struct GroupedGemm {
     const int32_t* scatter_rows;
     const float* scatter_scale;
     void* scatter_out;
+    // combine folded into the down projection (tcgen05 only; fold_cnt != NULL):
+    // after a warp has stored its rows of a tile (routed rows to out0, shared
+    // rows to out1), each row counts itself in fold_cnt[token][column tile];
+    // the arrival that completes a token's fold_need[token] + S rows sums
+    // them, y[t] = sum_j fold_w[t,j] out0[fold_slot[t,j]] + sum_s out1[s T + t]
+    // in fp32 in that order, into fold_y, and clears the counter.
+    int32_t* fold_cnt;           // [T][ceil(N / column tile)], zero between calls
+    const int32_t* fold_need;    // [T] kept choices of each token
+    const int32_t* fold_rows;    // [rows of out0] token of each routed row
+    const int32_t* fold_slot;    // [T][fold_nc] row of each choice, -1 if dropped
+    const float* fold_w;         // [T][fold_nc] gates
+    int fold_nc;
+    void* fold_y;                // [T][N]
     // layer path (tcgen05 only): statistics accumulators the previous kernels
     // filled; CTA 0's epilogue warps finalise them while waiting for their first
     // accumulator (fin_acc_mem == NULL: nothing to do)

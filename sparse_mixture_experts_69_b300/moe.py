@@ -21,6 +21,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_RELU, MOE_GELU, MOE_SWIGLU = 0, 1, 2
 MOE_TOKEN_CHOICE, MOE_EXPERT_CHOICE = 0, 1
 MOE_PRIORITY_TOKEN, MOE_PRIORITY_RANK = 0, 1
+MOE_COMBINE_AUTO, MOE_COMBINE_IN_GEMM, MOE_COMBINE_KERNEL = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_NONFINITE", 6: "MOE_ERR_TIMEOUT",
           7: "MOE_ERR_DEVICE_ARG"}
@@ -41,7 +42,8 @@ class moe_config(ctypes.Structure):
                 ("importance_weight", ctypes.c_float), ("reroute", ctypes.c_int32),
                 ("priority", ctypes.c_int32), ("pad_to_capacity", ctypes.c_int32),
                 ("routing", ctypes.c_int32), ("noise_draw", ctypes.c_int32),
-                ("noise_seed", ctypes.c_uint64), ("noise_counter", ctypes.c_uint64)]
+                ("noise_seed", ctypes.c_uint64), ("noise_counter", ctypes.c_uint64),
+                ("combine_mode", ctypes.c_int32)]
 
 
 @dataclass
@@ -65,13 +67,15 @@ class Config:
     noise_draw: int = 0
     noise_seed: int = 0
     noise_counter: int = 0
+    combine_mode: int = 0
 
     def c(self) -> moe_config:
         return moe_config(self.T, self.d_model, self.n_experts, self.top_k, self.d_ff,
                           self.n_shared, self.capacity_factor, self.renorm_topk, self.dtype,
                           self.act, self.importance_weight, self.reroute, self.priority,
                           self.pad_to_capacity, self.routing, self.noise_draw,
-                          self.noise_seed & (2**64 - 1), self.noise_counter & (2**64 - 1))
+                          self.noise_seed & (2**64 - 1), self.noise_counter & (2**64 - 1),
+                          self.combine_mode)
 
     @property
     def n_cand(self) -> int:

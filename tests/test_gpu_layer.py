@@ -303,3 +303,24 @@ def test_layer_token_order_capacity(cuda_device, T, E, k, cf, d, pad):
                                     capacity_factor=cf, pad_to_capacity=pad)
     o, _ = layer_vs_oracle(wl, cuda_device)
     assert (o["slot"] < 0).any()
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("mixtral", dict(T=3000, d_model=512, d_ff=512)),
+    ("deepseek", dict(T=2000, d_model=512, d_ff=256, n_experts=64, capacity_factor=1.0)),
+    ("decode", dict(d_model=512, d_ff=256)),
+    ("switch_reroute", dict(T=4096, d_model=256, d_ff=256, top_k=2, n_shared=1)),
+])
+def test_folded_combine_equals_the_combine_kernel(cuda_device, name, kw):
+    """The combine folded into the down GEMM and the separate combine kernel
+    add the same bf16 rows with the same gates in the same order, so y is
+    equal bit for bit (shared experts, drops and re-routed candidates
+    included); both match the oracle fed the GPU's routing."""
+    from gpu_helpers import layer_vs_oracle
+    wl = WORKLOADS[name].with_(**kw)
+    inp = make_inputs(wl, cuda_device)
+    ys = []
+    for mode in (moe.MOE_COMBINE_IN_GEMM, moe.MOE_COMBINE_KERNEL):
+        o, _ = layer_vs_oracle(wl.with_(combine_mode=mode), cuda_device, inp)
+        ys.append(o["y"])
+    assert torch.equal(ys[0], ys[1])
