@@ -201,7 +201,7 @@ __device__ __forceinline__ void load_token(const SelectArgs& a, int t, TokenRegs
     const size_t row = (size_t)t * a.E;
     const bool noisy = a.rl.zn && (a.noise || a.draw);
     const RouterLogits& rl = a.rl;
-    if (PARTS) {
+    if constexpr (PARTS) {
         // the K parts of [z | zn], added in part order, then the offset
         const size_t plane = (size_t)a.T * rl.Nr;
 #pragma unroll
@@ -230,20 +230,20 @@ __device__ __forceinline__ void load_token(const SelectArgs& a, int t, TokenRegs
                 if (noisy && !a.draw) r.eps[i] = a.noise[row + e];
             }
         }
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        const bool in = e < a.E;
-        if (!a.draw) r.eps[i] = 0.f;  // drawn noise: already in r (draw_token_eps)
-        if (a.from_scores) {
-            r.z[i] = in ? a.sel_in[row + e] : 0.f;
-            r.zn[i] = in ? a.probs_in[row + e] : 0.f;
-        } else {
-            r.z[i] = in ? rl.logits[row + e] : 0.f;
-            r.zn[i] = in && noisy ? rl.zn[row + e] : 0.f;
-            if (in && noisy && !a.draw) r.eps[i] = a.noise[row + e];
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            const bool in = e < a.E;
+            if (!a.draw) r.eps[i] = 0.f;  // drawn noise: already in r (draw_token_eps)
+            if (a.from_scores) {
+                r.z[i] = in ? a.sel_in[row + e] : 0.f;
+                r.zn[i] = in ? a.probs_in[row + e] : 0.f;
+            } else {
+                r.z[i] = in ? rl.logits[row + e] : 0.f;
+                r.zn[i] = in && noisy ? rl.zn[row + e] : 0.f;
+                if (in && noisy && !a.draw) r.eps[i] = a.noise[row + e];
+            }
         }
     }
 }
