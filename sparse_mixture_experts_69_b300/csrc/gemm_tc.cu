@@ -499,12 +499,23 @@ __device__ __forceinline__ void load_b_stage(uint8_t* sB_stage, const CUtensorMa
         }
 }
 
+// Bytes a ring stage receives for a tile whose group has `rows` rows from the
+// tile's first row on: tiles of at most 64 rows (M=64 MMAs) load a 64-row A
+// box, half the A bytes; the rest of the A slot stays unused.
+template <int BN, int EPI>
+__device__ __forceinline__ uint32_t stage_bytes(int rows) {
+    const bool short_a = EPI != EPI_ROUTER && rows <= 64;
+    return (uint32_t)((short_a ? Cfg<BN>::A_BYTES / 2 : Cfg<BN>::A_BYTES) + Cfg<BN>::B_BYTES);
+}
+
 // WEF: weights evict-first in L2 (a separate instantiation: the hinted copy
 // form, even with the normal policy, slowed the launches with weight reuse).
 template <int BN, int EPI, bool WEF>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0,
                            const __grid_constant__ CUtensorMap tmA1,
+                           const __grid_constant__ CUtensorMap tmA0s,
+                           const __grid_constant__ CUtensorMap tmA1s,
                            const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
     using C = Cfg<BN>;
@@ -534,6 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA0);
         prefetch_tmap(&tmA1);
+        prefetch_tmap(&tmA0s);
+        prefetch_tmap(&tmA1s);
         prefetch_tmap(&tmB0);
         prefetch_tmap(&tmB1);
     }
@@ -584,8 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int brow[C::B_LOADS];
             b_tile_rows<BN, EPI>(p, gt, brow);
             const int kb_hi = (sp + 1) * nkb / ks;
+            const uint32_t bytes = stage_bytes<BN, EPI>(gt.rows);
             for (int kb = sp * nkb / ks; kb < kb_hi && prefilled < C::STAGES; ++kb) {
-                mbar_arrive_expect_tx(&full[prefilled], C::STAGE_BYTES);
+                mbar_arrive_expect_tx(&full[prefilled], bytes);
                 load_b_stage<BN, WEF>(sB + prefilled * C::B_BYTES, mb, &full[prefilled], kb, brow,
                                       pol_w);
                 ++prefilled;
@@ -617,8 +631,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tile = w / ks, sp = w - tile * ks;
                 const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
                 const bool routed = gt.g < p.E;
-                const CUtensorMap* ma = routed ? &tmA0 : &tmA1;
+                // tiles of at most 64 rows (M=64 MMAs) load 64-row A boxes
+                const bool short_a = EPI != EPI_ROUTER && gt.rows <= 64;
+                const CUtensorMap* ma = short_a ? (routed ? &tmA0s : &tmA1s)
+                                                : (routed ? &tmA0 : &tmA1);
                 const CUtensorMap* mb = routed ? &tmB0 : &tmB1;
+                const uint32_t bytes = stage_bytes<BN, EPI>(gt.rows);
                 int brow[C::B_LOADS];
                 b_tile_rows<BN, EPI>(p, gt, brow);
                 const int kb_hi = (sp + 1) * nkb / ks;
@@ -629,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // prefilled stages already expect their bytes and hold B
                     const bool fresh = item >= prefilled;
-                    if (fresh) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    if (fresh) mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
                     for (int hk = 0; hk < KH; ++hk)
                         tma_load_2d(sA + stage * C::A_BYTES + hk * C::A_HALF, ma, &full[stage],
@@ -860,11 +878,16 @@ template <int BN, int EPI, bool WEF>
 static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     using C = Cfg<BN>;
     const GroupedGemm& p = a.p;
-    CUtensorMap mA0, mA1, mB0, mB1;
+    CUtensorMap mA0, mA1, mA0s, mA1s, mB0, mB1;
     const int G = p.E + p.S;
-    if (!make_map(&mA0, p.A0 ? p.A0 : p.A1, p.A0 ? p.rows_a0 : p.rows_a1, p.K, BM) ||
-        !make_map(&mA1, p.A1 ? p.A1 : p.A0, p.A1 ? p.rows_a1 : p.rows_a0, p.K, BM))
-        return cudaErrorInvalidValue;
+    // A maps with 128-row boxes, and with 64-row boxes for tiles of <= 64 rows
+    for (int box : {BM, 64}) {
+        CUtensorMap* m0 = box == BM ? &mA0 : &mA0s;
+        CUtensorMap* m1 = box == BM ? &mA1 : &mA1s;
+        if (!make_map(m0, p.A0 ? p.A0 : p.A1, p.A0 ? p.rows_a0 : p.rows_a1, p.K, box) ||
+            !make_map(m1, p.A1 ? p.A1 : p.A0, p.A1 ? p.rows_a1 : p.rows_a0, p.K, box))
+            return cudaErrorInvalidValue;
+    }
     const int brows0 = p.E * p.b_rows_group, brows1 = p.S * p.b_rows_group;
     if (!make_map(&mB0, p.B0 ? p.B0 : p.B1, p.B0 ? brows0 : brows1, p.K, C::B_BOX_ROWS) ||
         !make_map(&mB1, p.B1 ? p.B1 : p.B0, p.B1 ? brows1 : brows0, p.K, C::B_BOX_ROWS))
@@ -881,7 +904,7 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     const long long bound = std::max<long long>(1, mt * nt * (EPI == EPI_ROUTER ? a.ksplit : 1));
     const int grid = (int)std::min<long long>(bound, num_sms());
     return launch_k(grouped_gemm_tc_kernel<BN, EPI, WEF>, dim3(grid), dim3(kThreads), smem, st, mA0,
-                    mA1, mB0, mB1, a);
+                    mA1, mA0s, mA1s, mB0, mB1, a);
 }
 
 }  // namespace tc
