@@ -207,6 +207,76 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
+// ---- CTA-pair (cluster of two) forms, used by grouped_gemm_pair_kernel
+// TMEM allocation shared by the CTA pair: one warp of each CTA executes it.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// D (both CTAs' TMEM, 128 rows each) (+)= A (128 rows in each CTA's shared
+// memory) * B^T (N/2 rows in each CTA's shared memory), issued by one thread
+// of the even CTA
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the mbarrier at this shared-memory offset in every CTA of mask
+// once the pair MMAs issued so far by this thread are done.
+__device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+// TMA 2-D tile load into this CTA's shared memory whose completion is
+// counted on the mbarrier at `bar_cluster` (shared::cluster address), which
+// may be in the other CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_to_pair_bar(void* dst, const CUtensorMap* map,
+                                                        uint32_t bar_cluster, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Shared-memory address of the same object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Arrive on a barrier of another CTA of the cluster. Default semantics
+// (release at CTA scope): no cluster-wide fence, which would cost about a
+// microsecond per call. The arrival passes on a hardware-completed event (the
+// tcgen05.ld of an accumulator finished), not data written by this thread.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
 // barrier among the 128 epilogue threads (warps 2..5) only
 struct EpilogueBar {
     __device__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -691,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
                 // expert tiles of at most 64 rows (few-token experts) run M=64 MMAs
                 const bool m64 =
-                    EPI != EPI_ROUTER && tile_rows(mt_start, grows, G, nt, BM, tile) <= 64;
+                    EPI != EPI_ROUTER && tile_rows(mt_start, grows, G, nt, BM, tile, p.row_block) <= 64;
                 const uint32_t idesc = m64 ? C::IDESC64 : C::IDESC;
                 const int kb_lo = sp * nkb / ks, kb_hi = (sp + 1) * nkb / ks;
                 for (int kb = kb_lo; kb < kb_hi; ++kb) {
@@ -907,6 +977,391 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
                     mA1, mA0s, mA1s, mB0, mB1, a);
 }
 
+// ------------------------------------------------------------ CTA-pair kernel
+// The expert GEMM on 256-row tiles computed by a cluster of two CTAs with the
+// pair MMA (tcgen05.mma.cta_group::2, M = 256, N = 256): each CTA holds its
+// own 128 A rows and one half of the 256-wide weight tile in shared memory
+// and receives its 128 rows x 256 columns of the accumulator in its own TMEM.
+// Per SM a K block is 16 KB of A plus 16 KB of B for 128 x 256 x 64 of MMA
+// work, a third fewer operand bytes than the single-CTA tile (16 + 32 KB), so
+// the same 192 KB holds 6 ring stages instead of 4; both TMEM buffers stay,
+// so the epilogue of one tile overlaps the next tile's MMAs.
+//
+// Signals. Both CTAs' TMA copies of a stage complete on the even CTA's
+// `full` barrier (the odd CTA's copies through the pair form of the TMA
+// load), which the even CTA's producer arms with both CTAs' bytes. The even
+// CTA's warp 1 issues the MMAs once a stage is in, and its commits arrive on
+// `empty` (stage free) and `tfull` (accumulator ready) in both CTAs at once
+// (multicast). Each CTA's epilogue warps release an accumulator on the even
+// CTA's `tempty` (remote arrive from the odd CTA). Every wait is bounded in
+// time as in the single-CTA kernel; neither CTA frees TMEM or leaves before a
+// cluster barrier that both reach once every MMA of the pair is done. An
+// aborting odd CTA cannot see its own copies complete (they count on the
+// other CTA's barrier), so it waits 200 us, far longer than a copy takes,
+// before that barrier.
+struct PairCfg {
+    static constexpr int BN = 256;
+    static constexpr int A_BYTES = BM * BKH * 2;    // own 128 rows x 64
+    static constexpr int B_BYTES = 128 * BKH * 2;   // own half of the weight tile
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES_FIT = MOE_TC_SMEM / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int TMEM_COLS = 2 * BN;        // two accumulators
+    // M=256 (128 rows in each CTA), N=256, D=f32, A=B=bf16, both K-major
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                                      ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+    static constexpr int STAGING_BYTES = 4 * 32 * 33 * 4;
+    static constexpr size_t smem_bytes(int G) {
+        return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + sizeof(int) * (size_t)(2 * G + 1) +
+               16 + STAGING_BYTES;
+    }
+};
+static_assert(KH == 1, "the pair kernel loads one 64-wide K block per stage");
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
+                             const __grid_constant__ CUtensorMap tmA1,
+                             const __grid_constant__ CUtensorMap tmB0,
+                             const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+    using C = PairCfg;
+    constexpr int BN = C::BN;
+    static_assert(EPI == EPI_GLU || EPI == EPI_ACT, "expert GEMMs only");
+    const GroupedGemm& p = args.p;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* tfull = empty + C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* mt_start = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+    int* grows = mt_start + p.E + p.S + 1;
+    float* staging = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(grows + p.E + p.S) + 15) & ~(uintptr_t)15);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = (int)cluster_id_x(), nclusters = (int)cluster_count_x();
+    const int G = p.E + p.S;
+    const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
+    const int nt = (p.N + ncol_tile - 1) / ncol_tile;
+    const int nkb = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA0);
+        prefetch_tmap(&tmA1);
+        prefetch_tmap(&tmB0);
+        prefetch_tmap(&tmB1);
+    }
+    const bool early = p.early != 0;
+    if (!early) pdl_wait();
+    if (early)
+        build_tile_table<true>(p, 2 * BM, mt_start, grows);
+    else
+        build_tile_table<false>(p, 2 * BM, mt_start, grows);
+    __syncthreads();
+    const int total = mt_start[G] * nt;
+    // no work for this pair: both CTAs leave together, before any allocation
+    // or cluster-wide step (pair 0 stays when it owes the statistics)
+    if (cluster >= total && !(p.fin_acc_mem && cluster == 0)) {
+        if (early) pdl_wait();
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 8);  // lane 0 of the 4 epilogue warps of each CTA
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    // both CTAs' barriers are initialised before any remote arrive or
+    // multicast commit can reach them
+    cluster_sync_all();
+    const uint64_t pol_w = 0ull;
+    int prefilled = 0;
+    if (early && threadIdx.x == 0) {
+        for (int w = cluster; w < total && prefilled < C::STAGES; w += nclusters) {
+            const GroupTile gt = decode_tile<true>(p, mt_start, nt, 2 * BM, w);
+            const CUtensorMap* mb = gt.g < p.E ? &tmB0 : &tmB1;
+            int brow[Cfg<BN>::B_LOADS];
+            b_tile_rows<BN, EPI>(p, gt, brow);
+            for (int kb = 0; kb < nkb && prefilled < C::STAGES; ++kb) {
+                if (leader) {
+                    mbar_arrive_expect_tx(&full[prefilled], 2 * C::STAGE_BYTES);
+                    tma_load_2d(sB + prefilled * C::B_BYTES, mb, &full[prefilled], kb * BK,
+                                brow[rank]);
+                } else {
+                    tma_load_2d_to_pair_bar(sB + prefilled * C::B_BYTES, mb,
+                                            mapa_shared(smem_u32(&full[prefilled]), 0), kb * BK,
+                                            brow[rank]);
+                }
+                ++prefilled;
+            }
+        }
+    }
+    (void)pol_w;
+    if (early) pdl_wait();
+    pdl_trigger();
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;
+            bool ok = true;
+            int item = 0;
+            for (int w = cluster; w < total && ok; w += nclusters) {
+                const GroupTile gt = decode_tile(p, mt_start, nt, 2 * BM, w);
+                const bool routed = gt.g < p.E;
+                const CUtensorMap* ma = routed ? &tmA0 : &tmA1;
+                const CUtensorMap* mb = routed ? &tmB0 : &tmB1;
+                int brow[Cfg<BN>::B_LOADS];
+                b_tile_rows<BN, EPI>(p, gt, brow);
+                const int a_row = gt.a_row + BM * (int)rank;  // this CTA's 128 rows
+                for (int kb = 0; kb < nkb; ++kb, ++item) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, args.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool fresh = item >= prefilled;
+                    if (leader) {
+                        // arms the stage for both CTAs' bytes
+                        if (fresh) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                        tma_load_2d(sA + stage * C::A_BYTES, ma, &full[stage], kb * BK, a_row);
+                        if (fresh)
+                            tma_load_2d(sB + stage * C::B_BYTES, mb, &full[stage], kb * BK,
+                                        brow[rank]);
+                    } else {
+                        const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+                        tma_load_2d_to_pair_bar(sA + stage * C::A_BYTES, ma, bar, kb * BK, a_row);
+                        if (fresh)
+                            tma_load_2d_to_pair_bar(sB + stage * C::B_BYTES, mb, bar, kb * BK,
+                                                    brow[rank]);
+                    }
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok && leader) {
+                // aborting: let the copies of the armed stages land (both CTAs' bytes)
+                for (int s = 0; s < C::STAGES; ++s)
+                    if ((filled >> s) & 1u) {
+                        volatile int never = 0;
+                        mbar_wait(&full[s], (fill_parity >> s) & 1u, &never, p.status, kDrainNs);
+                    }
+            } else if (!ok) {
+                // the odd CTA's copies count on the even CTA's barriers: give
+                // any still in flight time to land in this CTA's shared memory
+                const unsigned long long t0 = globaltimer();
+                while (globaltimer() - t0 < 200000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // -------------------------------------------- MMA issuer (even CTA)
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int w = cluster; w < total && ok; w += nclusters, ++local) {
+                const int b = local & 1;
+                const uint32_t tph = (local >> 1) & 1;
+                if (!mbar_wait(&tempty[b], tph ^ 1, abort_flag, p.status, args.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status, args.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_sw128(smem_u32(sA + stage * C::A_BYTES));
+                    const uint64_t bd = sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BKH / 16; ++kk)
+                        umma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, C::IDESC,
+                                       (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit_pair_mc(&empty[stage], 0x3);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok && !(args.hold_first_acc && local == 0)) umma_commit_pair_mc(&tfull[b], 0x3);
+            }
+            // every pair MMA completes before the pair's TMEM and shared memory are released
+            umma_commit_pair_mc(drain, 0x1);
+            volatile int never = 0;
+            mbar_wait(drain, 0, &never, p.status, kDrainNs);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5, both CTAs)
+        if (p.fin_acc_mem && blockIdx.x == 0) {
+            const AuxAcc acc = aux_acc_at(p.fin_acc_mem, p.E, kAuxGroups);
+            const AuxOut out{p.fin_f, p.fin_P, p.fin_I, p.fin_out3, p.fin_w_imp};
+            aux_finalize(p.T, p.E, p.fin_k, acc, out, threadIdx.x - 64, 128, EpilogueBar{});
+        }
+        const int q = warp & 3;
+        const int trow = BM * (int)rank + 32 * q + lane;  // this thread's row of the 256-row tile
+        const uint64_t pol_o = l2_evict_last_policy();
+        const uint32_t tempty_remote0 = mapa_shared(smem_u32(&tempty[0]), 0);
+        const uint32_t tempty_remote1 = mapa_shared(smem_u32(&tempty[1]), 0);
+        int local = 0;
+        for (int w = cluster; w < total; w += nclusters, ++local) {
+            const GroupTile gt = decode_tile(p, mt_start, nt, 2 * BM, w);
+            const int b = local & 1;
+            const uint32_t tph = (local >> 1) & 1;
+            if (!mbar_wait(&tfull[b], tph, abort_flag, p.status, args.wait_ns)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t)(b * BN) + ((uint32_t)(32 * q) << 16);
+            const bool rv = trow < gt.rows;
+            const bool routed = gt.g < p.E;
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(routed ? p.out0 : p.out1);
+            uint32_t* stg = reinterpret_cast<uint32_t*>(staging) + q * 32 * 20;
+            const bool keep_l2 = MOE_TC_L2_HINTS && p.out_l2_keep;
+            int dst_row = rv ? gt.out_row + trow : -1;
+            if (EPI == EPI_GLU) {
+                // columns 0..127 hold the gate half (from the even CTA's
+                // weight rows), 128..255 the up half (the odd CTA's)
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    float g[16], u[16], v[32];
+                    tmem_ld16x2(taddr + c, taddr + 128 + c, g, u);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = silu(g[i]) * u[i];
+                    tmem_ld16x2(taddr + c + 16, taddr + 128 + c + 16, g, u);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[16 + i] = silu(g[i]) * u[i];
+                    const int n0 = gt.n_tile * 128 + c;
+                    if (n0 < p.N) store_rows32_bf16(out, p.N, n0, dst_row, v, stg, keep_l2, pol_o);
+                }
+            } else {
+                const int act = p.glu ? -1 : p.act;
+                float scale = 1.f;
+                if (routed && p.scatter_rows) {
+                    const int t = rv ? p.scatter_rows[gt.out_row + trow] : 0;
+                    out = reinterpret_cast<__nv_bfloat16*>(p.scatter_out);
+                    dst_row = rv ? t : -1;
+                    scale = rv ? p.scatter_scale[t] : 0.f;
+                }
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+                    const int n0 = gt.n_tile * BN + c;
+                    if (n0 < p.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = act_apply(act, v[i]) * scale;
+                        store_rows32_bf16(out, p.N, n0, dst_row, v, stg, keep_l2, pol_o);
+                    }
+                }
+                if (p.fold_cnt) fold_tile(p, gt, routed, trow, rv);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(&tempty[b]);
+                else
+                    mbar_arrive_remote(b ? tempty_remote1 : tempty_remote0);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // no CTA of the pair frees its TMEM or shared memory, or exits, while
+    // the pair's MMAs (drained above), copies or remote arrives may use them
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+}
+
+// Launches the pair kernel: clusters of two CTAs on SM pairs, at most one
+// cluster per two SMs.
+template <int EPI>
+static cudaError_t launch_pair(const TcArgs& a, cudaStream_t st) {
+    using C = PairCfg;
+    const GroupedGemm& p = a.p;
+    CUtensorMap mA0, mA1, mB0, mB1;
+    const int G = p.E + p.S;
+    if (!make_map(&mA0, p.A0 ? p.A0 : p.A1, p.A0 ? p.rows_a0 : p.rows_a1, p.K, BM) ||
+        !make_map(&mA1, p.A1 ? p.A1 : p.A0, p.A1 ? p.rows_a1 : p.rows_a0, p.K, BM))
+        return cudaErrorInvalidValue;
+    const int brows0 = p.E * p.b_rows_group, brows1 = p.S * p.b_rows_group;
+    if (!make_map(&mB0, p.B0 ? p.B0 : p.B1, p.B0 ? brows0 : brows1, p.K, 128) ||
+        !make_map(&mB1, p.B1 ? p.B1 : p.B0, p.B1 ? brows1 : brows0, p.K, 128))
+        return cudaErrorInvalidValue;
+    const size_t smem = C::smem_bytes(G);
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const int ncol_tile = EPI == EPI_GLU ? 128 : C::BN;
+    const long long nt = (p.N + ncol_tile - 1) / ncol_tile;
+    const int MT = 2 * BM;
+    long long mt = (long long)p.max_rows0 / MT + p.E + (long long)p.S * ((p.T + MT - 1) / MT);
+    if (p.E == 0) mt = (long long)p.S * ((p.T + MT - 1) / MT);
+    const long long bound = std::max<long long>(1, mt * nt);
+    const int nclusters = (int)std::min<long long>(bound, std::max(1, num_sms() / 2));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * nclusters);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<EPI>, mA0, mA1, mB0, mB1, a);
+}
+
 }  // namespace tc
 
 cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStream_t st) {
@@ -916,6 +1371,8 @@ cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStr
     a.wait_ns = wait_limit_ns();
     a.hold_first_acc = hold_first_accumulator();
     const bool wef = MOE_TC_L2_HINTS && g.b_evict_first;
+    if (g.pair && !wef)
+        return g.glu ? tc::launch_pair<tc::EPI_GLU>(a, st) : tc::launch_pair<tc::EPI_ACT>(a, st);
     if (g.glu)
         return wef ? tc::launch<256, tc::EPI_GLU, true>(a, st)
                    : tc::launch<256, tc::EPI_GLU, false>(a, st);

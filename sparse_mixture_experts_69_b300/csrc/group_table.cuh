@@ -3,8 +3,11 @@
 // Group g < E is routed expert g (rows offsets[g] .. offsets[g+1]-1 of A0);
 // group E + s is shared expert s (T rows of A1). Each group is cut into
 // ceil(M_g / BM) row tiles and nt column tiles. Tiles are numbered group by
-// group; inside a group column-tile-major, row tiles consecutive, so CTAs that
-// run at the same time share the same weight tile through L2.
+// group. Inside a group the row tiles are taken in blocks of rb
+// (GroupedGemm::row_block; 0: one block of all of them), and inside a block
+// column-tile-major with the block's row tiles consecutive: CTAs that run at
+// the same time share a weight tile through L2, and a block's token rows stay
+// in L2 while every weight tile of the expert passes over them.
 #pragma once
 
 #include "moe_internal.cuh"
@@ -78,9 +81,25 @@ __device__ __forceinline__ void build_tile_table(const GroupedGemm& p, int BM, i
     if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DEV_BAD_ARG);
 }
 
+// (row tile, column tile) of the local-th tile of a group of mt row tiles
+// and nt column tiles, in blocks of rb row tiles (rb <= 0: one block).
+__device__ __forceinline__ void tile_position(int local, int mt, int nt, int rb, int* m,
+                                              int* n) {
+    if (rb <= 0 || rb >= mt) {
+        *n = local / mt;
+        *m = local - *n * mt;
+        return;
+    }
+    const int blk = local / (rb * nt);
+    const int within = local - blk * rb * nt;
+    const int rows = min(rb, mt - blk * rb);  // row tiles of this block
+    *n = within / rows;
+    *m = blk * rb + (within - *n * rows);
+}
+
 // Valid rows of tile `tile` (at most BM) from the shared-memory tables alone.
 __device__ __forceinline__ int tile_rows(const int* mt_start, const int* grows, int G, int nt,
-                                         int BM, int tile) {
+                                         int BM, int tile, int rb) {
     int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -88,8 +107,9 @@ __device__ __forceinline__ int tile_rows(const int* mt_start, const int* grows, 
         else hi = mid - 1;
     }
     const int mt = mt_start[lo + 1] - mt_start[lo];
-    const int m0 = ((tile - mt_start[lo] * nt) % mt) * BM;
-    return min(BM, grows[lo] - m0);
+    int m, n;
+    tile_position(tile - mt_start[lo] * nt, mt, nt, rb, &m, &n);
+    return min(BM, grows[lo] - m * BM);
 }
 
 template <bool L2 = false>
@@ -106,9 +126,9 @@ __device__ __forceinline__ GroupTile decode_tile(const GroupedGemm& p, const int
     GroupTile t;
     t.g = lo;
     const int mt = mt_start[lo + 1] - mt_start[lo];
-    const int local = tile - mt_start[lo] * nt;
-    t.n_tile = local / mt;
-    t.m0 = (local % mt) * BM;
+    int m;
+    tile_position(tile - mt_start[lo] * nt, mt, nt, p.row_block, &m, &t.n_tile);
+    t.m0 = m * BM;
     bool bad = false;
     int a_row, out_row;
     const int M = group_rows<L2>(p, lo, &a_row, &out_row, &bad);

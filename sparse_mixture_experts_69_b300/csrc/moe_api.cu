@@ -8,6 +8,19 @@
 
 #include "aux_common.cuh"
 
+// Token rows (A operand) of one block of the expert GEMMs' tile order, in MB
+// (group_table.cuh); 0: no blocks (each weight tile sweeps all of a group's
+// rows before the next).
+#ifndef MOE_ROW_BLOCK_MB
+#define MOE_ROW_BLOCK_MB 32
+#endif
+
+// 1: the expert GEMMs of layers whose experts hold many rows run 256-row
+// tiles on CTA pairs (gemm_tc.cu, grouped_gemm_pair_kernel); 0: never.
+#ifndef MOE_PAIR_TILES
+#define MOE_PAIR_TILES 1
+#endif
+
 namespace moe {
 
 cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStream_t st);
@@ -347,6 +360,16 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     // h is read back by the down projection: keep it in L2 when it fits with
     // room to spare (126 MB of L2), else let it stream
     up.out_l2_keep = (double)(s.R_max + (double)s.S * s.T) * s.F * s.esize <= 80e6 ? 1 : 0;
+    // experts of at least 1024 rows on average (the Mixtral-shaped layer):
+    // 256-row tiles on CTA pairs, which halve each SM's weight bytes per MMA
+    const int pair = MOE_PAIR_TILES && (long long)s.R_max >= 1024LL * s.E ? 1 : 0;
+    up.pair = pair;
+    const int tile_rows_m = pair ? 256 : 128;
+    auto row_block = [&](int K) {
+        const double tile_mb = (double)tile_rows_m * K * s.esize / 1e6;
+        return MOE_ROW_BLOCK_MB > 0 ? std::max(1, (int)(MOE_ROW_BLOCK_MB / tile_mb)) : 0;
+    };
+    up.row_block = row_block(s.d);
     MOE_CUDA(launch_grouped_gemm(s, up, st));
     GroupedGemm dn{};
     dn.offsets = offsets;
@@ -383,6 +406,8 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     }
     dn.status = status;
     dn.b_evict_first = one_tile;
+    dn.pair = pair;
+    dn.row_block = row_block(s.F);
     // the up projection just launched signals only after its wait: when this
     // launch starts, whatever wrote the offsets before it is complete
     dn.early = 1;

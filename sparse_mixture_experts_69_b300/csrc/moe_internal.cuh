@@ -239,6 +239,11 @@ struct GroupedGemm {
     // once per launch: weights get an evict-first L2 policy and leave L2
     // before the activations (tcgen05 only; set for T <= 128)
     int b_evict_first;
+    // 1: 256-row tiles on CTA pairs (tcgen05 pair MMA, clusters of two CTAs),
+    // for groups of many rows (tcgen05 only)
+    int pair;
+    // row tiles per block of the tile order (group_table.cuh); 0: one block
+    int row_block;
 };
 cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream_t st);
 

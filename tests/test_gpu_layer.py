@@ -324,3 +324,24 @@ def test_folded_combine_equals_the_combine_kernel(cuda_device, name, kw):
         o, _ = layer_vs_oracle(wl.with_(combine_mode=mode), cuda_device, inp)
         ys.append(o["y"])
     assert torch.equal(ys[0], ys[1])
+
+
+@pytest.mark.parametrize("k,T,act", [(1, 8192, moe.MOE_RELU), (2, 4096, moe.MOE_SWIGLU),
+                                     (2, 4096, moe.MOE_GELU)])
+def test_pair_tiles_with_ragged_experts(cuda_device, k, T, act):
+    """Experts that hold 1024 rows or more on average (R_max >= 1024 E) run
+    the expert GEMMs on CTA pairs: 256-row tiles, each CTA holding 128 rows
+    and half of the weight tile, one pair MMA (M = 256) per K step. A strong
+    Zipf skew puts experts of thousands of rows (full tiles and a last tile
+    of 129..255 rows), of at most 128 rows (the odd CTA's rows all belong to
+    the next expert and are not stored) and of a handful of rows into the
+    same launches; y of every token matches the oracle fed the GPU's routing
+    (top-1: the down GEMM scatters gate * output into y; top-2: the combine
+    kernel)."""
+    from gpu_helpers import layer_vs_oracle
+    wl = WORKLOADS["mixtral"].with_(T=T, d_model=256, d_ff=256, zipf_s=1.5, top_k=k, act=act)
+    c = wl.cfg
+    assert c.T * k >= 1024 * c.n_experts
+    o, _ = layer_vs_oracle(wl, cuda_device)
+    counts = np.bincount(o["ids"].cpu().numpy().ravel(), minlength=c.n_experts)
+    assert counts.max() > 8 * 256 and ((counts > 0) & (counts <= 128)).any()
