@@ -380,7 +380,7 @@ def launches_per_step(wl):
     """Kernels of this library one step launches. Layer path: [Wg transpose
     (bf16)], router GEMM, fused selection + histogram + statistics, capacity
     scan + slots (one launch up to 256 token blocks), permute, up GEMM, down
-    GEMM, [combine: skipped where the down GEMM writes y itself, by its
+    GEMM (each two launches for layers of mixed expert sizes), [combine: skipped where the down GEMM writes y itself, by its
     folded combine (bf16, packed rows, combine_mode = 1) or, for top-1
     without shared experts, by scattering gate * output], [bias update]. Overflow policies:
     one capacity kernel instead of scan + slots; expert choice: select +
@@ -396,7 +396,11 @@ def launches_per_step(wl):
     if ec:
         return route_launches + 2 + 2 + 1
     cap_launches = 1 if policy else (1 if (T + 255) // 256 <= 256 else 2)
-    return (route_launches + cap_launches + 1 + 2 + (0 if combine_in_gemm else 1)
+    # expert projections: one launch each, or two for layers of mixed expert
+    # sizes (256 <= T k / E < 1024 rows per expert, bf16, T > 128)
+    split = c.dtype == 1 and T > 128 and 256 * c.n_experts <= T * k < 1024 * c.n_experts
+    gemm_launches = 4 if split else 2
+    return (route_launches + cap_launches + 1 + gemm_launches + (0 if combine_in_gemm else 1)
             + (1 if wl.bias_rate else 0))
 
 

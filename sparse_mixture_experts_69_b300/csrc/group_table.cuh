@@ -24,6 +24,13 @@ struct GroupTile {
     int b_row;    // first B row of the group (in B0 or B1)
 };
 
+// Whether a group of `rows` rows takes part in this launch (GroupedGemm::
+// rows_lo / rows_hi: a layer can run its many-row and its few-row experts as
+// two launches with different tile shapes; 0 means no bound).
+__device__ __forceinline__ bool in_launch(const GroupedGemm& p, int rows) {
+    return rows >= p.rows_lo && (p.rows_hi <= 0 || rows <= p.rows_hi);
+}
+
 // L2: read the offsets from L2 (ld.global.cg), for reads made before the wait
 // for the preceding kernel (the offsets are final by then, but an L1 line
 // could predate them); otherwise plain loads.
@@ -41,12 +48,12 @@ __device__ __forceinline__ int group_rows(const GroupedGemm& p, int g, int* a_ro
         }
         *a_row = lo;
         *out_row = lo;
-        return hi - lo;
+        return in_launch(p, hi - lo) ? hi - lo : 0;
     }
     const int s = g - p.E;
     *a_row = p.a1_row0 + s * p.a1_stride;
     *out_row = s * p.T;
-    return p.T;
+    return in_launch(p, p.T) ? p.T : 0;
 }
 
 // Warp 0 of the block fills mt_start[0..G] (row-tile prefix) and, if grows is

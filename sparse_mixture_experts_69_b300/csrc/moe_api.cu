@@ -20,6 +20,15 @@
 #ifndef MOE_PAIR_TILES
 #define MOE_PAIR_TILES 1
 #endif
+// ... when the experts hold at least this many rows on average (R_max / E)
+#ifndef MOE_PAIR_MIN_ROWS
+#define MOE_PAIR_MIN_ROWS 1024
+#endif
+// 1: layers of mixed expert sizes run each expert projection as two launches
+// (few-row experts on single CTAs, many-row experts on CTA pairs); 0: one.
+#ifndef MOE_SPLIT_LAUNCH
+#define MOE_SPLIT_LAUNCH 1
+#endif
 
 namespace moe {
 
@@ -362,15 +371,36 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     up.out_l2_keep = (double)(s.R_max + (double)s.S * s.T) * s.F * s.esize <= 80e6 ? 1 : 0;
     // experts of at least 1024 rows on average (the Mixtral-shaped layer):
     // 256-row tiles on CTA pairs, which halve each SM's weight bytes per MMA
-    const int pair = MOE_PAIR_TILES && (long long)s.R_max >= 1024LL * s.E ? 1 : 0;
-    up.pair = pair;
-    const int tile_rows_m = pair ? 256 : 128;
-    auto row_block = [&](int K) {
-        const double tile_mb = (double)tile_rows_m * K * s.esize / 1e6;
+    const int pair = MOE_PAIR_TILES && (long long)s.R_max >= (long long)MOE_PAIR_MIN_ROWS * s.E ? 1 : 0;
+    // experts of mixed sizes (at least 256 rows per expert on average, but
+    // not all large: the DeepSeek-shaped layer): each projection runs as two
+    // launches, the experts of fewer than kSplitRows rows on single CTAs,
+    // then the others (and the shared experts) on CTA pairs
+    constexpr int kSplitRows = 512;
+    const bool split = MOE_PAIR_TILES && MOE_SPLIT_LAUNCH && !pair && !one_tile &&
+                       s.dtype == MOE_BF16 && (long long)s.T * s.k >= 256LL * s.E;
+    auto row_block = [&](int K, int tile_rows) {
+        const double tile_mb = (double)tile_rows * K * s.esize / 1e6;
         return MOE_ROW_BLOCK_MB > 0 ? std::max(1, (int)(MOE_ROW_BLOCK_MB / tile_mb)) : 0;
     };
-    up.row_block = row_block(s.d);
-    MOE_CUDA(launch_grouped_gemm(s, up, st));
+    // one projection, as one launch or as the two launches described above
+    auto launch_parts = [&](GroupedGemm g, int K) -> cudaError_t {
+        g.pair = pair;
+        g.row_block = row_block(K, pair ? 256 : 128);
+        if (!split) return launch_grouped_gemm(s, g, st);
+        GroupedGemm light = g;
+        light.rows_hi = kSplitRows - 1;
+        cudaError_t err = launch_grouped_gemm(s, light, st);
+        if (err != cudaSuccess) return err;
+        GroupedGemm heavy = g;
+        heavy.rows_lo = kSplitRows;
+        heavy.pair = 1;
+        heavy.row_block = row_block(K, 256);
+        heavy.fin_acc_mem = nullptr;  // the first launch finalises the statistics
+        heavy.early = 1;              // the launch before it signals after its wait
+        return launch_grouped_gemm(s, heavy, st);
+    };
+    MOE_CUDA(launch_parts(up, s.d));
     GroupedGemm dn{};
     dn.offsets = offsets;
     dn.E = s.E;
@@ -406,12 +436,10 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
     }
     dn.status = status;
     dn.b_evict_first = one_tile;
-    dn.pair = pair;
-    dn.row_block = row_block(s.F);
     // the up projection just launched signals only after its wait: when this
     // launch starts, whatever wrote the offsets before it is complete
     dn.early = 1;
-    MOE_CUDA(launch_grouped_gemm(s, dn, st));
+    MOE_CUDA(launch_parts(dn, s.F));
     return MOE_OK;
 }
 

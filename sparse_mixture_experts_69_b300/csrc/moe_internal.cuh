@@ -244,6 +244,8 @@ struct GroupedGemm {
     int pair;
     // row tiles per block of the tile order (group_table.cuh); 0: one block
     int row_block;
+    // only groups of rows_lo .. rows_hi rows take part (0: no bound)
+    int rows_lo, rows_hi;
 };
 cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream_t st);
 

@@ -345,3 +345,22 @@ def test_pair_tiles_with_ragged_experts(cuda_device, k, T, act):
     o, _ = layer_vs_oracle(wl, cuda_device)
     counts = np.bincount(o["ids"].cpu().numpy().ravel(), minlength=c.n_experts)
     assert counts.max() > 8 * 256 and ((counts > 0) & (counts <= 128)).any()
+
+
+@pytest.mark.parametrize("mode", [moe.MOE_COMBINE_KERNEL, moe.MOE_COMBINE_IN_GEMM])
+def test_split_launch_for_mixed_expert_sizes(cuda_device, mode):
+    """Layers whose experts hold 256..1023 rows on average but of very mixed
+    sizes (DeepSeek-shaped: the selection bias sends most tokens to a few
+    experts) run each expert projection as two launches: experts of fewer
+    than 512 rows on single CTAs, the others and the shared expert on CTA
+    pairs. Here 9 experts hold 630..2048 rows and 9 hold 1..297; y of every
+    token matches the oracle fed the GPU's routing, with the combine kernel
+    and with the combine folded into the (two) down launches."""
+    from gpu_helpers import layer_vs_oracle
+    wl = WORKLOADS["deepseek"].with_(T=2048, d_model=256, d_ff=256, n_experts=32,
+                                     combine_mode=mode)
+    c = wl.cfg
+    assert 256 * c.n_experts <= c.T * c.top_k < 1024 * c.n_experts
+    o, _ = layer_vs_oracle(wl, cuda_device)
+    counts = o["counts"].cpu().numpy()
+    assert (counts >= 512).sum() >= 4 and ((counts > 0) & (counts < 512)).sum() >= 4
