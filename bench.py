@@ -466,6 +466,12 @@ def measure(wl, steps, warmup, dev, pg, world, local, cpu_budget, want_cpu, auto
         if pg:
             pg.barrier()
 
+    def reset_bias():
+        # every timed phase starts from the workload's initial selection bias:
+        # the bias update moves the routing a little each step
+        if bias is not None:
+            bias.copy_(inp["sel_bias"])
+
     # ------------------------------------------------ device-resident timing
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -478,6 +484,7 @@ def measure(wl, steps, warmup, dev, pg, world, local, cpu_budget, want_cpu, auto
     if auto_steps:  # about half a second of timed work
         est = ev0.elapsed_time(ev1) / warmup
         steps = int(min(4000, max(20, 500.0 / max(est, 1e-3))))
+    reset_bias()
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -635,6 +642,7 @@ def measure(wl, steps, warmup, dev, pg, world, local, cpu_budget, want_cpu, auto
     torch.cuda.synchronize()
     est = (time.perf_counter() - t0) / 10
     K2 = int(max(200, 1.2 / max(est, 1e-6)))
+    reset_bias()
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()

@@ -364,3 +364,27 @@ def test_split_launch_for_mixed_expert_sizes(cuda_device, mode):
     o, _ = layer_vs_oracle(wl, cuda_device)
     counts = o["counts"].cpu().numpy()
     assert (counts >= 512).sum() >= 4 and ((counts > 0) & (counts < 512)).sum() >= 4
+
+
+@pytest.mark.parametrize("kind", ["all_few_row", "all_many_row"])
+def test_split_launch_with_one_kind_of_expert(cuda_device, kind):
+    """The same layer shape class (256..1023 rows per expert on average) when
+    every expert falls on one side of 512 rows, so that one of the two
+    launches of each projection has no tile: uniform routing over 16 experts
+    (about 256 rows each, no shared expert: the many-row launch is empty),
+    and 8 experts of about 700 rows with a shared expert (the few-row launch
+    is empty). y of every token matches the oracle."""
+    from gpu_helpers import layer_vs_oracle
+    base = WORKLOADS["deepseek"].with_(d_model=256, d_ff=256, sel_bias=False, bias_rate=0.0)
+    if kind == "all_few_row":
+        wl = base.with_(T=2048, n_experts=16, top_k=2, n_shared=0)
+    else:
+        wl = base.with_(T=2800, n_experts=8, top_k=2)
+    c = wl.cfg
+    assert 256 * c.n_experts <= c.T * c.top_k < 1024 * c.n_experts
+    o, _ = layer_vs_oracle(wl, cuda_device)
+    counts = o["counts"].cpu().numpy()
+    if kind == "all_few_row":
+        assert counts.max() < 512
+    else:
+        assert counts.min() >= 512
