@@ -260,11 +260,10 @@ __device__ __forceinline__ void draw_token_eps(const SelectArgs& a, int t, Token
     }
 }
 
-// Sorts n = EPL (a power of two, at most 8) (key, expert, probability)
-// triples into descending key order, equal keys by ascending expert, with a
-// bitonic network of compile-time compare-exchanges (registers only).
+// Sorts N (a power of two, at most 8) 64-bit keys into descending order with
+// a bitonic network of compile-time compare-exchanges (registers only).
 template <int N>
-__device__ __forceinline__ void sort_desc(unsigned (&k)[N], int (&e)[N], float (&p)[N]) {
+__device__ __forceinline__ void sort_desc64(unsigned long long (&k)[N]) {
 #pragma unroll
     for (int size = 2; size <= N; size <<= 1)
 #pragma unroll
@@ -276,29 +275,23 @@ __device__ __forceinline__ void sort_desc(unsigned (&k)[N], int (&e)[N], float (
                     // within each bitonic block of `size`, the first half of
                     // the blocks sorts descending, the second ascending
                     const bool desc = ((i & size) == 0) || size == N;
-                    const bool j_first = k[j] > k[i] || (k[j] == k[i] && e[j] < e[i]);
-                    if (j_first == desc) {
-                        const unsigned tk = k[i];
-                        k[i] = k[j];
-                        k[j] = tk;
-                        const int te = e[i];
-                        e[i] = e[j];
-                        e[j] = te;
-                        const float tp = p[i];
-                        p[i] = p[j];
-                        p[j] = tp;
-                    }
+                    const unsigned long long hi = k[i] > k[j] ? k[i] : k[j];
+                    const unsigned long long lo = k[i] > k[j] ? k[j] : k[i];
+                    k[i] = desc ? hi : lo;
+                    k[j] = desc ? lo : hi;
                 }
             }
 }
 
 // Selection for token t from its loaded inputs. On return pr[] holds this
-// lane's probabilities, and lanes j < nc hold the j-th candidate (my_id) and
-// its gate (my_w): p_j over the sum of p of the first k candidates (renorm),
-// else p_j.
+// lane's probabilities (also stored to sp[0..E), the warp's row of shared
+// memory, when sp is not NULL; E <= 256 needs it), and lanes j < nc hold the
+// j-th candidate (my_id) and its gate (my_w): p_j over the sum of p of the
+// first k candidates (renorm), else p_j.
 template <int EPL>
 __device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const TokenRegs<EPL>& r,
-                                            float (&pr)[EPL], int& my_id, float& my_w) {
+                                            float (&pr)[EPL], float* sp, int& my_id,
+                                            float& my_w) {
     const int lane = threadIdx.x & 31;
     const int E = a.E;
     const size_t row = (size_t)t * E;
@@ -342,8 +335,9 @@ __device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const To
             pr[i] = e < E ? __expf(H[i] - m) : 0.f;
             part += pr[i];
         }
-        // the largest term is e^0 = 1, so the sum is at least 1
-        const float inv = 1.f / warp_sum(part);
+        // the largest term is e^0 = 1, so the sum is at least 1; the
+        // reciprocal is correctly rounded, as 1 / sum would be
+        const float inv = __frcp_rn(warp_sum(part));
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
@@ -358,45 +352,44 @@ __device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const To
         }
     }
     if (__any_sync(0xffffffffu, nonfinite) && lane == 0) flag_status(a.status, DEV_NONFINITE);
-
-    // top-nc: nc rounds of a warp arg-max ordered by (score desc, index asc).
-    float my_p = 0.f, psum = 0.f;
-    my_id = 0;
-    if (EPL <= 8) {
-        // Each lane sorts its candidates once (a sorting network on (key desc,
-        // expert asc)); a round is then the warp maximum of the lanes' first
-        // keys, the warp minimum of the expert index among the lanes holding
-        // it, and a shift of the winning lane's list.
-        int ex[EPL];
-        float pv[EPL];
+    if (sp) {
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            ex[i] = lane + 32 * i < E ? lane + 32 * i : 0x7FFFFFFF;
-            pv[i] = pr[i];
+            const int e = lane + 32 * i;
+            if (e < E) sp[e] = pr[i];
         }
-        sort_desc<EPL>(key, ex, pv);
-        for (int j = 0; j < a.nc; ++j) {
-            const bool has = ex[0] != 0x7FFFFFFF;
-            const unsigned top = __reduce_max_sync(0xffffffffu, has ? key[0] : 0u);
-            const int win = (int)__reduce_min_sync(
-                0xffffffffu, (has && key[0] == top) ? (unsigned)ex[0] : 0x7FFFFFFFu);
-            const int owner = win & 31;
-            const float pj = __shfl_sync(0xffffffffu, pv[0], owner);
-            if (lane == owner) {
+    }
+
+    // top-nc: nc rounds of a warp arg-max ordered by (score desc, index asc).
+    float my_p = 0.f;
+    my_id = 0;
+    if (EPL <= 8) {
+        // One 64-bit key per expert: the score key, and below it the
+        // complement of the expert index, so that the unsigned order is
+        // (score desc, index asc) and every key is distinct (0: no expert).
+        // Each lane sorts its keys once; a round is then the warp maximum of
+        // the lanes' first keys (high word, then low word among the lanes
+        // holding that high word) and a shift of the winning lane's list.
+        unsigned long long k64[EPL];
 #pragma unroll
-                for (int i = 0; i + 1 < EPL; ++i) {
-                    key[i] = key[i + 1];
-                    ex[i] = ex[i + 1];
-                    pv[i] = pv[i + 1];
-                }
-                ex[EPL - 1] = 0x7FFFFFFF;
-            }
-            if (j < a.k) psum += pj;
-            if (lane == j) {
-                my_id = win;
-                my_p = pj;
-            }
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            k64[i] = e < E ? ((unsigned long long)key[i] << 32) | (unsigned)~e : 0ull;
         }
+        sort_desc64<EPL>(k64);
+        for (int j = 0; j < a.nc; ++j) {
+            const unsigned hi = (unsigned)(k64[0] >> 32), lo = (unsigned)k64[0];
+            const unsigned top = __reduce_max_sync(0xffffffffu, hi);
+            const int win = (int)~__reduce_max_sync(0xffffffffu, hi == top ? lo : 0u);
+            if (lane == (win & 31)) {
+#pragma unroll
+                for (int i = 0; i + 1 < EPL; ++i) k64[i] = k64[i + 1];
+                k64[EPL - 1] = 0ull;
+            }
+            if (lane == j) my_id = win;
+        }
+        __syncwarp();  // every lane's sp[] stores are visible
+        if (lane < a.nc) my_p = sp[my_id];
     } else {
         // a lane-local scan per round over the candidates not yet taken
         unsigned taken = 0;
@@ -421,13 +414,15 @@ __device__ __forceinline__ void select_regs(const SelectArgs& a, int t, const To
                 if (i == slot_i) mine = pr[i];
             if (lane == owner) taken |= 1u << slot_i;
             const float pj = __shfl_sync(0xffffffffu, mine, owner);
-            if (j < a.k) psum += pj;
             if (lane == j) {
                 my_id = win;
                 my_p = pj;
             }
         }
     }
+    // the gates' denominator: the first k candidates' probabilities, summed
+    // over the warp in a fixed order
+    const float psum = warp_sum(lane < a.k ? my_p : 0.f);
     my_w = a.renorm ? my_p / psum : my_p;
     if (lane < a.nc && a.ids) {
         a.ids[(size_t)t * a.nc + lane] = my_id;
@@ -452,10 +447,13 @@ __global__ void __launch_bounds__(32 * kSelWarps, EPL <= 8 ? 4 : 1) router_selec
     pdl_trigger();
     if (t >= a.T) return;
     load_token<EPL, PARTS>(a, t, r);
+    // the warp's probabilities, where the candidates' gates are looked up
+    __shared__ float s_prob[EPL <= 8 ? kSelWarps * 32 * EPL : 1];
     float pr[EPL];
     int id;
     float w;
-    select_regs<EPL>(a, t, r, pr, id, w);
+    select_regs<EPL>(a, t, r, pr, EPL <= 8 ? s_prob + (threadIdx.x >> 5) * 32 * EPL : nullptr, id,
+                     w);
 }
 
 static int sel_blocks(int T) { return (T + kSelWarps - 1) / kSelWarps; }
@@ -522,12 +520,7 @@ __global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : EPL == 8 ? 4 : 
         float pr[EPL];
         int id;
         float w;
-        select_regs<EPL>(a, t, r, pr, id, w);
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) mine[e] = pr[i];
-        }
+        select_regs<EPL>(a, t, r, pr, mine, id, w);
         if (lane < a.k) {
             atomicAdd(&sI[id], to_fix(w));
             atomicAdd(&sC[id], 1u);

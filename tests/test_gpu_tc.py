@@ -21,6 +21,12 @@ pytestmark = pytest.mark.gpu
     (129, 7168, 256, 8, False, False, True),
     (64, 4096, 64, 6, False, False, False),
     (77, 512, 300, 4, False, False, False),
+    # 256-wide routers run on CTA pairs (256-row tiles): a ragged last pair
+    # tile with the K range split, an unsplit one with a column tail and the
+    # logit offset, and a noisy router whose 2E = 256 columns hold z and zn
+    (1000, 7168, 256, 8, False, False, True),
+    (300, 256, 200, 4, False, True, False),
+    (500, 512, 128, 2, True, False, False),
 ])
 def test_router_bf16(cuda_device, T, d, E, k, noisy, offset, bias):
     cfg = moe.Config(T=T, d_model=d, n_experts=E, top_k=k, d_ff=64, dtype=moe.MOE_BF16)
