@@ -142,9 +142,9 @@ MOE_API moe_status moe_capacity(const moe_config* cfg, int32_t* capacity, int32_
 MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Zero the parts of the workspace that must read zero between calls: the
- * status word and the counters the statistics and capacity kernels reset
- * after each use (enqueued on stream). Call once on a new workspace before its
- * first use, or allocate the workspace zero-filled. */
+ * status word and the counters the statistics, capacity and expert-GEMM
+ * kernels reset after each use (enqueued on stream). Call once on a new
+ * workspace before its first use, or allocate the workspace zero-filled. */
 MOE_API moe_status moe_workspace_reset(const moe_config* cfg, void* ws, size_t ws_bytes,
                                        moe_stream_t stream);
 

@@ -159,6 +159,37 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile 
         }
     }
 }
+// As mbar_wait, for a barrier whose phase is completed by a remote arrive
+// with release at cluster scope: the completed wait acquires at cluster
+// scope, so the releasing CTA's shared::cluster stores are visible.
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __noinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t parity,
+                                                   volatile int* abort_flag, int* status,
+                                                   unsigned long long limit_ns) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_acq_cluster(a, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_acq_cluster(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            flag_status(status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y) {
     asm volatile(
@@ -271,6 +302,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 // tcgen05.ld of an accumulator finished), not data written by this thread.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Remote arrive that releases this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -1025,6 +1064,21 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
 // aborting odd CTA cannot see its own copies complete (they count on the
 // other CTA's barrier), so it waits 200 us, far longer than a copy takes,
 // before that barrier.
+// Work-item ring of the pair kernel's dynamic tile order: slots, and the
+// consumers of each item (the even CTA's MMA issuer, 4 epilogue warps in each
+// CTA, the odd CTA's producer).
+constexpr int kItemRing = 4;
+constexpr int kItemConsumers = 10;
+// tile_ctr[0] is the launch's tile counter, tile_ctr[1] counts the pairs that
+// are done with it; the last pair to finish puts both back to zero for the
+// next launch (which touches them only after its wait for this one).
+__device__ __forceinline__ void release_tile_counter(int* tile_ctr, int nclusters) {
+    __threadfence();
+    if (atomicAdd(tile_ctr + 1, 1) == nclusters - 1) {
+        atomicExch(tile_ctr, 0);
+        atomicExch(tile_ctr + 1, 0);
+    }
+}
 struct PairCfg {
     static constexpr int BN = 256;
     static constexpr int A_BYTES = BM * BKH * 2;    // own 128 rows x 64
@@ -1043,6 +1097,10 @@ struct PairCfg {
     }
 };
 static_assert(KH == 1, "the pair kernel loads one 64-wide K block per stage");
+// barriers, TMEM slot, abort flag and the work-item ring fit the 256 bytes
+// before the tile table
+static_assert((2 * PairCfg::STAGES + 7 + 2 * kItemRing) * 8 + 4 * kItemRing <= 256,
+              "pair kernel barrier area");
 
 __device__ __forceinline__ uint32_t cluster_id_x() {
     uint32_t r;
@@ -1076,6 +1134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // work-item ring of the dynamic tile order (GroupedGemm::tile_ctr)
+    uint64_t* item_full = drain + 2;
+    uint64_t* item_empty = item_full + kItemRing;
+    volatile int* s_item = reinterpret_cast<volatile int*>(item_empty + kItemRing);
     int* mt_start = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
     int* grows = mt_start + p.E + p.S + 1;
     float* staging = reinterpret_cast<float*>(
@@ -1088,6 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
     const int nt = (p.N + ncol_tile - 1) / ncol_tile;
     const int nkb = (p.K + BK - 1) / BK;
+    const bool dyn = EPI != EPI_ROUTER && p.tile_ctr != nullptr;
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA0);
@@ -1109,6 +1172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // or cluster-wide step (pair 0 stays when it owes the statistics)
     if (cluster >= total && !(p.fin_acc_mem && cluster == 0)) {
         if (early) pdl_wait();
+        if (dyn && leader && threadIdx.x == 0) release_tile_counter(p.tile_ctr, nclusters);
         return;
     }
     if (threadIdx.x == 0) {
@@ -1121,6 +1185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&tempty[b], 8);  // lane 0 of the 4 epilogue warps of each CTA
         }
         mbar_init(drain, 1);
+        for (int s = 0; s < kItemRing; ++s) {
+            mbar_init(&item_full[s], 1);
+            mbar_init(&item_empty[s], kItemConsumers);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1132,7 +1200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_w = 0ull;
     int prefilled = 0;
     if (early && threadIdx.x == 0) {
-        for (int w = cluster; w < total && prefilled < C::STAGES; w += nclusters) {
+        // (dynamic order: only item 0, the one tile known before the wait)
+        for (int w = cluster; w < total && prefilled < C::STAGES && !(dyn && w != cluster);
+             w += nclusters) {
             const int tile = w / ks, sp = w - tile * ks;
             const GroupTile gt = decode_tile<true>(p, mt_start, nt, 2 * BM, tile);
             const CUtensorMap* mb = gt.g < p.E ? &tmB0 : &tmB1;
@@ -1164,6 +1234,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Work items of the pair, in order i = 0, 1, ...: item 0 is tile `cluster`;
+    // after it, every nclusters-th tile (static order), or (dynamic order) the
+    // next tile of the launch-wide counter, which the even CTA's producer
+    // takes one item ahead and hands to the 10 consumers (its MMA issuer, both
+    // CTAs' 4 epilogue warps, the odd CTA's producer) through the ring, the
+    // odd CTA's copy by a remote store released with the remote arrive.
+    // Values >= total end the sequence.
+    auto item_put = [&](int i, int v) -> bool {
+        const int s = i % kItemRing;
+        const uint32_t ph = (uint32_t)(i / kItemRing) & 1u;
+        if (!mbar_wait(&item_empty[s], ph ^ 1u, abort_flag, p.status, args.wait_ns)) return false;
+        s_item[s] = v;
+        st_shared_cluster(mapa_shared(smem_u32((const void*)&s_item[s]), 1), v);
+        mbar_arrive(&item_full[s]);
+        mbar_arrive_remote_release(mapa_shared(smem_u32(&item_full[s]), 1));
+        return true;
+    };
+    // -1: the wait gave up (timeout or abort)
+    auto item_get = [&](int i) -> int {
+        const int s = i % kItemRing;
+        const uint32_t ph = (uint32_t)(i / kItemRing) & 1u;
+        const bool okw =
+            leader ? mbar_wait(&item_full[s], ph, abort_flag, p.status, args.wait_ns)
+                   : mbar_wait_acq_cluster(&item_full[s], ph, abort_flag, p.status, args.wait_ns);
+        return okw ? s_item[s] : -1;
+    };
+    auto item_release = [&](int i) {
+        const int s = i % kItemRing;
+        if (leader)
+            mbar_arrive(&item_empty[s]);
+        else
+            mbar_arrive_remote_release(mapa_shared(smem_u32(&item_empty[s]), 0));
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -1173,7 +1276,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t filled = 0, fill_parity = 0;
             bool ok = true;
             int item = 0;
-            for (int w = cluster; w < total && ok; w += nclusters) {
+            int w_next = 0;
+            for (int it = 0; ok; ++it) {
+                int w = cluster + it * nclusters;
+                if (dyn && leader) {
+                    w = it == 0 ? cluster : w_next;
+                    if (w < total) w_next = nclusters + atomicAdd(p.tile_ctr, 1);  // one ahead
+                    if (!item_put(it, w < total ? w : total)) {
+                        ok = false;
+                        break;
+                    }
+                } else if (dyn) {
+                    w = item_get(it);
+                    if (w < 0) {
+                        ok = false;
+                        break;
+                    }
+                    item_release(it);
+                }
+                if (w >= total) break;
                 const int tile = w / ks, sp = w - tile * ks;
                 const GroupTile gt = decode_tile(p, mt_start, nt, 2 * BM, tile);
                 const bool routed = gt.g < p.E;
@@ -1233,7 +1354,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int local = 0;
             bool ok = true;
-            for (int w = cluster; w < total && ok; w += nclusters, ++local) {
+            for (int it = 0; ok; ++it, ++local) {
+                int w = cluster + it * nclusters;
+                if (dyn) {
+                    w = item_get(it);
+                    if (w < 0) {
+                        ok = false;
+                        break;
+                    }
+                    item_release(it);
+                }
+                if (w >= total) break;
                 const int sp = w % ks;
                 const int b = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
@@ -1282,7 +1413,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tempty_remote0 = mapa_shared(smem_u32(&tempty[0]), 0);
         const uint32_t tempty_remote1 = mapa_shared(smem_u32(&tempty[1]), 0);
         int local = 0;
-        for (int w = cluster; w < total; w += nclusters, ++local) {
+        for (int it = 0;; ++it, ++local) {
+            int w = cluster + it * nclusters;
+            if (dyn) {
+                // lane 0 takes the item for the warp, so the warp stays converged
+                int v = 0;
+                if (lane == 0) {
+                    v = item_get(it);
+                    if (v >= 0) item_release(it);
+                }
+                w = __shfl_sync(0xffffffffu, v, 0);
+                if (w < 0) break;
+            }
+            if (w >= total) break;
             const int tile = w / ks, sp = w - tile * ks;
             const GroupTile gt = decode_tile(p, mt_start, nt, 2 * BM, tile);
             const int b = local & 1;
@@ -1383,6 +1526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync_all();
     tc_fence_after();
     if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    if (dyn && leader && threadIdx.x == 0) release_tile_counter(p.tile_ctr, nclusters);
 }
 
 // Launches the pair kernel: clusters of two CTAs on SM pairs, at most one

@@ -29,6 +29,11 @@
 #ifndef MOE_SPLIT_LAUNCH
 #define MOE_SPLIT_LAUNCH 1
 #endif
+// 1: the CTA-pair expert GEMMs take their tiles from a launch-wide counter
+// (in order), so the tiles in flight stay a window of consecutive tiles
+#ifndef MOE_PAIR_DYNAMIC
+#define MOE_PAIR_DYNAMIC 1
+#endif
 
 namespace moe {
 
@@ -81,6 +86,7 @@ WsLayout ws_layout(const Shape& s) {
     L.blk_hist = take(nblk * E * 4);
     L.cap_ticket = take(16);
     L.seq_ticket = take(16);
+    L.tile_ctr = take(16);
     L.fold_cnt = take(s.dtype == MOE_BF16 ? T * ((d + kDownTileN - 1) / kDownTileN) * 4 : 0);
     L.zero_end = off;
     L.zn = take(T * E * 4);
@@ -359,6 +365,7 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
         up.fin_w_imp = s.w_imp;
     }
     up.status = status;
+    up.tile_ctr = MOE_PAIR_DYNAMIC ? at<int32_t>(ws, L.tile_ctr) : nullptr;
     // T <= 128 (decode): every expert, routed or shared, gets at most one
     // 128-row tile, so every weight tile is read once and the weights may leave
     // L2 first. Measured: decode layer 467 -> 455 us; on the Switch layer,
@@ -435,6 +442,7 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const void* xp,
         dn.fold_y = fold->y;
     }
     dn.status = status;
+    dn.tile_ctr = MOE_PAIR_DYNAMIC ? at<int32_t>(ws, L.tile_ctr) + 2 : nullptr;
     dn.b_evict_first = one_tile;
     // the up projection just launched signals only after its wait: when this
     // launch starts, whatever wrote the offsets before it is complete

@@ -57,6 +57,7 @@ struct WsLayout {
     size_t cap_ticket; // u32 ticket of the fused scan + slot kernel
     size_t fold_cnt;   // [T][down-GEMM column tiles] i32 arrivals of the folded combine
     size_t seq_ticket; // u32 ticket of the sequence-statistics kernel
+    size_t tile_ctr;   // [2][2] i32 tile counters of the CTA-pair expert GEMMs (up, down)
     size_t zero_end;   // end of the zero-between-calls prefix
     size_t zn;         // [T,E] f32 noise logits x.Wnoise
     size_t rpart;      // K parts of a split router GEMM (router_plan), bf16 only
@@ -247,6 +248,10 @@ struct GroupedGemm {
     int row_block;
     // only groups of rows_lo .. rows_hi rows take part (0: no bound)
     int rows_lo, rows_hi;
+    // CTA-pair kernel: [2] launch-wide tile counter and finished-pair count
+    // (zero before the launch, zero again after it) for a dynamic tile order;
+    // NULL: static order
+    int* tile_ctr;
 };
 cudaError_t launch_grouped_gemm(const Shape& s, const GroupedGemm& g, cudaStream_t st);
 
