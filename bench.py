@@ -98,27 +98,46 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def roofline_record(flops, ffn_bytes, ffn_ms, pk, pk_kind, traffic):
-    """The JSON roofline object of the expert FFN (two grouped-GEMM launches of
-    flops and ffn_bytes in total, ffn_ms per call). The bound is the larger of
-    the two floors: the algorithmic bytes at the measured HBM rate, or the
-    FLOPs at the measured bf16 rate. An FFN of a millisecond or more per call,
-    timed back to back, runs under the power cap, so its bf16 rate is the
-    sustained one, else the burst one."""
+def ffn_kernels(wl, R_max):
+    """(launches, kernel names) of one expert-FFN call, chosen as the library
+    chooses them from the layer's shape (R_max = the expert-sorted rows' bound,
+    moe_capacity): bf16 experts of at least 1024 rows on average run on CTA
+    pairs; 256 or more (T > 128) as two launches per projection; the rest as
+    one single-CTA launch per projection."""
+    c = wl.cfg
+    T, E, k = c.T, c.n_experts, c.top_k
+    if c.dtype != 1:
+        return 2, "grouped_gemm_simt_kernel (expert FFN: up + down launches)"
+    if R_max >= 1024 * E:
+        return 2, "grouped_gemm_pair_kernel (CTA pairs; expert FFN: up + down launches)"
+    if T > 128 and T * k >= 256 * E:
+        return 4, ("grouped_gemm_tc_kernel + grouped_gemm_pair_kernel (few-row experts on "
+                   "single CTAs, then many-row and shared experts on CTA pairs; expert FFN: "
+                   "2 launches per projection)")
+    return 2, "grouped_gemm_tc_kernel (expert FFN: up + down launches)"
+
+
+def roofline_record(flops, ffn_bytes, ffn_ms, pk, pk_kind, traffic, launches=2,
+                    kernel="grouped_gemm_tc_kernel (expert FFN: up + down launches)"):
+    """The JSON roofline object of the expert FFN (`launches` grouped-GEMM
+    launches of flops and ffn_bytes in total, ffn_ms per call). The bound is
+    the larger of the two floors: the algorithmic bytes at the measured HBM
+    rate, or the FLOPs at the measured bf16 rate. An FFN of a millisecond or
+    more per call, timed back to back, runs under the power cap, so its bf16
+    rate is the sustained one, else the burst one."""
     hbm = pk["hbm_gbs"]
     achieved_gbs = ffn_bytes / (ffn_ms / 1e3) / 1e9
     tflops = flops / (ffn_ms / 1e3) / 1e12
-    kernel = "grouped_gemm_tc_kernel (expert FFN: up + down launches)"
     sustained = ffn_ms >= 1.0
     peak_t = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
     if ffn_bytes / (hbm * 1e9) >= flops / (peak_t * 1e12):
         return {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": achieved_gbs / hbm, "traffic": traffic, "kernel": kernel,
-                "algorithmic_bytes_per_launch": ffn_bytes / 2, "peak_kind": pk_kind,
+                "algorithmic_bytes_per_launch": ffn_bytes / launches, "peak_kind": pk_kind,
                 "tflops": tflops, "tflops_frac_of_bf16_peak": tflops / pk["bf16_tflops"]}
     return {"bound": "tensor", "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
             "frac": tflops / peak_t, "traffic": traffic, "kernel": kernel,
-            "algorithmic_flops_per_launch": flops / 2,
+            "algorithmic_flops_per_launch": flops / launches,
             "peak_kind": pk_kind + (" sustained" if sustained else " burst"),
             "hbm_gbs": achieved_gbs, "hbm_frac": achieved_gbs / hbm}
 
@@ -397,9 +416,9 @@ def launches_per_step(wl):
         return route_launches + 2 + 2 + 1
     cap_launches = 1 if policy else (1 if (T + 255) // 256 <= 256 else 2)
     # expert projections: one launch each, or two for layers of mixed expert
-    # sizes (256 <= T k / E < 1024 rows per expert, bf16, T > 128)
-    split = c.dtype == 1 and T > 128 and 256 * c.n_experts <= T * k < 1024 * c.n_experts
-    gemm_launches = 4 if split else 2
+    # sizes (ffn_kernels)
+    from sparse_mixture_experts_69_b300 import moe
+    gemm_launches = ffn_kernels(wl, moe.moe_capacity(c)[1])[0]
     return (route_launches + cap_launches + 1 + gemm_launches + (0 if combine_in_gemm else 1)
             + (1 if wl.bias_rate else 0))
 
@@ -570,7 +589,9 @@ def measure(wl, steps, warmup, dev, pg, world, local, cpu_budget, want_cpu, auto
     flops = 2 * (R + S * T) * d * (F1 + F)
     ffn_ms = stage_ms["expert_ffn"]
     pk, pk_kind = peaks()
-    roofline = roofline_record(flops, ffn_bytes, ffn_ms, pk, pk_kind, ncu_traffic(wl.name))
+    n_launch, kname = ffn_kernels(wl, R_max)
+    roofline = roofline_record(flops, ffn_bytes, ffn_ms, pk, pk_kind, ncu_traffic(wl.name),
+                               n_launch, kname)
     # the memory-bound entry points: algorithmic bytes (inputs read once,
     # outputs written once) over their time
     noisy_b = (d * E * es + (T * E * 4 if inp["noise"] is not None else 0)) if wl.noisy else 0
