@@ -309,6 +309,11 @@ cudaError_t launch_capacity(const Shape& s, const int32_t* ids, int32_t* blk_his
 // ---------------------------------------------------------------- permute
 // One warp per token: read the row once (16-byte vectors), write it to each of
 // the token's kept rows. Algorithmic bytes: T d b read + R d b written.
+#ifndef MOE_PERMUTE_VPL
+#define MOE_PERMUTE_VPL 16
+#endif
+constexpr int kPermuteVpl = MOE_PERMUTE_VPL;  // 16-byte vectors a lane loads per pass
+
 __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec, int rows,
                                                       const uint4* __restrict__ x,
                                                       const int32_t* __restrict__ slot,
@@ -337,11 +342,12 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec, in
     }
     const uint4* src = x + (size_t)t * nvec;
     // the loop bound is warp-uniform so every shuffle has all lanes present;
-    // each lane loads up to 4 vectors before storing them
-    for (int v0 = 0; v0 < nvec; v0 += 128) {
-        uint4 val[4];
+    // each lane loads up to kPermuteVpl vectors before storing them
+    constexpr int kV = kPermuteVpl;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kV) {
+        uint4 val[kV];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kV; ++q) {
             const int v = v0 + 32 * q + lane;
             if (v < nvec) val[q] = __ldcs(src + v);
         }
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(256) permute_kernel(int T, int k, int nvec, in
             m &= m - 1;
             const int r = __shfl_sync(0xffffffffu, my_slot, j);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kV; ++q) {
                 const int v = v0 + 32 * q + lane;
                 if (v < nvec) xp[(size_t)r * nvec + v] = val[q];
             }

@@ -45,6 +45,10 @@ struct Vec<__nv_bfloat16> {
     }
 };
 
+#ifndef MOE_COMBINE_ROWS
+#define MOE_COMBINE_ROWS 1  // combine_rows_kernel for bf16 layers with k <= 8
+#endif
+
 // One warp per token. y[t] = sum_{kept j} w[t,j] yp[slot[t,j]] + sum_s ys[s,t],
 // fp32 accumulation in the fixed order j = 0..k-1, then s = 0..S-1. Each lane
 // covers up to VPL 16-byte vectors per pass and issues their loads together.
@@ -122,9 +126,104 @@ __global__ void __launch_bounds__(256, 4) combine_kernel(int T, int d, int k, in
     if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(status, DEV_NONFINITE);
 }
 
+// The same sums for k <= KMAX, with every kept row's loads of a pass issued
+// together before any is added (in the order j = 0..k-1, then the shared
+// experts, as above): a warp keeps k times as many bytes in flight.
+template <typename Tv, int VPL, int KMAX>
+__global__ void __launch_bounds__(256, 2) combine_rows_kernel(int T, int d, int k, int S,
+                                                             const Tv* __restrict__ yp,
+                                                             const int32_t* __restrict__ slot,
+                                                             const float* __restrict__ w,
+                                                             const Tv* __restrict__ ys,
+                                                             Tv* __restrict__ y, int* status) {
+    pdl_trigger();
+    constexpr int VN = Vec<Tv>::N;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    pdl_wait();
+    const int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
+    const float my_w = lane < k ? w[(size_t)t * k + lane] : 0.f;
+    unsigned m = __ballot_sync(0xffffffffu, my_slot >= 0);
+    const int nlive = __popc(m);
+    // the kept rows in order j = 0..k-1
+    const Tv* rows[KMAX];
+    float g[KMAX];
+#pragma unroll
+    for (int jj = 0; jj < KMAX; ++jj) {
+        const int j = m ? __ffs(m) - 1 : 0;
+        m &= m - 1;
+        const int r = __shfl_sync(0xffffffffu, my_slot, j);
+        g[jj] = __shfl_sync(0xffffffffu, my_w, j);
+        rows[jj] = yp + (size_t)(r < 0 ? 0 : r) * d;
+    }
+    const int nvec = d / VN;
+    bool bad = false;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * VPL) {
+        uint4 raw[KMAX][VPL];
+#pragma unroll
+        for (int jj = 0; jj < KMAX; ++jj)
+#pragma unroll
+            for (int q = 0; q < VPL; ++q) {
+                const int v = v0 + q * 32 + lane;
+                if (jj < nlive && v < nvec)
+                    raw[jj][q] = __ldg(reinterpret_cast<const uint4*>(rows[jj]) + v);
+            }
+        float acc[VPL][VN];
+#pragma unroll
+        for (int q = 0; q < VPL; ++q)
+#pragma unroll
+            for (int i = 0; i < VN; ++i) acc[q][i] = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < KMAX; ++jj)
+#pragma unroll
+            for (int q = 0; q < VPL; ++q)
+                if (jj < nlive && v0 + q * 32 + lane < nvec) {
+                    float val[VN];
+                    Vec<Tv>::load(&raw[jj][q], val);
+#pragma unroll
+                    for (int i = 0; i < VN; ++i) acc[q][i] = fmaf(g[jj], val[i], acc[q][i]);
+                }
+        for (int s = 0; s < S; ++s) {
+#pragma unroll
+            for (int q = 0; q < VPL; ++q) {
+                const int v = v0 + q * 32 + lane;
+                if (v < nvec) {
+                    float val[VN];
+                    const uint4 raw1 =
+                        __ldg(reinterpret_cast<const uint4*>(ys + ((size_t)s * T + t) * d) + v);
+                    Vec<Tv>::load(&raw1, val);
+#pragma unroll
+                    for (int i = 0; i < VN; ++i) acc[q][i] += val[i];
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) {
+            const int v = v0 + q * 32 + lane;
+            if (v < nvec) {
+#pragma unroll
+                for (int i = 0; i < VN; ++i) bad |= !isfinite(acc[q][i]);
+                Vec<Tv>::store(y + (size_t)t * d + (size_t)v * VN, acc[q]);
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(status, DEV_NONFINITE);
+}
+
 cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, const float* w,
                            const void* ys, void* y, int* status, cudaStream_t st) {
     dim3 grid((s.T + 7) / 8), block(256);
+#if MOE_COMBINE_ROWS
+    if (s.dtype == MOE_BF16 && s.nc <= 2)
+        return launch_k(combine_rows_kernel<__nv_bfloat16, 2, 2>, grid, block, 0, st, s.T, s.d,
+                        s.nc, ys ? s.S : 0, (const __nv_bfloat16*)yp, slot, w,
+                        (const __nv_bfloat16*)ys, (__nv_bfloat16*)y, status);
+    if (s.dtype == MOE_BF16 && s.nc <= 8)
+        return launch_k(combine_rows_kernel<__nv_bfloat16, 2, 8>, grid, block, 0, st, s.T, s.d,
+                        s.nc, ys ? s.S : 0, (const __nv_bfloat16*)yp, slot, w,
+                        (const __nv_bfloat16*)ys, (__nv_bfloat16*)y, status);
+#endif
     if (s.dtype == MOE_BF16)
         return launch_k(combine_kernel<__nv_bfloat16, 2>, grid, block, 0, st, s.T, s.d, s.nc,
                         ys ? s.S : 0, (const __nv_bfloat16*)yp, slot, w, (const __nv_bfloat16*)ys,
