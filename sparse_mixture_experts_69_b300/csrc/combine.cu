@@ -128,9 +128,12 @@ __global__ void __launch_bounds__(256, 4) combine_kernel(int T, int d, int k, in
 
 // The same sums for k <= KMAX, with every kept row's loads of a pass issued
 // together before any is added (in the order j = 0..k-1, then the shared
-// experts, as above): a warp keeps k times as many bytes in flight.
+// experts, as above): a warp keeps k times as many bytes in flight. A warp
+// takes `npass` consecutive passes of one token (32 VPL vectors each); small
+// token counts give each pass its own warp.
 template <typename Tv, int VPL, int KMAX>
 __global__ void __launch_bounds__(256, 2) combine_rows_kernel(int T, int d, int k, int S,
+                                                             int npass,
                                                              const Tv* __restrict__ yp,
                                                              const int32_t* __restrict__ slot,
                                                              const float* __restrict__ w,
@@ -139,8 +142,13 @@ __global__ void __launch_bounds__(256, 2) combine_rows_kernel(int T, int d, int 
     pdl_trigger();
     constexpr int VN = Vec<Tv>::N;
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int nvec = d / VN;
+    const int per_tok = (nvec + 32 * VPL * npass - 1) / (32 * VPL * npass);  // warps a token
+    const long long wi = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int t = (int)(wi / per_tok);
     if (t >= T) return;
+    const int v_begin = (int)(wi - (long long)t * per_tok) * 32 * VPL * npass;
+    const int v_end = min(nvec, v_begin + 32 * VPL * npass);
     pdl_wait();
     const int my_slot = lane < k ? slot[(size_t)t * k + lane] : -1;
     const float my_w = lane < k ? w[(size_t)t * k + lane] : 0.f;
@@ -157,16 +165,15 @@ __global__ void __launch_bounds__(256, 2) combine_rows_kernel(int T, int d, int 
         g[jj] = __shfl_sync(0xffffffffu, my_w, j);
         rows[jj] = yp + (size_t)(r < 0 ? 0 : r) * d;
     }
-    const int nvec = d / VN;
     bool bad = false;
-    for (int v0 = 0; v0 < nvec; v0 += 32 * VPL) {
+    for (int v0 = v_begin; v0 < v_end; v0 += 32 * VPL) {
         uint4 raw[KMAX][VPL];
 #pragma unroll
         for (int jj = 0; jj < KMAX; ++jj)
 #pragma unroll
             for (int q = 0; q < VPL; ++q) {
                 const int v = v0 + q * 32 + lane;
-                if (jj < nlive && v < nvec)
+                if (jj < nlive && v < v_end)
                     raw[jj][q] = __ldg(reinterpret_cast<const uint4*>(rows[jj]) + v);
             }
         float acc[VPL][VN];
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(256, 2) combine_rows_kernel(int T, int d, int 
         for (int jj = 0; jj < KMAX; ++jj)
 #pragma unroll
             for (int q = 0; q < VPL; ++q)
-                if (jj < nlive && v0 + q * 32 + lane < nvec) {
+                if (jj < nlive && v0 + q * 32 + lane < v_end) {
                     float val[VN];
                     Vec<Tv>::load(&raw[jj][q], val);
 #pragma unroll
@@ -188,7 +195,7 @@ __global__ void __launch_bounds__(256, 2) combine_rows_kernel(int T, int d, int 
 #pragma unroll
             for (int q = 0; q < VPL; ++q) {
                 const int v = v0 + q * 32 + lane;
-                if (v < nvec) {
+                if (v < v_end) {
                     float val[VN];
                     const uint4 raw1 =
                         __ldg(reinterpret_cast<const uint4*>(ys + ((size_t)s * T + t) * d) + v);
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(256, 2) combine_rows_kernel(int T, int d, int 
 #pragma unroll
         for (int q = 0; q < VPL; ++q) {
             const int v = v0 + q * 32 + lane;
-            if (v < nvec) {
+            if (v < v_end) {
 #pragma unroll
                 for (int i = 0; i < VN; ++i) bad |= !isfinite(acc[q][i]);
                 Vec<Tv>::store(y + (size_t)t * d + (size_t)v * VN, acc[q]);
@@ -215,14 +222,21 @@ cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, 
                            const void* ys, void* y, int* status, cudaStream_t st) {
     dim3 grid((s.T + 7) / 8), block(256);
 #if MOE_COMBINE_ROWS
-    if (s.dtype == MOE_BF16 && s.nc <= 2)
-        return launch_k(combine_rows_kernel<__nv_bfloat16, 2, 2>, grid, block, 0, st, s.T, s.d,
-                        s.nc, ys ? s.S : 0, (const __nv_bfloat16*)yp, slot, w,
+    if (s.dtype == MOE_BF16 && s.nc <= 8) {
+        // passes of a token per warp: all of them, unless the tokens are too
+        // few to fill the GPU with warps (decode), then one
+        const int passes = (s.d / 8 + 63) / 64;
+        const int npass = (long long)s.T * 4 < (long long)num_sms() * 16 ? 1 : passes;
+        const int per_tok = (passes + npass - 1) / npass;
+        const dim3 g((unsigned)(((long long)s.T * per_tok + 7) / 8));
+        if (s.nc <= 2)
+            return launch_k(combine_rows_kernel<__nv_bfloat16, 2, 2>, g, block, 0, st, s.T, s.d,
+                            s.nc, ys ? s.S : 0, npass, (const __nv_bfloat16*)yp, slot, w,
+                            (const __nv_bfloat16*)ys, (__nv_bfloat16*)y, status);
+        return launch_k(combine_rows_kernel<__nv_bfloat16, 2, 8>, g, block, 0, st, s.T, s.d,
+                        s.nc, ys ? s.S : 0, npass, (const __nv_bfloat16*)yp, slot, w,
                         (const __nv_bfloat16*)ys, (__nv_bfloat16*)y, status);
-    if (s.dtype == MOE_BF16 && s.nc <= 8)
-        return launch_k(combine_rows_kernel<__nv_bfloat16, 2, 8>, grid, block, 0, st, s.T, s.d,
-                        s.nc, ys ? s.S : 0, (const __nv_bfloat16*)yp, slot, w,
-                        (const __nv_bfloat16*)ys, (__nv_bfloat16*)y, status);
+    }
 #endif
     if (s.dtype == MOE_BF16)
         return launch_k(combine_kernel<__nv_bfloat16, 2>, grid, block, 0, st, s.T, s.d, s.nc,
