@@ -1064,6 +1064,13 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
 // aborting odd CTA cannot see its own copies complete (they count on the
 // other CTA's barrier), so it waits 200 us, far longer than a copy takes,
 // before that barrier.
+//
+// Tile order. With GroupedGemm::tile_ctr the pairs take their tiles in order
+// from a launch-wide counter, so the tiles in flight stay a window of
+// consecutive tiles (sharing weight panels and token blocks through L2);
+// pairs that each took every nclusters-th tile drifted apart over a launch
+// and tripled the DRAM reads of the Mixtral-shaped GEMMs.
+
 // Work-item ring of the pair kernel's dynamic tile order: slots, and the
 // consumers of each item (the even CTA's MMA issuer, 4 epilogue warps in each
 // CTA, the odd CTA's producer).
@@ -1079,6 +1086,7 @@ __device__ __forceinline__ void release_tile_counter(int* tile_ctr, int ncluster
         atomicExch(tile_ctr + 1, 0);
     }
 }
+
 struct PairCfg {
     static constexpr int BN = 256;
     static constexpr int A_BYTES = BM * BKH * 2;    // own 128 rows x 64
