@@ -73,6 +73,10 @@ struct TcArgs {
     // the selection kernel adds the parts in order s = 0, 1, ...
     int ksplit;
     float* part;
+    // router: rows of a tile (at most BM; 0: BM). A memory-bound router whose
+    // T / BM tiles would leave SMs idle takes shorter tiles, one per SM: the
+    // MMAs still run 128 rows, the copies and stores cover router_tm
+    int router_tm;
     unsigned long long wait_ns;  // limit of each pipeline mbarrier wait
     // 1: the MMA warp withholds the "accumulator ready" signal of its CTA's
     // first tile, so the epilogue's first wait can only end by running out
@@ -623,6 +627,9 @@ __device__ __forceinline__ uint32_t stage_bytes(int rows) {
 #ifndef MOE_ROUTER_PAIR
 #define MOE_ROUTER_PAIR 1  // 256-wide router GEMMs on CTA pairs
 #endif
+#ifndef MOE_ROUTER_SHORT_TILES
+#define MOE_ROUTER_SHORT_TILES 1  // memory-bound routers: one tile per SM
+#endif
 
 // The K block loaded at step j of a work item whose K range is [lo, hi). The
 // router's CTAs all start together, one tile each, and would otherwise read
@@ -675,6 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
     const int nt = (p.N + ncol_tile - 1) / ncol_tile;
     const int nkb = (p.K + BK - 1) / BK;
+    // rows of a tile: BM, or the router's shorter tiles
+    const int TM = EPI == EPI_ROUTER && args.router_tm > 0 ? args.router_tm : BM;
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA0);
@@ -690,9 +699,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool early = p.early != 0;
     if (!early) pdl_wait();
     if (early)
-        build_tile_table<true>(p, BM, mt_start, grows);
+        build_tile_table<true>(p, TM, mt_start, grows);
     else
-        build_tile_table<false>(p, BM, mt_start, grows);
+        build_tile_table<false>(p, TM, mt_start, grows);
     __syncthreads();
     // work items: output tiles, times the K parts of a split router GEMM
     const int ks = EPI == EPI_ROUTER ? args.ksplit : 1;
@@ -726,12 +735,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (early && threadIdx.x == 0) {
         for (int w = blockIdx.x; w < total && prefilled < C::STAGES; w += gridDim.x) {
             const int tile = w / ks, sp = w - tile * ks;
-            const GroupTile gt = decode_tile<true>(p, mt_start, nt, BM, tile);
+            const GroupTile gt = decode_tile<true>(p, mt_start, nt, TM, tile);
             const CUtensorMap* mb = gt.g < p.E ? &tmB0 : &tmB1;
             int brow[C::B_LOADS];
             b_tile_rows<BN, EPI>(p, gt, brow);
             const int kb_lo = sp * nkb / ks, kb_hi = (sp + 1) * nkb / ks;
-            const uint32_t bytes = stage_bytes<BN, EPI>(gt.rows);
+            const uint32_t bytes = EPI == EPI_ROUTER
+                                       ? (uint32_t)(TM * BK * 2 + C::B_BYTES)
+                                       : stage_bytes<BN, EPI>(gt.rows);
             for (int kb = kb_lo; kb < kb_hi && prefilled < C::STAGES; ++kb) {
                 mbar_arrive_expect_tx(&full[prefilled], bytes);
                 load_b_stage<BN, WEF>(sB + prefilled * C::B_BYTES, mb, &full[prefilled],
@@ -763,14 +774,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int item = 0;  // (tile, k block) pairs issued so far
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
                 const int tile = w / ks, sp = w - tile * ks;
-                const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
+                const GroupTile gt = decode_tile(p, mt_start, nt, TM, tile);
                 const bool routed = gt.g < p.E;
                 // tiles of at most 64 rows (M=64 MMAs) load 64-row A boxes
                 const bool short_a = EPI != EPI_ROUTER && gt.rows <= 64;
                 const CUtensorMap* ma = short_a ? (routed ? &tmA0s : &tmA1s)
                                                 : (routed ? &tmA0 : &tmA1);
                 const CUtensorMap* mb = routed ? &tmB0 : &tmB1;
-                const uint32_t bytes = stage_bytes<BN, EPI>(gt.rows);
+                const uint32_t bytes = EPI == EPI_ROUTER
+                                           ? (uint32_t)(TM * BK * 2 + C::B_BYTES)
+                                           : stage_bytes<BN, EPI>(gt.rows);
                 int brow[C::B_LOADS];
                 b_tile_rows<BN, EPI>(p, gt, brow);
                 const int kb_lo = sp * nkb / ks, kb_hi = (sp + 1) * nkb / ks;
@@ -876,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int local = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x, ++local) {
             const int tile = w / ks, sp = w - tile * ks;
-            const GroupTile gt = decode_tile(p, mt_start, nt, BM, tile);
+            const GroupTile gt = decode_tile(p, mt_start, nt, TM, tile);
             const int b = local & 1;
             const uint32_t tph = (local >> 1) & 1;
             if (!mbar_wait(&tfull[b], tph, abort_flag, p.status, args.wait_ns)) break;
@@ -892,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // thread = row; stage 32 rows x 32 columns, then each warp writes
                 // whole 128-byte row segments (lane = column)
                 float* stg = staging + q * 32 * 33;
-                const int rows_here = min(32, gt.rows - 32 * q);
+                const int rows_here = min(32, min(gt.rows, TM) - 32 * q);
                 const int E_r = args.E_router;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
@@ -1015,10 +1028,12 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     const GroupedGemm& p = a.p;
     CUtensorMap mA0, mA1, mA0s, mA1s, mB0, mB1;
     const int G = p.E + p.S;
-    // A maps with 128-row boxes, and with 64-row boxes for tiles of <= 64 rows
-    for (int box : {BM, 64}) {
-        CUtensorMap* m0 = box == BM ? &mA0 : &mA0s;
-        CUtensorMap* m1 = box == BM ? &mA1 : &mA1s;
+    const int tm = EPI == EPI_ROUTER && a.router_tm > 0 ? a.router_tm : BM;  // rows of a tile
+    // A maps with tile-high boxes, and with 64-row boxes for tiles of <= 64 rows
+    for (int i = 0; i < 2; ++i) {
+        const int box = i == 0 ? tm : 64;
+        CUtensorMap* m0 = i == 0 ? &mA0 : &mA0s;
+        CUtensorMap* m1 = i == 0 ? &mA1 : &mA1s;
         if (!make_map(m0, p.A0 ? p.A0 : p.A1, p.A0 ? p.rows_a0 : p.rows_a1, p.K, box) ||
             !make_map(m1, p.A1 ? p.A1 : p.A0, p.A1 ? p.rows_a1 : p.rows_a0, p.K, box))
             return cudaErrorInvalidValue;
@@ -1034,8 +1049,8 @@ static cudaError_t launch(const TcArgs& a, cudaStream_t st) {
     // upper bound of the tile count, from host-known sizes
     const int ncol_tile = EPI == EPI_GLU ? 128 : BN;
     const long long nt = (p.N + ncol_tile - 1) / ncol_tile;
-    long long mt = (long long)p.max_rows0 / BM + p.E + (long long)p.S * ((p.T + BM - 1) / BM);
-    if (p.E == 0) mt = (long long)p.S * ((p.T + BM - 1) / BM);
+    long long mt = (long long)p.max_rows0 / tm + p.E + (long long)p.S * ((p.T + tm - 1) / tm);
+    if (p.E == 0) mt = (long long)p.S * ((p.T + tm - 1) / tm);
     const long long bound = std::max<long long>(1, mt * nt * (EPI == EPI_ROUTER ? a.ksplit : 1));
     const int grid = (int)std::min<long long>(bound, num_sms());
     return launch_k(grouped_gemm_tc_kernel<BN, EPI, WEF>, dim3(grid), dim3(kThreads), smem, st, mA0,
@@ -1607,19 +1622,31 @@ cudaError_t launch_grouped_gemm_tc(const Shape& s, const GroupedGemm& g, cudaStr
 // keeping at least 4 blocks of K) while the work items fit one wave. The plan
 // assumes a 148-SM part whatever the device, so the split, and with it every
 // rounding of the logits, is the same on any GPU.
-void router_plan(int T, int d, int Nr, int* bn, int* ksplit, int* pair) {
+void router_plan(int T, int d, int Nr, int* bn, int* ksplit, int* pair, int* tile_rows) {
     constexpr int kPlanSms = 148;
     const int b = Nr <= 32 ? 32 : Nr <= 64 ? 64 : Nr <= 128 ? 128 : 256;
     const int pr = MOE_ROUTER_PAIR && b == 256 ? 1 : 0;
-    const int tm = pr ? 2 * tc::BM : tc::BM;  // rows of a tile
-    const long long tiles = (long long)((T + tm - 1) / tm) * ((Nr + b - 1) / b);
-    const long long ctas = tiles * (pr ? 2 : 1);  // CTAs per K part
     const int nkb = (d + tc::BK - 1) / tc::BK;
+    const long long ncol = (Nr + b - 1) / b;
+    // a memory-bound router (at most 128 columns) that would leave SMs idle
+    // with 128-row tiles and no split takes tiles of ceil(T / 148) rows
+    // (at least 64), one per SM
+    int tm = pr ? 2 * tc::BM : tc::BM;  // rows of a tile
+    if (MOE_ROUTER_SHORT_TILES && !pr && ncol == 1) {
+        const long long t128 = (T + tc::BM - 1) / tc::BM;
+        if (t128 < kPlanSms && !(t128 * 2 <= kPlanSms && nkb / 2 >= 4)) {
+            const int want = (int)((T + kPlanSms - 1) / kPlanSms);
+            if (want >= 64 && want < tc::BM) tm = want;
+        }
+    }
+    const long long tiles = (long long)((T + tm - 1) / tm) * ncol;
+    const long long ctas = tiles * (pr ? 2 : 1);  // CTAs per K part
     int s = 1;
     while (ctas * s * 2 <= kPlanSms && nkb / (s * 2) >= 4) s *= 2;
     *bn = b;
     *ksplit = s;
     if (pair) *pair = pr;
+    if (tile_rows) *tile_rows = pr ? 0 : tm;
 }
 
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
@@ -1654,9 +1681,10 @@ cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const
     a.E_router = s.E;
     a.wait_ns = wait_limit_ns();
     a.hold_first_acc = hold_first_accumulator();
-    int bn, ks, pair;
-    router_plan(s.T, s.d, Nr, &bn, &ks, &pair);
+    int bn, ks, pair, tm;
+    router_plan(s.T, s.d, Nr, &bn, &ks, &pair, &tm);
     a.ksplit = ks;
+    a.router_tm = tm;
     a.part = ks > 1 ? part : nullptr;
     if (ks > 1 && !part) return cudaErrorInvalidValue;
     if (pair) return tc::launch_pair<tc::EPI_ROUTER>(a, st);

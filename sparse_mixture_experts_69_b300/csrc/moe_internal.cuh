@@ -102,11 +102,13 @@ cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const
                                    const float* Wnoise, const float* offset, float* logits,
                                    float* zn, cudaStream_t st);
 // Router GEMM for bf16 inputs (tcgen05). router_plan gives its column tile
-// width, K split and whether it runs on CTA pairs (pair may be NULL); with a
+// width, K split, whether it runs on CTA pairs and the rows of its tiles
+// (pair and tile_rows may be NULL); with a
 // split (ksplit > 1) the kernel writes the raw parts to part [ksplit][T][Nr]
 // and logits, zn and offset are left to the selection kernel, otherwise it
 // writes logits (+ offset) and zn itself.
-void router_plan(int T, int d, int Nr, int* bn, int* ksplit, int* pair = nullptr);
+void router_plan(int T, int d, int Nr, int* bn, int* ksplit, int* pair = nullptr,
+                 int* tile_rows = nullptr);
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
                                     const float* offset, float* logits, float* zn, float* part,
                                     int* status, cudaStream_t st);

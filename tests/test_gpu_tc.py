@@ -27,6 +27,9 @@ pytestmark = pytest.mark.gpu
     (1000, 7168, 256, 8, False, False, True),
     (300, 256, 200, 4, False, True, False),
     (500, 512, 128, 2, True, False, False),
+    # a memory-bound router of 79 full-height tiles runs one 68-row tile per
+    # SM instead (148 tiles, the last of 4 rows)
+    (10000, 512, 16, 2, False, True, False),
 ])
 def test_router_bf16(cuda_device, T, d, E, k, noisy, offset, bias):
     cfg = moe.Config(T=T, d_model=d, n_experts=E, top_k=k, d_ff=64, dtype=moe.MOE_BF16)
