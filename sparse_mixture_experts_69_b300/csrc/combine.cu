@@ -46,7 +46,7 @@ struct Vec<__nv_bfloat16> {
 };
 
 #ifndef MOE_COMBINE_ROWS
-#define MOE_COMBINE_ROWS 1  // combine_rows_kernel for bf16 layers with k <= 8
+#define MOE_COMBINE_ROWS 1  // combine_rows_kernel for bf16 layers with 2 < k <= 8
 #endif
 
 // One warp per token. y[t] = sum_{kept j} w[t,j] yp[slot[t,j]] + sum_s ys[s,t],
@@ -222,17 +222,16 @@ cudaError_t launch_combine(const Shape& s, const void* yp, const int32_t* slot, 
                            const void* ys, void* y, int* status, cudaStream_t st) {
     dim3 grid((s.T + 7) / 8), block(256);
 #if MOE_COMBINE_ROWS
-    if (s.dtype == MOE_BF16 && s.nc <= 8) {
+    // k <= 2 keeps the one-row-at-a-time kernel: its 64 registers give twice
+    // the resident warps, and with two rows that wins (Mixtral-shaped combine
+    // 82 us against 89 us, Switch-shaped 6.4 against 8.5 us, in the layer bench)
+    if (s.dtype == MOE_BF16 && s.nc > 2 && s.nc <= 8) {
         // passes of a token per warp: all of them, unless the tokens are too
         // few to fill the GPU with warps (decode), then one
         const int passes = (s.d / 8 + 63) / 64;
         const int npass = (long long)s.T * 4 < (long long)num_sms() * 16 ? 1 : passes;
         const int per_tok = (passes + npass - 1) / npass;
         const dim3 g((unsigned)(((long long)s.T * per_tok + 7) / 8));
-        if (s.nc <= 2)
-            return launch_k(combine_rows_kernel<__nv_bfloat16, 2, 2>, g, block, 0, st, s.T, s.d,
-                            s.nc, ys ? s.S : 0, npass, (const __nv_bfloat16*)yp, slot, w,
-                            (const __nv_bfloat16*)ys, (__nv_bfloat16*)y, status);
         return launch_k(combine_rows_kernel<__nv_bfloat16, 2, 8>, g, block, 0, st, s.T, s.d,
                         s.nc, ys ? s.S : 0, npass, (const __nv_bfloat16*)yp, slot, w,
                         (const __nv_bfloat16*)ys, (__nv_bfloat16*)y, status);
