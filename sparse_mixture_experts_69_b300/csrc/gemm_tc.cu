@@ -1260,10 +1260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Work items of the pair, in order i = 0, 1, ...: item 0 is tile `cluster`;
     // after it, every nclusters-th tile (static order), or (dynamic order) the
     // next tile of the launch-wide counter, which the even CTA's producer
-    // takes one item ahead and hands to the 10 consumers (its MMA issuer, both
-    // CTAs' 4 epilogue warps, the odd CTA's producer) through the ring, the
-    // odd CTA's copy by a remote store released with the remote arrive.
-    // Values >= total end the sequence.
+    // takes two items ahead and hands to the 10 consumers (its MMA issuer,
+    // both CTAs' 4 epilogue warps, the odd CTA's producer) one item ahead
+    // through the ring, the odd CTA's copy by a remote store released with the
+    // remote arrive. Values >= total end the sequence.
     auto item_put = [&](int i, int v) -> bool {
         const int s = i % kItemRing;
         const uint32_t ph = (uint32_t)(i / kItemRing) & 1u;
@@ -1299,16 +1299,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t filled = 0, fill_parity = 0;
             bool ok = true;
             int item = 0;
-            int w_next = 0;
+            // dynamic order, even CTA: item it+1 is handed out before item it
+            // is loaded (so the odd CTA's producer never waits for it at a
+            // tile boundary), and its tile comes from a counter read one item
+            // earlier still (so the atomic's latency is hidden)
+            int w_cur = cluster, w_nxt = 0;
+            if (dyn && leader) {
+                ok = item_put(0, w_cur < total ? w_cur : total);
+                w_nxt = nclusters + atomicAdd(p.tile_ctr, 1);
+            }
             for (int it = 0; ok; ++it) {
                 int w = cluster + it * nclusters;
                 if (dyn && leader) {
-                    w = it == 0 ? cluster : w_next;
-                    if (w < total) w_next = nclusters + atomicAdd(p.tile_ctr, 1);  // one ahead
-                    if (!item_put(it, w < total ? w : total)) {
+                    w = w_cur;
+                    if (w >= total) break;  // the end mark went out as item it
+                    const int w_after = nclusters + atomicAdd(p.tile_ctr, 1);  // item it+2
+                    if (!item_put(it + 1, w_nxt < total ? w_nxt : total)) {
                         ok = false;
                         break;
                     }
+                    w_cur = w_nxt;
+                    w_nxt = w_after;
                 } else if (dyn) {
                     w = item_get(it);
                     if (w < 0) {
