@@ -395,9 +395,31 @@ def run_reference(a):
 ALL_CONFIGS = ["tiny", "switch", "mixtral", "deepseek", "decode"]
 
 
+def router_selects_in_gemm(c, noisy):
+    """The library's rule for selecting in the router GEMM's epilogue (no
+    selection launch): bf16, no noise, at most 32 experts and 8 candidates,
+    and a router plan of one K part (the library's router_plan for 32-wide
+    column tiles: 128-row tiles, or one tile of ceil(T / 148) >= 64 rows per
+    SM when 128-row tiles would leave SMs idle and no split applies; then
+    the K range splits while 2x the tiles fit 148 SMs and each part keeps 4
+    blocks of 64)."""
+    if c.dtype != 1 or noisy or c.n_experts > 32 or c.n_cand > 8:
+        return False
+    T, nkb = c.T, (c.d_model + 63) // 64
+    tm = 128
+    t128 = (T + 127) // 128
+    if t128 < 148 and not (t128 * 2 <= 148 and nkb // 2 >= 4):
+        want = (T + 147) // 148
+        if 64 <= want < 128:
+            tm = want
+    tiles = (T + tm - 1) // tm
+    return not (tiles * 2 <= 148 and nkb // 2 >= 4)
+
+
 def launches_per_step(wl):
     """Kernels of this library one step launches. Layer path: [Wg transpose
-    (bf16)], router GEMM, fused selection + histogram + statistics, capacity
+    (bf16)], router GEMM, fused selection + histogram + statistics (none when
+    the router GEMM selects itself), capacity
     scan + slots (one launch up to 256 token blocks), permute, up GEMM, down
     GEMM (each two launches for layers of mixed expert sizes), [combine: skipped where the down GEMM writes y itself, by its
     folded combine (bf16, packed rows, combine_mode = 1) or, for top-1
@@ -411,7 +433,7 @@ def launches_per_step(wl):
     combine_in_gemm = c.dtype == 1 and not c.pad_to_capacity and (
         scatter or c.combine_mode == 1)
     policy = nc > k or c.priority != 0
-    route_launches = (1 if c.dtype == 1 else 0) + 2
+    route_launches = (1 if c.dtype == 1 else 0) + (1 if router_selects_in_gemm(c, wl.noisy) else 2)
     if ec:
         return route_launches + 2 + 2 + 1
     cap_launches = 1 if policy else (1 if (T + 255) // 256 <= 256 else 2)

@@ -24,6 +24,7 @@
 // DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits. The
 // limit is 2 s unless moe_set_wait_limits changed it.
 #include <algorithm>
+#include <cfloat>
 #include <mutex>
 
 #include "aux_common.cuh"
@@ -41,6 +42,9 @@
 #endif
 #ifndef MOE_TC_SMEM
 #define MOE_TC_SMEM (192 * 1024)  // shared memory for the pipeline stages
+#endif
+#ifndef MOE_TC_MAX_STAGES
+#define MOE_TC_MAX_STAGES 8
 #endif
 #ifndef MOE_TC_L2_HINTS
 #define MOE_TC_L2_HINTS 1  // L2 eviction policies (b_evict_first, out_l2_keep)
@@ -62,6 +66,28 @@ constexpr unsigned long long kDrainNs = 250000000ull;
 
 enum Epi : int { EPI_ACT = 0, EPI_GLU = 1, EPI_ROUTER = 2 };
 
+// Selection in the router GEMM's epilogue: with one K part and at most 32
+// router columns (no noise), each epilogue thread holds one token's whole row
+// of logits and does that token's softmax, top-nc and gates itself, in place
+// of the one-warp-per-token selection kernel. Same outputs as that kernel; the
+// layer path also counts the capacity histogram and the statistics sums.
+struct RouterSel {
+    int on;
+    int k, nc, renorm;
+    const float* bias;  // [E] or NULL: selection scores p + bias
+    float* probs;       // [T,E]
+    float* sel;         // [T,E] or NULL
+    int32_t* ids;       // [T,nc]
+    float* w;           // [T,nc]
+    int32_t* blk_hist;  // [E][nblk_cap] or NULL
+    int nblk_cap;
+    void* acc_mem;      // statistics accumulators (aux_common.cuh) or NULL
+    // 1: no early pdl_trigger, so the next kernel launches only when this one
+    // is complete (no selection kernel follows to order the next router
+    // weight copy after this GEMM's reads)
+    int late_trigger;
+};
+
 struct TcArgs {
     GroupedGemm p;
     const float* offset;  // router: [E] or NULL
@@ -77,6 +103,7 @@ struct TcArgs {
     // T / BM tiles would leave SMs idle takes shorter tiles, one per SM: the
     // MMAs still run 128 rows, the copies and stores cover router_tm
     int router_tm;
+    RouterSel rs;
     unsigned long long wait_ns;  // limit of each pipeline mbarrier wait
     // 1: the MMA warp withholds the "accumulator ready" signal of its CTA's
     // first tile, so the epilogue's first wait can only end by running out
@@ -92,7 +119,7 @@ struct Cfg {
     static constexpr int B_BYTES = B_HALF * KH;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES_FIT = MOE_TC_SMEM / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int STAGES = STAGES_FIT > MOE_TC_MAX_STAGES ? MOE_TC_MAX_STAGES : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // power of two for BN in {32..256}
     static constexpr int B_BOX_ROWS = BN < 128 ? BN : 128;
     static constexpr int B_LOADS = BN / B_BOX_ROWS;
@@ -627,6 +654,9 @@ __device__ __forceinline__ uint32_t stage_bytes(int rows) {
 #ifndef MOE_ROUTER_PAIR
 #define MOE_ROUTER_PAIR 1  // 256-wide router GEMMs on CTA pairs
 #endif
+#ifndef MOE_ROUTER_SEL_IN_GEMM
+#define MOE_ROUTER_SEL_IN_GEMM 1  // selection in the epilogue of narrow unsplit routers
+#endif
 #ifndef MOE_ROUTER_SHORT_TILES
 #define MOE_ROUTER_SHORT_TILES 1  // memory-bound routers: one tile per SM
 #endif
@@ -647,6 +677,128 @@ __device__ __forceinline__ int k_block(int j, int lo, int hi, int tile) {
         return lo + x;
     }
     return j;
+}
+
+// The selection of token t from its row of raw router sums v[0..E) (E <= 32),
+// as router_select_kernel does it for a token: logits z = v + offset, the
+// max-subtracted fp32 softmax, keys ordered by (score desc, index asc) with
+// score H (or p + bias), the first nc candidates, and gates p_j over the sum of
+// the first k candidates' p (renorm) or p_j. Only the summation order of the
+// softmax denominator and of the gates' sum differs (sequential here). With
+// aux statistics, each warp adds its tokens' probabilities (fp32, butterfly
+// order, then fixed point), gates (fixed point) and counts per expert into the
+// accumulators, and every choice into the capacity histogram.
+__device__ __forceinline__ unsigned sel_key(float v) {
+    const unsigned b = __float_as_uint(__fadd_rn(v, 0.f));
+    return b ^ ((b >> 31) ? 0xFFFFFFFFu : 0x80000000u);
+}
+__device__ __forceinline__ void router_select_rows(const RouterSel& rs, const float* offset,
+                                                   int E, int t, bool valid,
+                                                   const float (&v)[32], int* status) {
+    const int lane = threadIdx.x & 31;
+    float h[32], pr[32];
+    bool nonfinite = false;
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        h[i] = -FLT_MAX;
+        if (i < E) {
+            h[i] = v[i] + (offset ? offset[i] : 0.f);
+            if (!isfinite(h[i])) nonfinite = true;
+            m = fmaxf(m, h[i]);
+        }
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        pr[i] = i < E ? __expf(h[i] - m) : 0.f;
+        sum += pr[i];
+    }
+    const float inv = __frcp_rn(sum);
+    unsigned key[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        key[i] = 0u;
+        if (i < E) {
+            pr[i] = pr[i] * inv;
+            const float sc = rs.bias ? pr[i] + rs.bias[i] : h[i];
+            key[i] = sel_key(sc);
+            if (valid) {
+                rs.probs[(size_t)t * E + i] = pr[i];
+                if (rs.sel) rs.sel[(size_t)t * E + i] = sc;
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, valid && nonfinite) && lane == 0) flag_status(status, DEV_NONFINITE);
+    // top-nc by repeated arg-max; a strict > keeps the lower index among equal keys
+    unsigned taken = 0u;
+    int id[8];
+    float pj[8];
+    float psum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        id[j] = 0;
+        pj[j] = 0.f;
+        if (j < rs.nc) {
+            int be = -1;
+            unsigned bk = 0u;
+            float bp = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < E && !((taken >> i) & 1u) && (be < 0 || key[i] > bk)) {
+                    be = i;
+                    bk = key[i];
+                    bp = pr[i];
+                }
+            if (be >= 0) taken |= 1u << be;  // nc <= E: always
+            id[j] = be < 0 ? 0 : be;
+            pj[j] = bp;
+            if (j < rs.k) psum += bp;
+        }
+    }
+    const bool aux = rs.acc_mem != nullptr;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j < rs.nc) {
+            const float wj = rs.renorm ? pj[j] / psum : pj[j];
+            pj[j] = wj;
+            if (valid && rs.ids) {
+                rs.ids[(size_t)t * rs.nc + j] = id[j];
+                rs.w[(size_t)t * rs.nc + j] = wj;
+                if (j < rs.k && rs.blk_hist)
+                    atomicAdd(&rs.blk_hist[(size_t)id[j] * rs.nblk_cap + t / kCapBlockTokens], 1);
+            }
+        }
+    }
+    if (!aux) return;
+    const AuxAcc acc = aux_acc_at(rs.acc_mem, E, kAuxGroups);
+    const size_t g = (size_t)(blockIdx.x % acc.groups) * E;
+    for (int e = 0; e < E; ++e) {
+        float pe = 0.f;
+        unsigned long long ie = 0ull;
+        unsigned ce = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i == e) pe = valid ? pr[i] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (valid && j < rs.k && id[j] == e) {
+                ie += to_fix(pj[j]);
+                ++ce;
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            pe += __shfl_xor_sync(0xffffffffu, pe, o);
+            ie += __shfl_xor_sync(0xffffffffu, ie, o);
+        }
+        ce = __reduce_add_sync(0xffffffffu, ce);
+        if (lane == 0) {
+            const unsigned long long pf = to_fix(pe);
+            if (pf) atomicAdd(&acc.P[g + e], pf);
+            if (ie) atomicAdd(&acc.I[g + e], ie);
+            if (ce) atomicAdd(&acc.cnt[g + e], ce);
+        }
+    }
 }
 
 // WEF: weights evict-first in L2 (a separate instantiation: the hinted copy
@@ -673,6 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    static_assert((2 * C::STAGES + 5) * 8 + 8 <= 256, "barrier area");
     int* mt_start = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
     int* grows = mt_start + p.E + p.S + 1;  // [G] rows of each group
     float* staging = reinterpret_cast<float*>(
@@ -754,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (early) pdl_wait();
     // dependents may launch once every CTA is past the wait: a kernel that
     // follows this one can rely on the kernel before this one being complete
-    pdl_trigger();
+    if (!(EPI == EPI_ROUTER && args.rs.late_trigger)) pdl_trigger();
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
@@ -929,6 +1082,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     __syncwarp();
+                }
+                if constexpr (BN == 32) {
+                    if (args.rs.on) {
+                        float v[32];
+                        tmem_ld32(taddr, v);
+                        router_select_rows(args.rs, args.offset, E_r, gt.out_row + row,
+                                           row < rows_here + 32 * q, v, p.status);
+                    }
                 }
             } else {
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(routed ? p.out0 : p.out1);
@@ -1108,7 +1269,7 @@ struct PairCfg {
     static constexpr int B_BYTES = 128 * BKH * 2;   // own half of the weight tile
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES_FIT = MOE_TC_SMEM / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int STAGES = STAGES_FIT > MOE_TC_MAX_STAGES ? MOE_TC_MAX_STAGES : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN;        // two accumulators
     // M=256 (128 rows in each CTA), N=256, D=f32, A=B=bf16, both K-major
     static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -1660,9 +1821,17 @@ void router_plan(int T, int d, int Nr, int* bn, int* ksplit, int* pair, int* til
     if (tile_rows) *tile_rows = pr ? 0 : tm;
 }
 
+bool router_sel_in_gemm(const Shape& s, bool noisy) {
+    if (!MOE_ROUTER_SEL_IN_GEMM || s.dtype != MOE_BF16 || noisy || s.E > 32 || s.nc > 8)
+        return false;
+    int bn, ks, pair;
+    router_plan(s.T, s.d, s.E, &bn, &ks, &pair);
+    return bn == 32 && ks == 1 && !pair;
+}
+
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
                                     const float* offset, float* logits, float* zn, float* part,
-                                    int* status, cudaStream_t st) {
+                                    int* status, cudaStream_t st, const RouterSelOut* so) {
     tc::TcArgs a{};
     GroupedGemm& p = a.p;
     p.offsets = nullptr;
@@ -1696,6 +1865,22 @@ cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const
     router_plan(s.T, s.d, Nr, &bn, &ks, &pair, &tm);
     a.ksplit = ks;
     a.router_tm = tm;
+    if (so) {
+        if (!router_sel_in_gemm(s, zn != nullptr) || Nr != s.E) return cudaErrorInvalidValue;
+        a.rs.on = 1;
+        a.rs.k = s.k;
+        a.rs.nc = s.nc;
+        a.rs.renorm = s.renorm;
+        a.rs.bias = so->bias;
+        a.rs.probs = so->probs;
+        a.rs.sel = so->sel;
+        a.rs.ids = so->ids;
+        a.rs.w = so->w;
+        a.rs.blk_hist = so->blk_hist;
+        a.rs.nblk_cap = (s.T + kCapBlockTokens - 1) / kCapBlockTokens;
+        a.rs.acc_mem = so->acc_mem;
+        a.rs.late_trigger = so->late_trigger;
+    }
     a.part = ks > 1 ? part : nullptr;
     if (ks > 1 && !part) return cudaErrorInvalidValue;
     if (pair) return tc::launch_pair<tc::EPI_ROUTER>(a, st);

@@ -255,6 +255,18 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const void* x
             rl.nsplit = ks;
         }
         MOE_CUDA(launch_transpose_router_w(s, Wg, Wnoise, wgT, st));
+        if (router_sel_in_gemm(s, noisy)) {
+            // the GEMM's epilogue selects: no selection kernel
+            RouterSelOut so{bias, probs, sel, ids, w, nullptr, nullptr, 1};
+            if (aux_out3) {
+                so.blk_hist = uses_policy(s) ? nullptr : at<int32_t>(ws, L.blk_hist);
+                so.acc_mem = at<void>(ws, L.aux_acc);
+                so.late_trigger = 0;  // the capacity kernel follows (statistics: the up GEMM)
+            }
+            MOE_CUDA(launch_router_gemm_bf16(s, Nr, x, wgT, offset, logits, zn,
+                                             at<float>(ws, L.rpart), status, st, &so));
+            return MOE_OK;
+        }
         MOE_CUDA(launch_router_gemm_bf16(s, Nr, x, wgT, offset, logits, zn,
                                          at<float>(ws, L.rpart), status, st));
     } else {

@@ -109,9 +109,25 @@ cudaError_t launch_router_gemm_f32(const Shape& s, int Nr, const float* x, const
 // writes logits (+ offset) and zn itself.
 void router_plan(int T, int d, int Nr, int* bn, int* ksplit, int* pair = nullptr,
                  int* tile_rows = nullptr);
+// The selection's outputs when the router GEMM's epilogue selects
+// (router_sel_in_gemm: bf16, no noise, E <= 32, nc <= 8, one K part): as
+// launch_router_select writes them, plus, on the layer path, the capacity
+// histogram and the statistics sums of launch_router_select_fused.
+struct RouterSelOut {
+    const float* bias;  // [E] or NULL
+    float* probs;       // [T,E]
+    float* sel;         // [T,E] or NULL
+    int32_t* ids;       // [T,nc] or NULL (then w is NULL too)
+    float* w;           // [T,nc]
+    int32_t* blk_hist;  // capacity histogram or NULL
+    void* acc_mem;      // statistics accumulators or NULL
+    int late_trigger;   // 1 when no kernel of the call follows (moe_route)
+};
+bool router_sel_in_gemm(const Shape& s, bool noisy);
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
                                     const float* offset, float* logits, float* zn, float* part,
-                                    int* status, cudaStream_t st);
+                                    int* status, cudaStream_t st,
+                                    const RouterSelOut* so = nullptr);
 // The router's standard-normal draws for (s.noise_seed, s.noise_counter), [T,E]
 cudaError_t launch_draw_noise(const Shape& s, float* noise, cudaStream_t st);
 
@@ -296,7 +312,9 @@ int hold_first_accumulator();
 //  - the kernels those exceptions rely on call pdl_trigger() only after
 //    pdl_wait(): the selection kernels (the router GEMM before them is then
 //    complete), the permute and gather kernels (the capacity or selection
-//    kernel that wrote the offsets is then complete) and the tcgen05 GEMM.
+//    kernel that wrote the offsets is then complete) and the tcgen05 GEMM;
+//    a router GEMM that selects itself and ends moe_route does not trigger
+//    at all, so the next call's weight copy launches after it is complete.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

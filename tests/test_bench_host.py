@@ -30,8 +30,8 @@ def test_ffn_kernels_follow_the_layer_shape(name, launches, kernel):
 
 
 @pytest.mark.parametrize("name,per_step", [
-    # transpose, router GEMM, fused select, scan + slots, permute, up, down, combine
-    ("mixtral", 8),
+    # transpose, router GEMM (it selects too), scan + slots, permute, up, down, combine
+    ("mixtral", 7),
     # the same with two launches per projection, and the bias update
     ("deepseek", 11),
     # no combine launch: the top-1 down GEMM writes y
@@ -43,3 +43,16 @@ def test_ffn_kernels_follow_the_layer_shape(name, launches, kernel):
 ])
 def test_launches_per_step(name, per_step):
     assert bench.launches_per_step(WORKLOADS[name]) == per_step
+
+
+@pytest.mark.parametrize("T,d,E,noisy,fused", [
+    (16384, 4096, 8, False, True),    # Mixtral-shaped: 148 tiles of 111 rows
+    (2048, 256, 8, False, True),      # 4 K blocks: no split
+    (2048, 4096, 8, False, False),    # 16 tiles: K split in 4 parts
+    (10000, 512, 16, False, True),    # 148 tiles of 68 rows
+    (8192, 1024, 32, True, False),    # noisy
+    (64, 4096, 64, False, False),     # more than 32 experts
+])
+def test_router_selects_in_gemm(T, d, E, noisy, fused):
+    c = WORKLOADS["mixtral"].with_(T=T, d_model=d, n_experts=E).cfg
+    assert bench.router_selects_in_gemm(c, noisy) == fused

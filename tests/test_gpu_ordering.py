@@ -20,7 +20,7 @@ def _small(name):
     return WORKLOADS[name].with_(T=1024, d_model=256, d_ff=512)
 
 
-@pytest.mark.parametrize("name", ["switch", "deepseek", "decode"])
+@pytest.mark.parametrize("name", ["switch", "deepseek", "decode", "mixtral"])
 def test_inputs_written_just_before_the_call(cuda_device, name):
     """Wg, W1, W2 and x are overwritten by device kernels on the same stream
     immediately before moe_layer_fwd: the result must be the one for the new
@@ -84,7 +84,7 @@ def test_layer_in_a_cuda_graph(cuda_device, name):
         assert torch.equal(got, ref[key]), key
 
 
-@pytest.mark.parametrize("name", ["switch", "deepseek"])
+@pytest.mark.parametrize("name", ["switch", "deepseek", "mixtral"])
 def test_back_to_back_calls_with_different_router_weights(cuda_device, name):
     """Two layer calls, then two moe_route calls, queued back to back on one
     stream with one workspace and different router weights: the second

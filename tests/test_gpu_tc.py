@@ -8,7 +8,7 @@ import torch
 import oracle
 from sparse_mixture_experts_69_b300 import moe, synth
 
-from gpu_helpers import TOL_LOGITS, assert_rowwise, check_topk_valid, np32
+from gpu_helpers import TOL_GATE, TOL_LOGITS, assert_rowwise, check_topk_valid, np32
 from test_gpu_stages import run_ffn
 
 pytestmark = pytest.mark.gpu
@@ -58,6 +58,55 @@ def test_router_bf16(cuda_device, T, d, E, k, noisy, offset, bias):
     assert len(diff) <= max(1, T // 1000), diff
     same = [t for t in range(T) if t not in diff]
     assert_rowwise(np32(w)[same], r["w"][same], TOL_LOGITS, "gates")
+
+
+@pytest.mark.parametrize("T,d,E,k,reroute,bias,renorm,offset", [
+    (300, 64, 8, 2, 0, False, 1, False),
+    (257, 128, 32, 8, 0, True, 1, False),
+    (129, 64, 17, 3, 2, False, 0, False),
+    (5, 64, 1, 1, 0, False, 1, False),
+    (1000, 192, 2, 2, 0, True, 1, True),
+    (2000, 256, 8, 2, 6, False, 1, True),
+    # one short tile per SM (148 tiles of 68 rows, the last of 4)
+    (10000, 512, 16, 2, 0, False, 1, False),
+])
+def test_selection_in_router_gemm(cuda_device, T, d, E, k, reroute, bias, renorm, offset):
+    """Routers of at most 32 columns with one K part select in the GEMM's
+    epilogue, one token per thread. Small integer x and Wg make every logit
+    an exact integer (many ties, which the lower index must win): logits equal
+    the oracle's exactly, and on the GPU's own scores and probabilities the
+    ids of all n_cand candidates are bit-exact against the oracle's
+    selection, the gates within the division's rounding."""
+    cfg = moe.Config(T=T, d_model=d, n_experts=E, top_k=k, reroute=reroute, renorm_topk=renorm,
+                     d_ff=64, dtype=moe.MOE_BF16)
+    nc = k + reroute
+    dev = cuda_device
+    bf = torch.bfloat16
+    x = (synth.randint((T, d), 12, 101, 5) - 2).to(bf)
+    Wg = (synth.randint((d, E), 12, 102, 3) - 1).to(bf)
+    off = synth.zipf_logit_offset(E, 1.2) if offset else None
+    b = synth.uniform((E,), 12, 105, -0.1, 0.1) if bias else None
+    g = lambda t: None if t is None else t.to(dev)
+    logits = torch.empty((T, E), device=dev)
+    probs = torch.empty((T, E), device=dev)
+    sel = torch.empty((T, E), device=dev)
+    ids = torch.empty((T, nc), dtype=torch.int32, device=dev)
+    w = torch.empty((T, nc), device=dev)
+    ws = moe.workspace(cfg, dev)
+    moe.moe_route(cfg, g(x), g(Wg), None, None, g(off), g(b), logits, probs, sel, ids, w, 0, ws)
+    assert moe.moe_read_device_error(cfg, ws) == 0
+    r = oracle.router(x, Wg, k, offset=off, bias=b, renorm=bool(renorm))
+    if offset:
+        assert_rowwise(np32(logits), r["z"], TOL_LOGITS, "logits")
+    else:
+        np.testing.assert_array_equal(np32(logits), r["z"].astype(np.float32))
+    assert_rowwise(np32(probs), r["p"], TOL_LOGITS, "probs")
+    assert_rowwise(np32(sel), r["s"], TOL_LOGITS, "sel_scores")
+    ref_ids, ref_w = oracle.select_candidates(np32(sel), np32(probs), k, nc, renorm=bool(renorm))
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids)
+    # a gate is an fp32 quotient: relative rounding, except in the subnormal
+    # range (far-down candidates), where it is at most one step of 2**-149
+    np.testing.assert_allclose(np32(w), ref_w, rtol=TOL_GATE, atol=2.0**-149)
 
 
 @pytest.mark.parametrize("act", [moe.MOE_RELU, moe.MOE_GELU, moe.MOE_SWIGLU])
