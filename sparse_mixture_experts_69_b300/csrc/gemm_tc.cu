@@ -679,45 +679,60 @@ __device__ __forceinline__ int k_block(int j, int lo, int hi, int tile) {
     return j;
 }
 
-// The selection of token t from its row of raw router sums v[0..E) (E <= 32),
-// as router_select_kernel does it for a token: logits z = v + offset, the
-// max-subtracted fp32 softmax, keys ordered by (score desc, index asc) with
+// The selection of token t from its row of raw router sums v[0..E) (E <= EMAX
+// <= 32), as router_select_kernel does it for a token: logits z = v + offset,
+// the max-subtracted fp32 softmax, keys ordered by (score desc, index asc) with
 // score H (or p + bias), the first nc candidates, and gates p_j over the sum of
 // the first k candidates' p (renorm) or p_j. Only the summation order of the
-// softmax denominator and of the gates' sum differs (sequential here). With
-// aux statistics, each warp adds its tokens' probabilities (fp32, butterfly
-// order, then fixed point), gates (fixed point) and counts per expert into the
-// accumulators, and every choice into the capacity histogram.
+// softmax denominator and of the gates' sum differs (a pairwise tree and a
+// sequential sum here). With aux statistics, each warp adds its tokens'
+// probabilities (fp32, butterfly order, then fixed point), gates (fixed point)
+// and counts per expert into the accumulators, and every choice into the
+// capacity histogram. One warp per SM sub-partition runs this, so the chains
+// are kept short: EMAX = 8 sorts 64-bit keys (score key, complemented index)
+// with a register network and reduces all experts' statistics together.
 __device__ __forceinline__ unsigned sel_key(float v) {
     const unsigned b = __float_as_uint(__fadd_rn(v, 0.f));
     return b ^ ((b >> 31) ? 0xFFFFFFFFu : 0x80000000u);
 }
-__device__ __forceinline__ void router_select_rows(const RouterSel& rs, const float* offset,
+template <int EMAX>
+__device__ __forceinline__ void router_select_rows(const RouterSel rs, const float* offset,
                                                    int E, int t, bool valid,
-                                                   const float (&v)[32], int* status) {
+                                                   const float (&v)[32], float* stg,
+                                                   int* status) {
     const int lane = threadIdx.x & 31;
-    float h[32], pr[32];
+    float h[EMAX], pr[EMAX];
     bool nonfinite = false;
-    float m = -FLT_MAX;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < EMAX; ++i) {
         h[i] = -FLT_MAX;
         if (i < E) {
             h[i] = v[i] + (offset ? offset[i] : 0.f);
             if (!isfinite(h[i])) nonfinite = true;
-            m = fmaxf(m, h[i]);
         }
     }
-    float sum = 0.f;
+    // pairwise maximum and sum (log-depth chains)
+    float red[EMAX];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < EMAX; ++i) red[i] = h[i];
+#pragma unroll
+    for (int w = EMAX / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) red[i] = fmaxf(red[i], red[i + w]);
+    const float m = red[0];
+#pragma unroll
+    for (int i = 0; i < EMAX; ++i) {
         pr[i] = i < E ? __expf(h[i] - m) : 0.f;
-        sum += pr[i];
+        red[i] = pr[i];
     }
-    const float inv = __frcp_rn(sum);
-    unsigned key[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int w = EMAX / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) red[i] += red[i + w];
+    const float inv = __frcp_rn(red[0]);
+    unsigned key[EMAX];
+#pragma unroll
+    for (int i = 0; i < EMAX; ++i) {
         key[i] = 0u;
         if (i < E) {
             pr[i] = pr[i] * inv;
@@ -730,33 +745,52 @@ __device__ __forceinline__ void router_select_rows(const RouterSel& rs, const fl
         }
     }
     if (__any_sync(0xffffffffu, valid && nonfinite) && lane == 0) flag_status(status, DEV_NONFINITE);
-    // top-nc by repeated arg-max; a strict > keeps the lower index among equal keys
-    unsigned taken = 0u;
     int id[8];
     float pj[8];
-    float psum = 0.f;
+    if constexpr (EMAX == 8) {
+        // one sort of (score key, complemented index): keys are distinct and
+        // the unsigned order is (score desc, index asc); 0 marks no expert
+        unsigned long long k64[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        id[j] = 0;
-        pj[j] = 0.f;
-        if (j < rs.nc) {
-            int be = -1;
-            unsigned bk = 0u;
-            float bp = 0.f;
+        for (int i = 0; i < 8; ++i)
+            k64[i] = i < E ? ((unsigned long long)key[i] << 32) | (unsigned)~i : 0ull;
+        sort_desc64<8>(k64);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < E && !((taken >> i) & 1u) && (be < 0 || key[i] > bk)) {
-                    be = i;
-                    bk = key[i];
-                    bp = pr[i];
-                }
-            if (be >= 0) taken |= 1u << be;  // nc <= E: always
-            id[j] = be < 0 ? 0 : be;
-            pj[j] = bp;
-            if (j < rs.k) psum += bp;
+        for (int j = 0; j < 8; ++j) {
+            id[j] = (int)(~(unsigned)k64[j]) & 7;
+            pj[j] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i == id[j]) pj[j] = pr[i];
+        }
+    } else {
+        // repeated arg-max; a strict > keeps the lower index among equal keys
+        unsigned taken = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            id[j] = 0;
+            pj[j] = 0.f;
+            if (j < rs.nc) {
+                int be = -1;
+                unsigned bk = 0u;
+                float bp = 0.f;
+#pragma unroll
+                for (int i = 0; i < EMAX; ++i)
+                    if (i < E && !((taken >> i) & 1u) && (be < 0 || key[i] > bk)) {
+                        be = i;
+                        bk = key[i];
+                        bp = pr[i];
+                    }
+                if (be >= 0) taken |= 1u << be;  // nc <= E: always
+                id[j] = be < 0 ? 0 : be;
+                pj[j] = bp;
+            }
         }
     }
-    const bool aux = rs.acc_mem != nullptr;
+    float psum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (j < rs.k) psum += pj[j];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         if (j < rs.nc) {
@@ -770,33 +804,66 @@ __device__ __forceinline__ void router_select_rows(const RouterSel& rs, const fl
             }
         }
     }
-    if (!aux) return;
+    if (rs.acc_mem == nullptr) return;
     const AuxAcc acc = aux_acc_at(rs.acc_mem, E, kAuxGroups);
     const size_t g = (size_t)(blockIdx.x % acc.groups) * E;
-    for (int e = 0; e < E; ++e) {
-        float pe = 0.f;
-        unsigned long long ie = 0ull;
-        unsigned ce = 0u;
+    if constexpr (EMAX == 8) {
+        // the warp's 32 x 8 probabilities and its gate and count sums per
+        // expert in its staging area (free once the logits are out); lane e
+        // then adds expert e's column in row order
+        float* cs = stg;                                                // [8][33]
+        unsigned long long* si = reinterpret_cast<unsigned long long*>(stg + 264);  // [8]
+        unsigned* sc = reinterpret_cast<unsigned*>(stg + 280);          // [8]
+        if (lane < 8) {
+            si[lane] = 0ull;
+            sc[lane] = 0u;
+        }
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i == e) pe = valid ? pr[i] : 0.f;
+        for (int e = 0; e < 8; ++e) cs[e * 33 + lane] = valid ? pr[e] : 0.f;
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            if (valid && j < rs.k && id[j] == e) {
-                ie += to_fix(pj[j]);
-                ++ce;
+            if (valid && j < rs.k) {
+                atomicAdd(&si[id[j]], to_fix(pj[j]));
+                atomicAdd(&sc[id[j]], 1u);
             }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            pe += __shfl_xor_sync(0xffffffffu, pe, o);
-            ie += __shfl_xor_sync(0xffffffffu, ie, o);
-        }
-        ce = __reduce_add_sync(0xffffffffu, ce);
-        if (lane == 0) {
+        __syncwarp();
+        if (lane < E) {
+            float pe = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) pe += cs[lane * 33 + r];
             const unsigned long long pf = to_fix(pe);
-            if (pf) atomicAdd(&acc.P[g + e], pf);
-            if (ie) atomicAdd(&acc.I[g + e], ie);
-            if (ce) atomicAdd(&acc.cnt[g + e], ce);
+            if (pf) atomicAdd(&acc.P[g + lane], pf);
+            if (si[lane]) atomicAdd(&acc.I[g + lane], si[lane]);
+            if (sc[lane]) atomicAdd(&acc.cnt[g + lane], sc[lane]);
+        }
+        __syncwarp();
+    } else {
+        for (int e = 0; e < E; ++e) {
+            float pe = 0.f;
+            unsigned long long ie = 0ull;
+            unsigned ce = 0u;
+#pragma unroll
+            for (int i = 0; i < EMAX; ++i)
+                if (i == e) pe = valid ? pr[i] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (valid && j < rs.k && id[j] == e) {
+                    ie += to_fix(pj[j]);
+                    ++ce;
+                }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                pe += __shfl_xor_sync(0xffffffffu, pe, o);
+                ie += __shfl_xor_sync(0xffffffffu, ie, o);
+            }
+            ce = __reduce_add_sync(0xffffffffu, ce);
+            if (lane == 0) {
+                const unsigned long long pf = to_fix(pe);
+                if (pf) atomicAdd(&acc.P[g + e], pf);
+                if (ie) atomicAdd(&acc.I[g + e], ie);
+                if (ce) atomicAdd(&acc.cnt[g + e], ce);
+            }
         }
     }
 }
@@ -1087,8 +1154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (args.rs.on) {
                         float v[32];
                         tmem_ld32(taddr, v);
-                        router_select_rows(args.rs, args.offset, E_r, gt.out_row + row,
-                                           row < rows_here + 32 * q, v, p.status);
+                        const bool tv = row < rows_here + 32 * q;
+                        if (E_r <= 8)
+                            router_select_rows<8>(args.rs, args.offset, E_r, gt.out_row + row, tv,
+                                                  v, stg, p.status);
+                        else
+                            router_select_rows<32>(args.rs, args.offset, E_r, gt.out_row + row,
+                                                   tv, v, stg, p.status);
                     }
                 }
             } else {

@@ -337,6 +337,29 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 // ------------------------------------------------------------ device helpers
+// Sorts N (a power of two, at most 8) 64-bit keys into descending order with
+// a bitonic network of compile-time compare-exchanges (registers only).
+template <int N>
+__device__ __forceinline__ void sort_desc64(unsigned long long (&k)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    // within each bitonic block of `size`, the first half of
+                    // the blocks sorts descending, the second ascending
+                    const bool desc = ((i & size) == 0) || size == N;
+                    const unsigned long long hi = k[i] > k[j] ? k[i] : k[j];
+                    const unsigned long long lo = k[i] > k[j] ? k[j] : k[i];
+                    k[i] = desc ? hi : lo;
+                    k[j] = desc ? lo : hi;
+                }
+            }
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

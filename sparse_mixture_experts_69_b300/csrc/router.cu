@@ -260,29 +260,6 @@ __device__ __forceinline__ void draw_token_eps(const SelectArgs& a, int t, Token
     }
 }
 
-// Sorts N (a power of two, at most 8) 64-bit keys into descending order with
-// a bitonic network of compile-time compare-exchanges (registers only).
-template <int N>
-__device__ __forceinline__ void sort_desc64(unsigned long long (&k)[N]) {
-#pragma unroll
-    for (int size = 2; size <= N; size <<= 1)
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    // within each bitonic block of `size`, the first half of
-                    // the blocks sorts descending, the second ascending
-                    const bool desc = ((i & size) == 0) || size == N;
-                    const unsigned long long hi = k[i] > k[j] ? k[i] : k[j];
-                    const unsigned long long lo = k[i] > k[j] ? k[j] : k[i];
-                    k[i] = desc ? hi : lo;
-                    k[j] = desc ? lo : hi;
-                }
-            }
-}
-
 // Selection for token t from its loaded inputs. On return pr[] holds this
 // lane's probabilities (also stored to sp[0..E), the warp's row of shared
 // memory, when sp is not NULL; E <= 256 needs it), and lanes j < nc hold the
