@@ -695,11 +695,27 @@ __device__ __forceinline__ unsigned sel_key(float v) {
     const unsigned b = __float_as_uint(__fadd_rn(v, 0.f));
     return b ^ ((b >> 31) ? 0xFFFFFFFFu : 0x80000000u);
 }
+// Row t of a [T, E] fp32 output from a thread's registers: two 16-byte
+// stores when E = 8 and the base is 16-byte aligned, else E scalar stores.
+template <int EMAX>
+__device__ __forceinline__ void store_row(float* base, int E, int t, const float (&x)[EMAX]) {
+    float* dst = base + (size_t)t * E;
+    if (EMAX == 8 && E == 8 && (reinterpret_cast<uintptr_t>(base) & 15) == 0) {
+        reinterpret_cast<float4*>(dst)[0] = make_float4(x[0], x[1], x[2], x[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(x[4], x[5], x[6], x[7]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < EMAX; ++i)
+            if (i < E) dst[i] = x[i];
+    }
+}
+
+// logits: NULL when the caller has written them, else the [T, E] output.
 template <int EMAX>
 __device__ __forceinline__ void router_select_rows(const RouterSel rs, const float* offset,
                                                    int E, int t, bool valid,
-                                                   const float (&v)[32], float* stg,
-                                                   int* status) {
+                                                   const float (&v)[32], float* logits,
+                                                   float* stg, int* status) {
     const int lane = threadIdx.x & 31;
     float h[EMAX], pr[EMAX];
     bool nonfinite = false;
@@ -731,18 +747,21 @@ __device__ __forceinline__ void router_select_rows(const RouterSel rs, const flo
         for (int i = 0; i < w; ++i) red[i] += red[i + w];
     const float inv = __frcp_rn(red[0]);
     unsigned key[EMAX];
+    float sc[EMAX];
 #pragma unroll
     for (int i = 0; i < EMAX; ++i) {
         key[i] = 0u;
+        sc[i] = 0.f;
         if (i < E) {
             pr[i] = pr[i] * inv;
-            const float sc = rs.bias ? pr[i] + rs.bias[i] : h[i];
-            key[i] = sel_key(sc);
-            if (valid) {
-                rs.probs[(size_t)t * E + i] = pr[i];
-                if (rs.sel) rs.sel[(size_t)t * E + i] = sc;
-            }
+            sc[i] = rs.bias ? pr[i] + rs.bias[i] : h[i];
+            key[i] = sel_key(sc[i]);
         }
+    }
+    if (valid) {
+        if (logits) store_row<EMAX>(logits, E, t, h);
+        store_row<EMAX>(rs.probs, E, t, pr);
+        if (rs.sel) store_row<EMAX>(rs.sel, E, t, sc);
     }
     if (__any_sync(0xffffffffu, valid && nonfinite) && lane == 0) flag_status(status, DEV_NONFINITE);
     int id[8];
@@ -1127,8 +1146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* stg = staging + q * 32 * 33;
                 const int rows_here = min(32, min(gt.rows, TM) - 32 * q);
                 const int E_r = args.E_router;
+                // at most 8 experts selected here: the selection writes the logits
+                const int c_end = (BN == 32 && args.rs.on && E_r <= 8) ? 0 : BN;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = 0; c < c_end; c += 32) {
                     float v[32];
                     tmem_ld32(taddr + c, v);
 #pragma unroll
@@ -1157,10 +1178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool tv = row < rows_here + 32 * q;
                         if (E_r <= 8)
                             router_select_rows<8>(args.rs, args.offset, E_r, gt.out_row + row, tv,
-                                                  v, stg, p.status);
+                                                  v, args.logits, stg, p.status);
                         else
                             router_select_rows<32>(args.rs, args.offset, E_r, gt.out_row + row,
-                                                   tv, v, stg, p.status);
+                                                   tv, v, nullptr, stg, p.status);
                     }
                 }
             } else {
