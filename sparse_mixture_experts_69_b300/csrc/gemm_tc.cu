@@ -82,9 +82,11 @@ struct RouterSel {
     int32_t* blk_hist;  // [E][nblk_cap] or NULL
     int nblk_cap;
     void* acc_mem;      // statistics accumulators (aux_common.cuh) or NULL
-    // 1: no early pdl_trigger, so the next kernel launches only when this one
-    // is complete (no selection kernel follows to order the next router
-    // weight copy after this GEMM's reads)
+    // 1: no pdl_trigger at the start. No selection kernel follows to order the
+    // next router-weight copy after this GEMM's reads of the copy, so each
+    // CTA signals only once its last accumulator is complete (every copy it
+    // issued has landed), from one epilogue thread; the next kernel may then
+    // overwrite the weight copy during the epilogue
     int late_trigger;
 };
 
@@ -1133,6 +1135,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tph = (local >> 1) & 1;
             if (!mbar_wait(&tfull[b], tph, abort_flag, p.status, args.wait_ns)) break;
             tc_fence_after();
+            if (EPI == EPI_ROUTER && args.rs.late_trigger && w + (int)gridDim.x >= total &&
+                threadIdx.x == 64)
+                pdl_trigger();  // this CTA's last accumulator: its reads are all done
             const uint32_t taddr = tmem_base + (uint32_t)(b * BN) + ((uint32_t)(32 * q) << 16);
             // M=64 tiles: accumulator row r is in TMEM lane 32 (r / 16) + r % 16,
             // so lanes 0..15 of each lane quadrant hold 16 rows and 16..31 none

@@ -121,7 +121,8 @@ struct RouterSelOut {
     float* w;           // [T,nc]
     int32_t* blk_hist;  // capacity histogram or NULL
     void* acc_mem;      // statistics accumulators or NULL
-    int late_trigger;   // 1 when no kernel of the call follows (moe_route)
+    int late_trigger;   // 1 when no kernel of the call follows (moe_route): signal
+                        // dependents only after the last accumulator
 };
 bool router_sel_in_gemm(const Shape& s, bool noisy);
 cudaError_t launch_router_gemm_bf16(const Shape& s, int Nr, const void* x, const void* wgT,
@@ -313,8 +314,10 @@ int hold_first_accumulator();
 //    pdl_wait(): the selection kernels (the router GEMM before them is then
 //    complete), the permute and gather kernels (the capacity or selection
 //    kernel that wrote the offsets is then complete) and the tcgen05 GEMM;
-//    a router GEMM that selects itself and ends moe_route does not trigger
-//    at all, so the next call's weight copy launches after it is complete.
+//    a router GEMM that selects itself and ends moe_route triggers in each
+//    CTA only once that CTA's last accumulator is complete (all its copies of
+//    the router weights have landed), so the next call's weight copy cannot
+//    overwrite them while they are read.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
