@@ -414,7 +414,7 @@ constexpr int kSelWarps = 8;
 
 // Standalone selection.
 template <int EPL, bool PARTS>
-__global__ void __launch_bounds__(32 * kSelWarps, EPL <= 8 ? 4 : 1) router_select_kernel(SelectArgs a) {
+__global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 4 : EPL == 8 ? 5 : 1) router_select_kernel(SelectArgs a) {
     const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
     TokenRegs<EPL> r;
     if (a.draw && t < a.T) draw_token_eps<EPL>(a, t, r);
@@ -472,7 +472,7 @@ cudaError_t launch_router_select(const Shape& s, const RouterLogits& rl, float* 
 // For E <= 128, 32 registers a thread (eight blocks an SM) keep every warp of a
 // T = 8192 grid resident at once.
 template <int EPL, bool PARTS>
-__global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : EPL == 8 ? 4 : 1) router_select_fused_kernel(
+__global__ void __launch_bounds__(32 * kSelWarps, EPL <= 4 ? 8 : EPL == 8 ? 5 : 1) router_select_fused_kernel(
     SelectArgs a, int32_t* blk_hist, int nblk_cap, AuxAcc acc, AuxOut out, int defer_final) {
     const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
     TokenRegs<EPL> r;
